@@ -1,0 +1,125 @@
+"""Build and read the paged NVFP4 cache and FP8 windows of a workload (oracle side).
+
+Test infrastructure.  Quantizes the seeded float32 rows of ``workloads`` with
+``formats`` and places the bytes with ``layout``; reads them back as float64
+dequantized values.  Used to give the CUDA path its input bytes in parity tests
+and to compute expected outputs; it never reads anything the CUDA path wrote.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import workloads as W
+from . import formats as F
+from . import layout as LY
+from . import attention as A
+
+
+class Pools:
+    """K/V (or index-key) pools of one cache: uint8 [num_pages][bytes per page]."""
+
+    def __init__(self, num_pages: int, d: int, kind: str):
+        self.d = d
+        self.kind = kind  # "k" (K-layout) or "v" (V-layout)
+        self.data = np.zeros((num_pages, LY.k_data_bytes(d)), np.uint8)
+        self.scale = np.zeros((num_pages, LY.k_scale_bytes(d)), np.uint8)
+
+    def store(self, page, slots, codes, scales):
+        f = LY.store_k_page if self.kind == "k" else LY.store_v_page
+        f(self.data, self.scale, page, slots, codes, scales)
+
+    def load(self, page):
+        f = LY.load_k_page if self.kind == "k" else LY.load_v_page
+        return f(self.data, self.scale, page, self.d)
+
+
+def tensor_scales(wl: W.Workload, sample_pages: int = 64):
+    """FP32 tensor scales fixed at fill.  The amax is taken over the whole
+    distribution's reach: N(0,1) x8 outliers; to keep a full-size fill and a
+    page-sampled oracle consistent, the scale is derived from a fixed bound
+    (|x| <= 8 * 6 sigma) rather than from the drawn data: ts = fp32(48 / 2688)."""
+    ts = F.F32(F.F32(48.0) / F.F32(2688.0))
+    tw = F.F32(F.F32(48.0) / F.F32(448.0))
+    return ts, tw
+
+
+def quantize_rows_nvfp4(rows, ts):
+    return F.nvfp4_quantize(rows, ts)
+
+
+def fill_pages(wl: W.Workload, ts_k, ts_v, pages=None):
+    """Quantize and store the filled tokens of ``wl`` into fresh K and V pools.
+    ``pages``: optional set of physical pages to fill (others stay zero)."""
+    Kp = Pools(wl.num_pages, wl.d, "k")
+    Vp = Pools(wl.num_pages, wl.d, "v")
+    for (b, t0, t1) in wl.fill_segments():
+        for j in range(t0 // W.PAGE, (t1 + W.PAGE - 1) // W.PAGE):
+            p = int(wl.page_table[b, j])
+            if pages is not None and p not in pages:
+                continue
+            lo = max(t0, j * W.PAGE) - j * W.PAGE
+            hi = min(t1, (j + 1) * W.PAGE) - j * W.PAGE
+            slots = np.arange(lo, hi)
+            for pool, tens, ts in ((Kp, W.T_K, ts_k), (Vp, W.T_V, ts_v)):
+                rows = wl.page_rows(tens, p)[lo:hi]
+                c, s = F.nvfp4_quantize(rows, ts)
+                pool.store(p, slots, c, s)
+    return Kp, Vp
+
+
+def append_tokens(wl: W.Workload, Kp: Pools, Vp: Pools, krows, vrows, seq_idx, pos, ts_k, ts_v):
+    """Quantize and write tokens (krows/vrows [n][d]) at (seq_idx[i], pos[i])."""
+    for i in range(len(seq_idx)):
+        b, t = int(seq_idx[i]), int(pos[i])
+        p = int(wl.page_table[b, t // W.PAGE])
+        for pool, rows, ts in ((Kp, krows, ts_k), (Vp, vrows, ts_v)):
+            c, s = F.nvfp4_quantize(rows[i:i + 1], ts)
+            pool.store(p, np.array([t % W.PAGE]), c, s)
+
+
+def dequant_seq(wl: W.Workload, pool: Pools, ts, b: int, n_tok: int) -> np.ndarray:
+    """float64 [n_tok][d] dequantized tokens [0, n_tok) of sequence b."""
+    out = np.empty((n_tok, pool.d))
+    for j in range((n_tok + W.PAGE - 1) // W.PAGE):
+        p = int(wl.page_table[b, j])
+        c, s = pool.load(p)
+        x = F.nvfp4_dequantize(c, s, ts)
+        n = min(W.PAGE, n_tok - j * W.PAGE)
+        out[j * W.PAGE:j * W.PAGE + n] = x[:n]
+    return out
+
+
+def dequant_tokens(wl: W.Workload, pool: Pools, ts, b: int, idx) -> np.ndarray:
+    """float64 [len(idx)][d] dequantized tokens ``idx`` of sequence b."""
+    out = np.empty((len(idx), pool.d))
+    cache = {}
+    for i, t in enumerate(idx):
+        p = int(wl.page_table[b, int(t) // W.PAGE])
+        if p not in cache:
+            c, s = pool.load(p)
+            cache[p] = F.nvfp4_dequantize(c, s, ts)
+        out[i] = cache[p][int(t) % W.PAGE]
+    return out
+
+
+def window_codes(wl: W.Workload, tw_k, tw_v, b: int):
+    """FP8 codes [128][d] of the window K and V of sequence b."""
+    return (F.fp8_quantize(wl.window_rows(W.T_KW, b), tw_k),
+            F.fp8_quantize(wl.window_rows(W.T_VW, b), tw_v))
+
+
+def expected_decode(wl: W.Workload, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b: int, heads=None, scale=None):
+    """Oracle decode of sequence b (all or some heads): global [0, L_b) + window [0, win_len_b)."""
+    d = wl.d
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    L = int(wl.seq_len[b])
+    K = dequant_seq(wl, Kp, ts_k, b, L)
+    V = dequant_seq(wl, Vp, ts_v, b, L)
+    kw, vw = window_codes(wl, tw_k, tw_v, b)
+    n = int(wl.win_len[b])
+    Kw = F.fp8_dequantize(kw[:n], tw_k)
+    Vw = F.fp8_dequantize(vw[:n], tw_v)
+    q = F.bf16_to_f64(wl.q_bits_seq(b))
+    if heads is not None:
+        q = q[heads]
+    return A.decode(q, K, V, Kw, Vw, scale)

@@ -1,0 +1,168 @@
+"""Byte layout of one 64-token page of the NVFP4 cache (oracle; test infrastructure).
+
+The pages fix only that the global KV is stored in FP4 and paged ([blog]
+"SWA bounded replay": compressed, shared across layers, FP4); the byte layout is
+this library's definition, chosen so that a 64-token page is a few contiguous
+runs of bytes.  Written out here address by address:
+
+K-layout (K and the 128-wide index keys), d channels, s = min(8, d/32) - 1:
+  data  [64 tokens][d/2 bytes]: channel pair (2j, 2j+1) of token t sits in
+        byte   t*(d/2) + 16*((j div 16) XOR (t AND s)) + (j mod 16),
+        channel 2j in the low nibble, 2j+1 in the high nibble.
+  scale [d/128 groups][64 tokens][8 bytes]: the scale of block j (channels
+        16j..16j+15) of token t sits in byte ((j div 8)*64 + t)*8 + (j mod 8).
+V-layout (V), d channels:
+  data  [8 octets][d channels][4 bytes]: channel ch of token t is nibble
+        (t mod 8) of the little-endian 32-bit word ((t div 8)*d + ch), i.e.
+        byte 4*((t div 8)*d + ch) + (t mod 8) div 2, low nibble for even t.
+  scale [d/16 blocks][64 tokens]: block j of token t sits in byte j*64 + t.
+Each pool is an array [num_pages][bytes per page] of uint8.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+PAGE = 64
+
+
+def k_data_bytes(d: int) -> int:
+    return PAGE * d // 2
+
+
+def k_scale_bytes(d: int) -> int:
+    return PAGE * d // 16
+
+
+v_data_bytes = k_data_bytes
+v_scale_bytes = k_scale_bytes
+
+
+def _k_data_addr(t: int, j: int, d: int) -> int:
+    s = min(8, d // 32) - 1
+    return t * (d // 2) + 16 * ((j // 16) ^ (t & s)) + (j % 16)
+
+
+def _k_scale_addr(t: int, j: int) -> int:
+    return ((j // 8) * PAGE + t) * 8 + (j % 8)
+
+
+def _v_data_addr(t: int, ch: int, d: int) -> tuple:
+    return 4 * ((t // 8) * d + ch) + (t % 8) // 2, (t % 2)
+
+
+def _v_scale_addr(t: int, j: int) -> int:
+    return j * PAGE + t
+
+
+def store_k_token(data_pool, scale_pool, page, t, codes, scales):
+    """Write one token's NVFP4 codes [d] (0..15) and scale bytes [d/16] into page ``page``, slot ``t``."""
+    d = len(codes)
+    for j in range(d // 2):
+        data_pool[page, _k_data_addr(t, j, d)] = (int(codes[2 * j]) & 0xF) | ((int(codes[2 * j + 1]) & 0xF) << 4)
+    for j in range(d // 16):
+        scale_pool[page, _k_scale_addr(t, j)] = scales[j]
+
+
+def load_k_token(data_pool, scale_pool, page, t, d):
+    codes = np.empty(d, np.uint8)
+    for j in range(d // 2):
+        b = int(data_pool[page, _k_data_addr(t, j, d)])
+        codes[2 * j] = b & 0xF
+        codes[2 * j + 1] = b >> 4
+    scales = np.array([scale_pool[page, _k_scale_addr(t, j)] for j in range(d // 16)], np.uint8)
+    return codes, scales
+
+
+def store_v_token(data_pool, scale_pool, page, t, codes, scales):
+    d = len(codes)
+    for ch in range(d):
+        a, hi = _v_data_addr(t, ch, d)
+        old = int(data_pool[page, a])
+        c = int(codes[ch]) & 0xF
+        data_pool[page, a] = (old & 0x0F) | (c << 4) if hi else (old & 0xF0) | c
+    for j in range(d // 16):
+        scale_pool[page, _v_scale_addr(t, j)] = scales[j]
+
+
+def load_v_token(data_pool, scale_pool, page, t, d):
+    codes = np.empty(d, np.uint8)
+    for ch in range(d):
+        a, hi = _v_data_addr(t, ch, d)
+        b = int(data_pool[page, a])
+        codes[ch] = (b >> 4) if hi else (b & 0xF)
+    scales = np.array([scale_pool[page, _v_scale_addr(t, j)] for j in range(d // 16)], np.uint8)
+    return codes, scales
+
+
+# ---- vectorized forms of the same formulas (used on whole pages) -------------
+
+def k_data_index(d: int) -> np.ndarray:
+    """[64][d/2] byte address of channel pair j of token t (formula above)."""
+    t = np.arange(PAGE)[:, None]
+    j = np.arange(d // 2)[None, :]
+    s = min(8, d // 32) - 1
+    return t * (d // 2) + 16 * ((j // 16) ^ (t & s)) + (j % 16)
+
+
+def k_scale_index(d: int) -> np.ndarray:
+    t = np.arange(PAGE)[:, None]
+    j = np.arange(d // 16)[None, :]
+    return ((j // 8) * PAGE + t) * 8 + (j % 8)
+
+
+def v_data_index(d: int) -> tuple:
+    """([64][d] byte address, [64][d] high-nibble flag) of channel ch of token t."""
+    t = np.arange(PAGE)[:, None]
+    ch = np.arange(d)[None, :]
+    return 4 * ((t // 8) * d + ch) + (t % 8) // 2, np.broadcast_to(t % 2 == 1, (PAGE, d))
+
+
+def v_scale_index(d: int) -> np.ndarray:
+    t = np.arange(PAGE)[:, None]
+    j = np.arange(d // 16)[None, :]
+    return j * PAGE + t
+
+
+def store_k_page(data_pool, scale_pool, page, slots, codes, scales):
+    """Write tokens at ``slots`` of page ``page``: codes [n][d], scales [n][d/16]."""
+    d = codes.shape[1]
+    slots = np.asarray(slots)
+    packed = (codes[:, 0::2] & 0xF) | ((codes[:, 1::2] & 0xF) << 4)
+    data_pool[page, k_data_index(d)[slots]] = packed.astype(np.uint8)
+    scale_pool[page, k_scale_index(d)[slots]] = scales
+
+
+def load_k_page(data_pool, scale_pool, page, d):
+    """codes [64][d], scales [64][d/16] of a whole page."""
+    b = data_pool[page][k_data_index(d)]
+    codes = np.empty((PAGE, d), np.uint8)
+    codes[:, 0::2] = b & 0xF
+    codes[:, 1::2] = b >> 4
+    return codes, scale_pool[page][k_scale_index(d)]
+
+
+def store_v_page(data_pool, scale_pool, page, slots, codes, scales):
+    d = codes.shape[1]
+    slots = np.asarray(slots)
+    addr, hi = v_data_index(d)
+    a = addr[slots]
+    h = hi[slots]
+    c = (codes & 0xF).astype(np.uint8)
+    # the two tokens of one byte (slots 2i, 2i+1) may arrive in one call:
+    # write even slots, then odd slots, so no byte is read-modify-written twice at once
+    ev = (slots % 2 == 0)
+    for sel in (ev, ~ev):
+        if sel.any():
+            aa = a[sel]
+            oo = data_pool[page, aa]
+            cc = c[sel]
+            hh = h[sel]
+            data_pool[page, aa] = np.where(hh, (oo & 0x0F) | (cc << 4), (oo & 0xF0) | cc).astype(np.uint8)
+    scale_pool[page, v_scale_index(d)[slots]] = scales
+
+
+def load_v_page(data_pool, scale_pool, page, d):
+    addr, hi = v_data_index(d)
+    b = data_pool[page][addr]
+    codes = np.where(hi, b >> 4, b & 0xF).astype(np.uint8)
+    return codes, scale_pool[page][v_scale_index(d)]

@@ -1,0 +1,140 @@
+"""Pins of the oracle's E2M1 / E4M3 tables and NVFP4 / FP8 encoders.
+
+Each check is independent of the oracle's own code: literal value lists typed
+from the OCP definitions, hand-worked blocks under tests/golden, an
+independent library (ml_dtypes, when installed), closed-form error bounds and
+idempotence.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from conftest import golden_lines
+from oracle import formats as F
+
+# OCP MX v1.0, FP4 E2M1 element values for codes 0..15 (sign bit = bit 3)
+E2M1_OCP = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+            -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_e2m1_table_matches_ocp_list():
+    for c in range(16):
+        assert F.E2M1[c] == E2M1_OCP[c]
+        assert math.copysign(1.0, F.E2M1[c]) == math.copysign(1.0, E2M1_OCP[c])
+
+
+def test_e4m3_table_landmarks():
+    # OCP OFP8 E4M3: a few values every implementation must agree on
+    landmarks = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+                 0x38: 1.0, 0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0,
+                 0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0, 0x77: 240.0, 0x30: 0.5}
+    for c, v in landmarks.items():
+        assert F.E4M3[c] == v, hex(c)
+    assert math.isnan(F.E4M3[0x7F]) and math.isnan(F.E4M3[0xFF])
+    assert np.isfinite(F.E4M3[np.r_[0:0x7F, 0x80:0xFF]]).all()
+    # monotone in code on the positive half, symmetric in sign
+    pos = F.E4M3[:0x7F]
+    assert (np.diff(pos) > 0).all()
+    assert (F.E4M3[0x80:0xFF] == -pos).all()
+
+
+def test_tables_match_ml_dtypes():
+    ml = pytest.importorskip("ml_dtypes")
+    e4 = np.arange(256, dtype=np.uint8).view(ml.float8_e4m3fn).astype(np.float64)
+    fin = np.isfinite(e4)
+    assert (fin == np.isfinite(F.E4M3)).all()
+    assert (e4[fin] == F.E4M3[fin]).all()
+    e2 = np.arange(16, dtype=np.uint8).view(ml.float4_e2m1fn).astype(np.float64)
+    assert (e2 == F.E2M1).all()
+
+
+def test_e2m1_tie_table():
+    # magnitude -> code under ties-to-even (worked from the grid)
+    cases = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6,
+             0.26: 1, 0.74: 1, 0.76: 2, 4.9: 6, 5.1: 7, 6.0: 7, 7.0: 7, 1e9: 7,
+             0.0: 0, 0.24: 0}
+    for v, c in cases.items():
+        assert int(F.e2m1_encode(np.float32(v))) == c, v
+        assert int(F.e2m1_encode(np.float32(-v))) == c | 8, -v
+
+
+def test_e4m3_rounding_golden():
+    for line in golden_lines("e4m3_rounding_cases.txt"):
+        x, code = line.split()
+        assert int(F.e4m3_encode(np.float32(float(x)))) == int(code, 16), line
+
+
+def test_encoders_match_ml_dtypes_in_range():
+    ml = pytest.importorskip("ml_dtypes")
+    g = np.random.default_rng(1)
+    x = np.concatenate([g.standard_normal(20000).astype(np.float32) * 50,
+                        g.standard_normal(2000).astype(np.float32) * 1e-3])
+    x = x[np.abs(x) <= 448]
+    ref = x.astype(ml.float8_e4m3fn).view(np.uint8)
+    assert (F.e4m3_encode(x) == ref).all()
+    v = (g.standard_normal(20000) * 2).astype(np.float32)
+    v = v[np.abs(v) <= 6]
+    ref4 = v.astype(ml.float4_e2m1fn).astype(np.float64)
+    assert (F.E2M1[F.e2m1_encode(v)] == ref4).all()
+
+
+def test_nvfp4_worked_blocks():
+    for line in golden_lines("nvfp4_worked_blocks.txt"):
+        ts, xs, sc, cs = [p.strip() for p in line.split(";")]
+        x = np.array([float(v) for v in xs.split()], np.float32)
+        c, s = F.nvfp4_quantize(x, np.float32(float(ts)))
+        assert int(s[0]) == int(sc, 16), line
+        assert [int(v) for v in c] == [int(v, 16) for v in cs.split()], line
+
+
+def test_nvfp4_error_bound_and_zero_blocks():
+    g = np.random.default_rng(2)
+    x = (g.standard_normal((4000, 64)) * g.choice([0.01, 1, 8, 40], (4000, 1))).astype(np.float32)
+    x[7] = 0.0
+    ts = np.float32(48.0 / 2688.0)
+    c, s = F.nvfp4_quantize(x, ts)
+    xh = F.nvfp4_dequantize(c, s, ts)
+    assert (c[7] == 0).all() and (s[7] == 0).all()
+    blk = x.reshape(4000, 4, 16).astype(np.float64)
+    den = (F.E4M3[s] * np.float64(ts))[..., None]
+    v = np.abs(blk) / np.where(den > 0, den, 1)
+    step = np.where(v < 2, 0.5, np.where(v < 4, 1.0, 2.0))
+    bound = np.where(v < 6, 0.5 * step * den, np.abs(blk) - 6 * den) + 1e-6 * np.abs(blk) + 1e-30
+    err = np.abs(blk - xh.reshape(blk.shape))
+    assert (err <= bound).all()
+    # the block scale makes the largest element land near the top of the grid
+    # (E4M3 keeps 3 mantissa bits: relative rounding <= 1/16 when the scale is normal)
+    amax = np.abs(blk).max(-1)
+    nz = (F.E4M3[s] >= 2.0 ** -6) & (amax <= 6 * 448 * np.float64(ts))   # normal, unsaturated scale
+    assert (np.abs(amax[nz] / (F.E4M3[s][nz] * np.float64(ts)) - 6) <= 6 / (1 - 1 / 16) - 6 + 1e-9).all()
+
+
+def test_nvfp4_idempotent_on_grid_values():
+    # dequantized values re-quantize to the same bytes (same tensor scale)
+    g = np.random.default_rng(3)
+    x = (g.standard_normal((500, 32)) * 3).astype(np.float32)
+    ts = np.float32(0.01)
+    c, s = F.nvfp4_quantize(x, ts)
+    xh = F.nvfp4_dequantize(c, s, ts).astype(np.float32)
+    c2, s2 = F.nvfp4_quantize(xh, ts)
+    # -0 codes of elements that dequantize to 0 may lose their sign: compare magnitudes there
+    same = (c2 == c) | ((c & 7) == 0) & ((c2 & 7) == 0)
+    assert same.all() and (s2 == s).all()
+
+
+def test_fp8_quantize_roundtrip():
+    g = np.random.default_rng(4)
+    x = (g.standard_normal(10000) * 4).astype(np.float32)
+    tw = np.float32(np.abs(x).max() / np.float32(448))
+    c = F.fp8_quantize(x, tw)
+    xh = F.fp8_dequantize(c, tw)
+    rel = np.abs(xh - x) / np.maximum(np.abs(x), 2.0 ** -6 * float(tw))
+    assert rel.max() <= 2.0 ** -4 + 1e-6      # half an ulp of a 3-bit mantissa
+
+
+def test_rejects_nonfinite():
+    with pytest.raises(ValueError):
+        F.e4m3_encode(np.float32(np.inf))
+    with pytest.raises(ValueError):
+        F.nvfp4_quantize(np.zeros(16, np.float32), np.float32(0.0))
