@@ -1,0 +1,207 @@
+/*
+ * pkv.h - C ABI of the GB300 (sm_103a) decode-attention library for a paged
+ * NVFP4 global KV cache plus an FP8 sliding window.
+ *
+ * What the calls compute (sources: the vLLM blog "DeepSeek-V4.1-Flash sur
+ * vLLM : 5x de débit agentique dès le jour 0" - sections "SWA bounded replay",
+ * "Côté encodeur : reconstruire la fenêtre lors d'un hit de cache", "Kernels"
+ * paragraphs "Logits MQA creux" and "MegaAttention avec KV compressé NVFP4",
+ * "Performances agentiques"; and the cocoloop summary, section "Les
+ * particularités du modèle lui-même"):
+ *   - the global KV is compressed, shared by every query head (MQA over one
+ *     latent) and stored in FP4 (NVFP4 here: E2M1 values, one E4M3 scale per
+ *     16 consecutive channels of a token, one FP32 scale per tensor), in
+ *     64-token pages reached through a page table;
+ *   - a sliding window of the last 128 positions is kept uncompressed in FP8
+ *     (E4M3, one FP32 scale per tensor);
+ *   - decode attention = softmax over the global tokens plus the window entries;
+ *   - sparse MQA logits: an index score per position picks the top-k positions
+ *     that decode attention then reads;
+ *   - bounded replay: after a prefix hit of length H the 128 tokens [H-128, H)
+ *     are re-run with the window clipped at s = H-128.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *     aligned, on the device the context was created on.  Nothing is freed or
+ *     retained by the library after a call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous on that stream; host-side validation happens
+ *     before any launch and returns PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED
+ *     without launching anything.
+ *   - Faults found on the device (a page id outside [0, num_pages), a sequence
+ *     longer than its page table) never trap: the kernel skips the access,
+ *     records a code in the context's device error word and finishes.
+ *     pkv_get_error() synchronizes the stream and returns/clears it.
+ *   - A context is not thread-safe; use one per host thread / stream.
+ *   - Nothing here allocates device memory per call: scratch comes from the
+ *     caller through (ws, ws_bytes); pkv_workspace_bytes() gives the size.
+ *
+ * Cache byte layout (one 64-token page; d = head dim, multiple of 128, <= 512):
+ *   K-layout (K, index keys):
+ *     data  [64][d/2]: channel pair (2j,2j+1) of token t at byte
+ *           t*(d/2) + 16*((j/16) ^ (t & s)) + j%16, s = min(8, d/32)-1,
+ *           channel 2j in the low nibble;
+ *     scale [d/128][64][8]: block j of token t at ((j/8)*64 + t)*8 + j%8.
+ *   V-layout (V):
+ *     data  [8][d][4]: channel c of token t is nibble t%8 of the little-endian
+ *           32-bit word (t/8)*d + c;
+ *     scale [d/16][64]: block j of token t at j*64 + t.
+ *   Window: FP8 codes [B][128][d], row-major.  Queries: bf16 [.][H][d].
+ *   Outputs: O float32 [.][H][d], LSE float32 [.][H] (natural log; -inf and
+ *   O = 0 for an empty entry set).
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, k > limit ... */
+  PKV_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels implement */
+  PKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  PKV_ERR_BAD_PAGE = 4,      /* device: page id out of range / length beyond page table */
+  PKV_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up */
+  PKV_ERR_WORKSPACE = 6      /* ws_bytes smaller than pkv_workspace_bytes() */
+} pkv_status;
+
+typedef struct pkv_ctx pkv_ctx;
+
+/* Shapes fixed for the life of a context. */
+typedef struct {
+  int d;              /* head dim of K, V and Q (d_qk = d_v): 128, 256, 384 or 512 */
+  int n_heads;        /* query heads sharing the KV: 1..64 */
+  int page_size;      /* tokens per page: must be 64 */
+  int window;         /* sliding-window entries: must be 128 */
+  int d_index;        /* index-key width: must be 128 */
+  int n_index_heads;  /* index heads: 1..64 */
+} pkv_config;
+
+/* One paged NVFP4 K/V cache (pools indexed by physical page id). */
+typedef struct {
+  uint8_t* k_data;    /* [num_pages][64*d/2]  K-layout */
+  uint8_t* k_scale;   /* [num_pages][64*d/16] K-layout */
+  uint8_t* v_data;    /* [num_pages][64*d/2]  V-layout */
+  uint8_t* v_scale;   /* [num_pages][64*d/16] V-layout */
+  int num_pages;
+  float ts_k;         /* FP32 tensor scales, > 0, fixed when the cache is created */
+  float ts_v;
+} pkv_kv_cache;
+
+/* Paged NVFP4 index keys (d_index channels, K-layout). */
+typedef struct {
+  uint8_t* data;      /* [num_pages][64*d_index/2] */
+  uint8_t* scale;     /* [num_pages][64*d_index/16] */
+  int num_pages;
+  float ts;
+} pkv_idx_cache;
+
+/* FP8 (E4M3) window K/V. */
+typedef struct {
+  const uint8_t* k;   /* [B][128][d] */
+  const uint8_t* v;   /* [B][128][d] */
+  float tw_k;         /* FP32 tensor scales, > 0 */
+  float tw_v;
+  const int32_t* win_len;  /* device [B]: valid entries 0..128 (decode only; NULL = 128) */
+} pkv_window;
+
+/* Operations for pkv_workspace_bytes. */
+enum { PKV_OP_DECODE = 1, PKV_OP_SCORE_TOPK = 2, PKV_OP_REPLAY = 3 };
+
+/* Create a context on CUDA device `device` (made current for the call).
+ * Allocates the context's 4-byte device error word.  Returns
+ * PKV_ERR_UNSUPPORTED for shapes outside the config rules above. */
+pkv_status pkv_init(const pkv_config* cfg, int device, pkv_ctx** out);
+void pkv_destroy(pkv_ctx* ctx);
+
+/* Bytes of scratch the op needs for `batch` sequences (replay: sequences,
+ * each with 128 queries) of at most `max_len` tokens each (score_topk: `k` is
+ * passed in max_len's place of the selection size only through the call). */
+size_t pkv_workspace_bytes(const pkv_ctx* ctx, int op, int batch, int max_len);
+
+/* NVFP4 quantize + append ("MegaAttention avec KV compressé NVFP4": the cache
+ * format; the write side of it).  Token i (K row k_new[i], V row v_new[i],
+ * float32 [n][d]) is written at position pos[i] of sequence seq_idx[i]: page
+ * page_table[seq_idx[i]*max_pages + pos[i]/64], slot pos[i]%64.  Per block of
+ * 16 channels: amax, s = fp32(amax / fp32(6*ts)), scale byte = E4M3(s) (nearest,
+ * ties to even, saturating), codes = E2M1(fp32(x / fp32(E4M3[S]*ts))) (nearest,
+ * ties to even, |v| >= 6 -> 6, sign kept; all 0 when S = 0).  Entries are
+ * independent; two entries with the same (sequence, position) race. */
+pkv_status pkv_append_kv(pkv_ctx* ctx, const float* k_new, const float* v_new,
+                         const int32_t* seq_idx, const int32_t* pos, int n,
+                         const pkv_kv_cache* cache, const int32_t* page_table,
+                         int max_pages, void* stream);
+
+/* Same quantize + append for index keys (float32 [n][d_index], K-layout). */
+pkv_status pkv_append_index(pkv_ctx* ctx, const float* k_idx_new, const int32_t* seq_idx,
+                            const int32_t* pos, int n, const pkv_idx_cache* icache,
+                            const int32_t* page_table, int max_pages, void* stream);
+
+/* FP8 (E4M3) encode with a tensor scale: out[i] = E4M3(fp32(x[i] / tw)),
+ * nearest, ties to even, saturating at 448, sign kept.  Used to write the
+ * sliding window ("uncompressed FP8") and the FP8 index queries. */
+pkv_status pkv_quantize_fp8(const float* x, size_t n, float tw, uint8_t* out, void* stream);
+
+/* Sparse MQA logits + top-k ("Logits MQA creux"): for each sequence b and
+ * position t < seq_len[b],
+ *   score_t = sum_h w[b][h] * ReLU(tq * ts * (q_idx[b][h] . k_t))
+ * with q_idx FP8 [B][n_index_heads][d_index] (scale tq), w float32
+ * [B][n_index_heads], keys from `icache` through page_table.  Writes the k
+ * positions of highest score (ties: lower position first) to out_idx
+ * int32 [B][k] in ascending order, -1 padded when seq_len[b] < k, and the
+ * scores to out_score float32 [B][max_pages*64] when not NULL.  1 <= k <= 4096. */
+pkv_status pkv_score_topk(pkv_ctx* ctx, const uint8_t* q_idx, float tq, const float* w,
+                          const pkv_idx_cache* icache, const int32_t* page_table,
+                          int max_pages, const int32_t* seq_len, int B, int k,
+                          int32_t* out_idx, float* out_score, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* Decode attention (flash-decoding split along the sequence + LSE merge).
+ * For sequence b, query head h (q bf16 [B][n_heads][d]):
+ *   entries = global tokens [0, seq_len[b]) (or, if sel_idx != NULL, the
+ *             positions sel_idx[b][0..k), -1 entries skipped) followed by the
+ *             window entries [0, win_len[b]);
+ *   z = softmax_scale * q.k_hat, O = softmax(z) . v_hat, LSE = ln sum exp z,
+ *   k_hat/v_hat the exact dequantized values.  Writes out float32 [B][H][d]
+ *   and out_lse float32 [B][H] (may be NULL). */
+pkv_status pkv_decode_attn(pkv_ctx* ctx, const void* q_bf16, const pkv_kv_cache* cache,
+                           const int32_t* page_table, int max_pages, const int32_t* seq_len,
+                           int B, const int32_t* sel_idx, int k, const pkv_window* win,
+                           float softmax_scale, float* out, float* out_lse, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* Bounded replay ("SWA bounded replay", "Côté encodeur"): for sequence b with
+ * prefix length H_b = prefix_len[b] >= 128 and s_b = H_b - 128, query r
+ * (q bf16 [B][128][n_heads][d], position s_b + r) attends the global tokens
+ * [0, s_b) and the chunk-window entries [0, r] (chunk_win->k/v [B][128][d]:
+ * FP8 K/V of positions s_b..H_b-1; win_len ignored).
+ * Writes out float32 [B][128][H][d], out_lse float32 [B][128][H] (may be NULL). */
+pkv_status pkv_replay_attn(pkv_ctx* ctx, const void* q_bf16, const pkv_kv_cache* cache,
+                           const int32_t* page_table, int max_pages, const int32_t* prefix_len,
+                           int B, const pkv_window* chunk_win, float softmax_scale,
+                           float* out, float* out_lse, void* ws, size_t ws_bytes, void* stream);
+
+/* LSE merge of two partial results over disjoint entry sets (the combine step
+ * of flash-decoding; decode merges its global and window segments this way):
+ *   lse = ln(e^lse_a + e^lse_b), o = e^(lse_a-lse) o_a + e^(lse_b-lse) o_b,
+ * rows x dv float32; a part with lse = -inf has weight 0.  o/lse may alias a. */
+pkv_status pkv_merge(const float* o_a, const float* lse_a, const float* o_b,
+                     const float* lse_b, float* o, float* lse, int rows, int dv,
+                     void* stream);
+
+/* Synchronize `stream`, return and clear the context's device error word
+ * (PKV_OK, PKV_ERR_BAD_PAGE or PKV_ERR_TIMEOUT), or PKV_ERR_CUDA. */
+pkv_status pkv_get_error(pkv_ctx* ctx, void* stream);
+
+const char* pkv_status_str(pkv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

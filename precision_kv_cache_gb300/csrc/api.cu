@@ -1,0 +1,310 @@
+// C ABI of the library (declared in include/pkv.h): argument validation,
+// scratch carving and kernel selection.  Every compute step runs in the
+// kernels of this directory; nothing here touches tensor data on the host.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <new>
+
+#include "pkv_common.cuh"
+#include "attn_args.cuh"
+#include "attn_tc.h"
+#include "launch.h"
+
+struct pkv_ctx {
+  pkv_config cfg;
+  int device;
+  int num_sms;
+  int* d_err;
+};
+
+namespace {
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+inline pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+bool valid_d(int d) { return d == 128 || d == 256 || d == 512; }
+
+bool valid_cache(const pkv_ctx* c, const pkv_kv_cache* kc) {
+  if (!kc || !kc->k_data || !kc->k_scale || !kc->v_data || !kc->v_scale) return false;
+  if (!aligned16(kc->k_data) || !aligned16(kc->k_scale) || !aligned16(kc->v_data) || !aligned16(kc->v_scale))
+    return false;
+  if (kc->num_pages <= 0) return false;
+  if (!(kc->ts_k > 0.f) || !(kc->ts_v > 0.f) || !(kc->ts_k < INFINITY) || !(kc->ts_v < INFINITY)) return false;
+  (void)c;
+  return true;
+}
+
+bool valid_window(const pkv_window* w) {
+  if (!w || !w->k || !w->v || !aligned16(w->k) || !aligned16(w->v)) return false;
+  return (w->tw_k > 0.f && w->tw_k < INFINITY && w->tw_v > 0.f && w->tw_v < INFINITY);
+}
+
+// Split policy of the CUDA-core attention path: enough (split, head group,
+// query row) units to give every SM several blocks, splits of >= 256 entries.
+void choose_split(const pkv_ctx* c, int n_groups, int max_entries, int* n_split, int* chunk) {
+  const int hg = (c->cfg.n_heads + 7) / 8;
+  const long long units = (long long)n_groups * hg;
+  const long long target = 4LL * c->num_sms;
+  int ns = (int)std::max<long long>(1, (target + units - 1) / units);
+  const int max_ns = std::max(1, (max_entries + 255) / 256);
+  ns = std::min(ns, max_ns);
+  int ch = (max_entries + ns - 1) / ns;
+  ch = std::max(64, (ch + 63) / 64 * 64);
+  *chunk = ch;
+  *n_split = std::max(1, (max_entries + ch - 1) / ch);
+}
+
+size_t attn_ws_bytes(const pkv_ctx* c, int n_groups, int max_entries) {
+  int ns, ch;
+  choose_split(c, n_groups, max_entries, &ns, &ch);
+  const size_t H = c->cfg.n_heads, D = c->cfg.d;
+  size_t simple = (size_t)n_groups * ns * H * (D + 1) * 4 + 256;
+  size_t tc = pkv_attn_tc_ws_bytes(c->num_sms, c->cfg.n_heads, c->cfg.d, n_groups, max_entries);
+  return std::max(simple, tc);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_str(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_BAD_PAGE: return "page id out of range or sequence longer than its page table";
+    case PKV_ERR_TIMEOUT: return "bounded wait timed out on the device";
+    case PKV_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+pkv_status pkv_init(const pkv_config* cfg, int device, pkv_ctx** out) {
+  if (!cfg || !out) return PKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!valid_d(cfg->d) || cfg->n_heads < 1 || cfg->n_heads > 64 || cfg->page_size != PKV_PAGE ||
+      cfg->window != PKV_WINDOW || cfg->d_index != 128 || cfg->n_index_heads < 1 || cfg->n_index_heads > 64)
+    return PKV_ERR_UNSUPPORTED;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return PKV_ERR_CUDA;
+  DeviceGuard g(device);
+  pkv_ctx* c = new (std::nothrow) pkv_ctx;
+  if (!c) return PKV_ERR_CUDA;
+  c->cfg = *cfg;
+  c->device = device;
+  if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    delete c;
+    return PKV_ERR_CUDA;
+  }
+  if (cudaMalloc(&c->d_err, sizeof(int)) != cudaSuccess) { delete c; return PKV_ERR_CUDA; }
+  if (cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) { cudaFree(c->d_err); delete c; return PKV_ERR_CUDA; }
+  if (pkv_attn_tc_init(device) != cudaSuccess) { cudaFree(c->d_err); delete c; return PKV_ERR_CUDA; }
+  *out = c;
+  return PKV_OK;
+}
+
+void pkv_destroy(pkv_ctx* c) {
+  if (!c) return;
+  DeviceGuard g(c->device);
+  cudaFree(c->d_err);
+  delete c;
+}
+
+size_t pkv_workspace_bytes(const pkv_ctx* c, int op, int batch, int max_len) {
+  if (!c || batch <= 0 || max_len < 0) return 0;
+  switch (op) {
+    case PKV_OP_DECODE: return attn_ws_bytes(c, batch, max_len + PKV_WINDOW);
+    case PKV_OP_REPLAY: return attn_ws_bytes(c, batch * PKV_WINDOW, max_len + PKV_WINDOW);
+    case PKV_OP_SCORE_TOPK:
+      return (size_t)batch * (size_t)max_len * 4 + pkv_topk_ws_bytes(batch, PKV_TOPK_MAX_K) + 256;
+  }
+  return 0;
+}
+
+pkv_status pkv_append_kv(pkv_ctx* c, const float* k_new, const float* v_new, const int32_t* seq_idx,
+                         const int32_t* pos, int n, const pkv_kv_cache* cache, const int32_t* page_table,
+                         int max_pages, void* stream) {
+  if (!c || n < 0 || max_pages <= 0) return PKV_ERR_INVALID_ARG;
+  if (n == 0) return PKV_OK;
+  if (!k_new || !v_new || !seq_idx || !pos || !page_table || !aligned16(k_new) || !aligned16(v_new))
+    return PKV_ERR_INVALID_ARG;
+  if (!valid_cache(c, cache)) return PKV_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  return cuda_status(pkv_launch_append_kv(c->cfg.d, k_new, v_new, seq_idx, pos, n, *cache, page_table,
+                                          max_pages, c->d_err, (cudaStream_t)stream));
+}
+
+pkv_status pkv_append_index(pkv_ctx* c, const float* x, const int32_t* seq_idx, const int32_t* pos, int n,
+                            const pkv_idx_cache* ic, const int32_t* page_table, int max_pages, void* stream) {
+  if (!c || n < 0 || max_pages <= 0) return PKV_ERR_INVALID_ARG;
+  if (n == 0) return PKV_OK;
+  if (!x || !seq_idx || !pos || !page_table || !ic || !ic->data || !ic->scale || !aligned16(x) ||
+      !aligned16(ic->data) || !aligned16(ic->scale) || ic->num_pages <= 0 || !(ic->ts > 0.f) || !(ic->ts < INFINITY))
+    return PKV_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  return cuda_status(pkv_launch_append_index(x, seq_idx, pos, n, *ic, page_table, max_pages, c->d_err,
+                                             (cudaStream_t)stream));
+}
+
+pkv_status pkv_quantize_fp8(const float* x, size_t n, float tw, uint8_t* out, void* stream) {
+  if (n == 0) return PKV_OK;
+  if (!x || !out || !aligned16(x) || ((uintptr_t)out & 3u) || !(tw > 0.f) || !(tw < INFINITY))
+    return PKV_ERR_INVALID_ARG;
+  return cuda_status(pkv_launch_quantize_fp8(x, n, tw, out, (cudaStream_t)stream));
+}
+
+pkv_status pkv_score_topk(pkv_ctx* c, const uint8_t* q_idx, float tq, const float* w, const pkv_idx_cache* ic,
+                          const int32_t* page_table, int max_pages, const int32_t* seq_len, int B, int k,
+                          int32_t* out_idx, float* out_score, void* ws, size_t ws_bytes, void* stream) {
+  if (!c || B <= 0 || max_pages <= 0 || k < 1 || k > PKV_TOPK_MAX_K) return PKV_ERR_INVALID_ARG;
+  if (!q_idx || !w || !ic || !ic->data || !ic->scale || !page_table || !seq_len || !out_idx)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(ic->data) || !aligned16(ic->scale) || ic->num_pages <= 0 || !(ic->ts > 0.f) ||
+      !(tq > 0.f) || !(tq < INFINITY) || !(ic->ts < INFINITY))
+    return PKV_ERR_INVALID_ARG;
+  if ((long long)max_pages * PKV_PAGE > (1LL << 30)) return PKV_ERR_UNSUPPORTED;
+  const int Lmax = max_pages * PKV_PAGE;
+  const size_t need = pkv_workspace_bytes(c, PKV_OP_SCORE_TOPK, B, Lmax);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return PKV_ERR_WORKSPACE;
+  DeviceGuard g(c->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* p = (uint8_t*)ws;
+  float* scores = out_score;
+  if (!scores) scores = (float*)p;
+  p += (size_t)B * Lmax * 4;
+  p = (uint8_t*)(((uintptr_t)p + 255) & ~(uintptr_t)255);
+  cudaError_t e = pkv_launch_score_simple(q_idx, tq, w, *ic, page_table, max_pages, seq_len, B,
+                                          c->cfg.n_index_heads, scores, Lmax, c->d_err, st);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  return cuda_status(pkv_launch_topk(scores, Lmax, seq_len, B, k, out_idx, p, st));
+}
+
+static pkv_status run_attention(pkv_ctx* c, pkv::AttnArgs& a, int max_entries, float* out, float* out_lse,
+                                void* ws, size_t ws_bytes, cudaStream_t st) {
+  const size_t need = attn_ws_bytes(c, a.n_groups, max_entries);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return PKV_ERR_WORKSPACE;
+  // the tensor-core kernel takes the dense cases it supports
+  if (pkv_attn_tc_supported(a, c->cfg.d)) {
+    cudaError_t e = pkv_launch_attn_tc(a, c->num_sms, max_entries, out, out_lse, ws, st);
+    return cuda_status(e);
+  }
+  int ns, ch;
+  choose_split(c, a.n_groups, max_entries, &ns, &ch);
+  a.n_split = ns;
+  a.chunk = ch;
+  a.part_o = (float*)ws;
+  a.part_lse = (float*)((uint8_t*)ws + (size_t)a.n_groups * ns * a.H * a.D * 4);
+  cudaError_t e = pkv_launch_attn_simple(c->cfg.d, a, st);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  return cuda_status(pkv_launch_merge_splits(a.part_o, a.part_lse, ns, a.n_groups, a.H, a.D, out, out_lse, st));
+}
+
+pkv_status pkv_decode_attn(pkv_ctx* c, const void* q, const pkv_kv_cache* cache, const int32_t* page_table,
+                           int max_pages, const int32_t* seq_len, int B, const int32_t* sel_idx, int k,
+                           const pkv_window* win, float softmax_scale, float* out, float* out_lse, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!c || B <= 0 || max_pages <= 0 || !q || !page_table || !seq_len || !out || !aligned16(q) || !aligned16(out))
+    return PKV_ERR_INVALID_ARG;
+  if (!valid_cache(c, cache) || !valid_window(win)) return PKV_ERR_INVALID_ARG;
+  if (sel_idx && (k < 1 || k > PKV_TOPK_MAX_K)) return PKV_ERR_INVALID_ARG;
+  if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
+    return PKV_ERR_INVALID_ARG;
+  if ((long long)max_pages * PKV_PAGE > (1LL << 30)) return PKV_ERR_UNSUPPORTED;
+  DeviceGuard g(c->device);
+  pkv::AttnArgs a{};
+  a.q = (const uint16_t*)q;
+  a.cache = *cache;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.lens = seq_len;
+  a.sel = sel_idx;
+  a.k = sel_idx ? k : 0;
+  a.wk = win->k;
+  a.wv = win->v;
+  a.tw_k = win->tw_k;
+  a.tw_v = win->tw_v;
+  a.win_len = win->win_len;
+  a.scale = softmax_scale;
+  a.H = c->cfg.n_heads;
+  a.D = c->cfg.d;
+  a.n_groups = B;
+  a.replay = 0;
+  a.err = c->d_err;
+  const int max_entries = (sel_idx ? k : max_pages * PKV_PAGE) + PKV_WINDOW;
+  return run_attention(c, a, max_entries, out, out_lse, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+pkv_status pkv_replay_attn(pkv_ctx* c, const void* q, const pkv_kv_cache* cache, const int32_t* page_table,
+                           int max_pages, const int32_t* prefix_len, int B, const pkv_window* cw,
+                           float softmax_scale, float* out, float* out_lse, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!c || B <= 0 || max_pages <= 0 || !q || !page_table || !prefix_len || !out || !aligned16(q) ||
+      !aligned16(out))
+    return PKV_ERR_INVALID_ARG;
+  if (!valid_cache(c, cache) || !valid_window(cw)) return PKV_ERR_INVALID_ARG;
+  if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
+    return PKV_ERR_INVALID_ARG;
+  if ((long long)max_pages * PKV_PAGE > (1LL << 30) || (long long)B * PKV_WINDOW > (1LL << 24))
+    return PKV_ERR_UNSUPPORTED;
+  DeviceGuard g(c->device);
+  pkv::AttnArgs a{};
+  a.q = (const uint16_t*)q;
+  a.cache = *cache;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.lens = prefix_len;
+  a.sel = nullptr;
+  a.k = 0;
+  a.wk = cw->k;
+  a.wv = cw->v;
+  a.tw_k = cw->tw_k;
+  a.tw_v = cw->tw_v;
+  a.win_len = nullptr;
+  a.scale = softmax_scale;
+  a.H = c->cfg.n_heads;
+  a.D = c->cfg.d;
+  a.n_groups = B * PKV_WINDOW;
+  a.replay = 1;
+  a.err = c->d_err;
+  const int max_entries = max_pages * PKV_PAGE + PKV_WINDOW;
+  return run_attention(c, a, max_entries, out, out_lse, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+pkv_status pkv_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b, float* o,
+                     float* lse, int rows, int dv, void* stream) {
+  if (rows < 0 || dv <= 0) return PKV_ERR_INVALID_ARG;
+  if (rows == 0) return PKV_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o || !lse) return PKV_ERR_INVALID_ARG;
+  return cuda_status(pkv_launch_merge2(o_a, lse_a, o_b, lse_b, o, lse, rows, dv, (cudaStream_t)stream));
+}
+
+pkv_status pkv_get_error(pkv_ctx* c, void* stream) {
+  if (!c) return PKV_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PKV_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, c->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+  if (h & PKV_DEVERR_TIMEOUT) return PKV_ERR_TIMEOUT;
+  if (h & PKV_DEVERR_BAD_PAGE) return PKV_ERR_BAD_PAGE;
+  return PKV_OK;
+}
+
+}  // extern "C"

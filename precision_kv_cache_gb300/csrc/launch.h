@@ -1,0 +1,31 @@
+// Host-side launchers of the library's kernels (internal; the public ABI is include/pkv.h).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+#define PKV_TOPK_CAND 4096
+#define PKV_TOPK_MAX_K 4096
+
+namespace pkv { struct AttnArgs; }
+
+cudaError_t pkv_launch_append_kv(int d, const float* k_new, const float* v_new, const int32_t* seq_idx,
+                                 const int32_t* pos, int n, const pkv_kv_cache& cache,
+                                 const int32_t* page_table, int max_pages, int* err, cudaStream_t st);
+cudaError_t pkv_launch_append_index(const float* x, const int32_t* seq_idx, const int32_t* pos, int n,
+                                    const pkv_idx_cache& ic, const int32_t* page_table, int max_pages,
+                                    int* err, cudaStream_t st);
+cudaError_t pkv_launch_quantize_fp8(const float* x, size_t n, float tw, uint8_t* out, cudaStream_t st);
+cudaError_t pkv_launch_attn_simple(int d, const pkv::AttnArgs& a, cudaStream_t st);
+cudaError_t pkv_launch_merge_splits(const float* part_o, const float* part_lse, int n_split, int rows_g,
+                                    int H, int D, float* out, float* out_lse, cudaStream_t st);
+cudaError_t pkv_launch_merge2(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+                              float* o, float* lse, int rows, int dv, cudaStream_t st);
+cudaError_t pkv_launch_score_simple(const uint8_t* q_idx, float tq, const float* w, const pkv_idx_cache& ic,
+                                    const int32_t* page_table, int max_pages, const int32_t* seq_len, int B,
+                                    int Hi, float* scores, int Lmax, int* err, cudaStream_t st);
+size_t pkv_topk_ws_bytes(int B, int k);
+cudaError_t pkv_launch_topk(const float* scores, int Lmax, const int32_t* seq_len, int B, int k,
+                            int32_t* out, void* ws, cudaStream_t st);

@@ -1,0 +1,98 @@
+// Device-side helpers shared by the kernels of the library: FP4/FP8 code
+// conversion, page addressing, error reporting.  Written from the OCP MX v1.0
+// (E2M1) and OCP OFP8 (E4M3, FN variant) definitions and the byte layout of
+// include/pkv.h; nothing here is shared with the CPU oracle.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+#define PKV_PAGE 64
+#define PKV_WINDOW 128
+
+// device error word bits (pkv_get_error maps them to pkv_status)
+#define PKV_DEVERR_BAD_PAGE 1
+#define PKV_DEVERR_TIMEOUT 2
+
+namespace pkv {
+
+__device__ __forceinline__ void report(int* err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// ---------------------------------------------------------------- encoders
+// E4M3 code of a finite a >= 0: nearest finite value, ties to the even code,
+// saturating at 448 (0x7E).  Subnormals (a < 2^-6) are multiples of 2^-9.
+__device__ __forceinline__ uint32_t e4m3_code_pos(float a) {
+  if (!(a < 448.f)) return 0x7Eu;
+  if (a < 0.015625f) {                       // 2^-6
+    return (uint32_t)__float2int_rn(a * 512.f);   // exact scaling; RNE -> 0..8 (8 = 2^-6, code 0x08)
+  }
+  const uint32_t u = __float_as_uint(a);
+  int e = (int)(u >> 23) - 127 + 7;           // biased E4M3 exponent, >= 1
+  const uint32_t m = u & 0x7FFFFFu;
+  uint32_t keep = m >> 20;                    // 3 kept mantissa bits
+  const uint32_t rem = m & 0xFFFFFu;          // 20 dropped bits
+  keep += (rem > 0x80000u) || (rem == 0x80000u && (keep & 1u));
+  if (keep == 8u) { keep = 0u; e += 1; }
+  const uint32_t code = ((uint32_t)e << 3) | keep;
+  return code > 0x7Eu ? 0x7Eu : code;
+}
+
+__device__ __forceinline__ uint32_t e4m3_code(float x) {
+  return e4m3_code_pos(fabsf(x)) | (signbit(x) ? 0x80u : 0u);
+}
+
+// E2M1 code of v: magnitude grid {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even
+// code (the grid points with even codes win their midpoints), |v| >= 6 -> 6.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  const float a = fabsf(v);
+  const uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) +
+                     (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+  return c | (signbit(v) ? 8u : 0u);
+}
+
+// ---------------------------------------------------------------- decoders
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
+  const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+  return (c & 0x80u) ? -v : v;
+}
+
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  // magnitudes of codes 0..7 are 0, .5, 1, 1.5, 2, 3, 4, 6
+  const uint32_t m = c & 7u;
+  const float mag = (m < 4u) ? 0.5f * (float)m : (float)(1u << ((m >> 1) - 1u)) * ((m & 1u) ? 1.5f : 1.0f);
+  return (c & 8u) ? -mag : mag;
+}
+
+// ---------------------------------------------------------------- page layout
+template <int D>
+struct KLayout {
+  static constexpr int kRowBytes = D / 2;
+  static constexpr int kSwz = (D / 32 < 8 ? D / 32 : 8) - 1;
+  // byte offset of channel pair j of token t inside a page's data block
+  __device__ __forceinline__ static int data(int t, int j) {
+    return t * kRowBytes + 16 * ((j >> 4) ^ (t & kSwz)) + (j & 15);
+  }
+  // byte offset of the scale of block j of token t
+  __device__ __forceinline__ static int scale(int t, int j) {
+    return (((j >> 3) * PKV_PAGE + t) << 3) + (j & 7);
+  }
+};
+
+template <int D>
+struct VLayout {
+  // 32-bit word holding channel c of tokens 8*(t/8) .. 8*(t/8)+7 (nibble t%8)
+  __device__ __forceinline__ static int word(int t, int c) { return (t >> 3) * D + c; }
+  __device__ __forceinline__ static int scale(int t, int j) { return j * PKV_PAGE + t; }
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+}  // namespace pkv

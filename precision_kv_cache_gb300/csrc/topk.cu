@@ -1,0 +1,308 @@
+// Exact top-k over per-sequence float32 scores (ties to the lower position,
+// output ascending) by radix select on the order-preserving 32-bit key.
+//
+//   pass 1  histogram of key bits [31:20] (4096 bins)       -> boundary bin b1
+//   pass 2  emit keys above b1; histogram bits [19:8] of b1  -> boundary bin b2
+//   pass 3  emit keys above (b1,b2); collect keys in (b1,b2) as candidates
+//   finish  sort candidates by (key desc, position asc), emit what is still needed
+//           (if the candidate buffer overflowed: an ordered scan of the sequence)
+//   sort    the k emitted positions ascending (bitonic, one block per sequence)
+#include "pkv_common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+constexpr int TK_BINS = 4096;
+constexpr int TK_ITEMS = 16;            // scores per thread per pass
+constexpr int TK_THREADS = 256;
+
+// state words per sequence
+enum { ST_BIN1 = 0, ST_NEED1, ST_BIN2, ST_NEED2, ST_OUT, ST_NCAND, ST_OVF, ST_L, ST_WORDS = 8 };
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ int seq_length(const int32_t* seq_len, int b, int Lmax) {
+  int L = seq_len[b];
+  return L < 0 ? 0 : (L > Lmax ? Lmax : L);
+}
+
+__global__ void __launch_bounds__(TK_THREADS) tk_pass1(const float* __restrict__ scores, int Lmax,
+                                                       const int32_t* __restrict__ seq_len,
+                                                       uint32_t* __restrict__ hist) {
+  __shared__ uint32_t h[TK_BINS];
+  const int b = blockIdx.y;
+  for (int i = threadIdx.x; i < TK_BINS; i += TK_THREADS) h[i] = 0u;
+  __syncthreads();
+  const int L = seq_length(seq_len, b, Lmax);
+  const int base = blockIdx.x * TK_THREADS * TK_ITEMS;
+  const float* s = scores + (size_t)b * Lmax;
+  for (int i = 0; i < TK_ITEMS; ++i) {
+    const int t = base + i * TK_THREADS + threadIdx.x;
+    if (t < L) atomicAdd(&h[order_key(s[t]) >> 20], 1u);
+  }
+  __syncthreads();
+  uint32_t* g = hist + (size_t)b * TK_BINS;
+  for (int i = threadIdx.x; i < TK_BINS; i += TK_THREADS)
+    if (h[i]) atomicAdd(&g[i], h[i]);
+}
+
+// One block of 1024 threads per sequence: find the bin where the count of keys
+// at or above it first reaches `need` (scanning from the top bin down).
+__global__ void __launch_bounds__(1024) tk_find(const uint32_t* __restrict__ hist, int* __restrict__ state,
+                                                const int32_t* __restrict__ seq_len, int Lmax, int k, int level) {
+  __shared__ uint32_t warp_tot[32];
+  const int b = blockIdx.x;
+  int* st = state + b * ST_WORDS;
+  int need;
+  if (level == 1) {
+    const int L = seq_length(seq_len, b, Lmax);
+    if (threadIdx.x == 0) st[ST_L] = L;
+    if (L <= k) {            // everything is selected
+      if (threadIdx.x == 0) { st[ST_BIN1] = -1; st[ST_NEED1] = 0; st[ST_BIN2] = -1; st[ST_NEED2] = 0; }
+      return;
+    }
+    need = k;
+  } else {
+    if (st[ST_BIN1] < 0) return;
+    need = st[ST_NEED1];
+  }
+  const uint32_t* hb = hist + (size_t)b * TK_BINS;
+  // thread i owns bins 4095-4i .. 4092-4i (top first)
+  const int top = TK_BINS - 1 - 4 * threadIdx.x;
+  uint32_t c[4], sum = 0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) { c[j] = hb[top - j]; sum += c[j]; }
+  // exclusive prefix over threads (thread order = descending bins)
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  uint32_t wpre = 0u;
+  for (int i = 0; i < wid; ++i) wpre += warp_tot[i];
+  uint32_t above = wpre + incl - sum;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (above < (uint32_t)need && above + c[j] >= (uint32_t)need) {
+      if (level == 1) { st[ST_BIN1] = top - j; st[ST_NEED1] = need - (int)above; }
+      else { st[ST_BIN2] = top - j; st[ST_NEED2] = need - (int)above; }
+    }
+    above += c[j];
+  }
+}
+
+__device__ __forceinline__ void emit(int32_t* out_b, int* st, int t) {
+  const int p = atomicAdd(&st[ST_OUT], 1);
+  out_b[p] = t;
+}
+
+__global__ void __launch_bounds__(TK_THREADS) tk_pass2(const float* __restrict__ scores, int Lmax,
+                                                       int* __restrict__ state, uint32_t* __restrict__ hist2,
+                                                       int32_t* __restrict__ out, int k) {
+  __shared__ uint32_t h[TK_BINS];
+  const int b = blockIdx.y;
+  int* st = state + b * ST_WORDS;
+  const int L = st[ST_L];
+  const int bin1 = st[ST_BIN1];
+  for (int i = threadIdx.x; i < TK_BINS; i += TK_THREADS) h[i] = 0u;
+  __syncthreads();
+  const int base = blockIdx.x * TK_THREADS * TK_ITEMS;
+  const float* s = scores + (size_t)b * Lmax;
+  int32_t* ob = out + (size_t)b * k;
+  for (int i = 0; i < TK_ITEMS; ++i) {
+    const int t = base + i * TK_THREADS + threadIdx.x;
+    if (t < L) {
+      const uint32_t key = order_key(s[t]);
+      const int hi = (int)(key >> 20);
+      if (hi > bin1) emit(ob, st, t);
+      else if (hi == bin1) atomicAdd(&h[(key >> 8) & 0xFFFu], 1u);
+    }
+  }
+  __syncthreads();
+  if (bin1 < 0) return;
+  uint32_t* g = hist2 + (size_t)b * TK_BINS;
+  for (int i = threadIdx.x; i < TK_BINS; i += TK_THREADS)
+    if (h[i]) atomicAdd(&g[i], h[i]);
+}
+
+__global__ void __launch_bounds__(TK_THREADS) tk_pass3(const float* __restrict__ scores, int Lmax,
+                                                       int* __restrict__ state, unsigned long long* __restrict__ cand,
+                                                       int cap, int32_t* __restrict__ out, int k) {
+  const int b = blockIdx.y;
+  int* st = state + b * ST_WORDS;
+  const int bin1 = st[ST_BIN1];
+  if (bin1 < 0) return;
+  const int bin2 = st[ST_BIN2];
+  const int L = st[ST_L];
+  const int base = blockIdx.x * TK_THREADS * TK_ITEMS;
+  const float* s = scores + (size_t)b * Lmax;
+  int32_t* ob = out + (size_t)b * k;
+  unsigned long long* cb = cand + (size_t)b * cap;
+  for (int i = 0; i < TK_ITEMS; ++i) {
+    const int t = base + i * TK_THREADS + threadIdx.x;
+    if (t < L) {
+      const uint32_t key = order_key(s[t]);
+      if ((int)(key >> 20) != bin1) continue;
+      const int mid = (int)((key >> 8) & 0xFFFu);
+      if (mid > bin2) emit(ob, st, t);
+      else if (mid == bin2) {
+        const int c = atomicAdd(&st[ST_NCAND], 1);
+        if (c < cap) cb[c] = ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
+        else st[ST_OVF] = 1;
+      }
+    }
+  }
+}
+
+// bitonic sort of n (power of two) 64-bit values in shared memory, descending
+__device__ void bitonic_desc(unsigned long long* v, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = ((lo & size) == 0);
+        const unsigned long long a = v[lo], c = v[hi];
+        if ((a < c) == desc) { v[lo] = c; v[hi] = a; }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) tk_finish(const float* __restrict__ scores, int Lmax,
+                                                  int* __restrict__ state,
+                                                  const unsigned long long* __restrict__ cand, int cap,
+                                                  int32_t* __restrict__ out, int k) {
+  extern __shared__ unsigned long long sv[];
+  const int b = blockIdx.x;
+  int* st = state + b * ST_WORDS;
+  const int bin1 = st[ST_BIN1];
+  if (bin1 < 0) return;
+  const int need = st[ST_NEED2];
+  int32_t* ob = out + (size_t)b * k;
+  if (!st[ST_OVF]) {
+    const int n = min(st[ST_NCAND], cap);
+    int n2 = 1;
+    while (n2 < n) n2 <<= 1;
+    for (int i = threadIdx.x; i < n2; i += blockDim.x) sv[i] = i < n ? cand[(size_t)b * cap + i] : 0ull;
+    __syncthreads();
+    bitonic_desc(sv, n2);
+    const int base = st[ST_OUT];
+    for (int i = threadIdx.x; i < need; i += blockDim.x)
+      ob[base + i] = (int)(0xFFFFFFFFu - (uint32_t)(sv[i] & 0xFFFFFFFFull));
+    __syncthreads();
+    if (threadIdx.x == 0) st[ST_OUT] = base + need;
+    return;
+  }
+  // Overflow: many scores share the boundary's top 24 bits.  Ordered scan of the
+  // sequence: histogram of the low 8 bits among the prefix, then emit in
+  // position order so equal keys go to the lower positions first.
+  __shared__ uint32_t h[256];
+  __shared__ int sel_bin, sel_need, taken;
+  __shared__ uint32_t wcnt[32];
+  const uint32_t prefix = ((uint32_t)bin1 << 12) | (uint32_t)st[ST_BIN2];
+  const int L = st[ST_L];
+  const float* s = scores + (size_t)b * Lmax;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0u;
+  __syncthreads();
+  for (int t = threadIdx.x; t < L; t += blockDim.x) {
+    const uint32_t key = order_key(s[t]);
+    if ((key >> 8) == prefix) atomicAdd(&h[key & 0xFFu], 1u);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int above = 0;
+    for (int i = 255; i >= 0; --i) {
+      if (above + (int)h[i] >= need) { sel_bin = i; sel_need = need - above; break; }
+      above += (int)h[i];
+    }
+    taken = 0;
+  }
+  __syncthreads();
+  const uint32_t T = (prefix << 8) | (uint32_t)sel_bin;
+  const int base = st[ST_OUT];
+  __shared__ int emitted;
+  if (threadIdx.x == 0) emitted = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < L; t0 += blockDim.x) {
+    const int t = t0 + threadIdx.x;
+    uint32_t key = 0u;
+    bool above = false, tie = false;
+    if (t < L) {
+      key = order_key(s[t]);
+      above = ((key >> 8) == prefix) && (key > T);
+      tie = (key == T);
+    }
+    if (above) { const int p = atomicAdd(&emitted, 1); ob[base + p] = t; }
+    // rank of this tie among the ties of this block, in position order
+    const unsigned bal = __ballot_sync(0xffffffffu, tie);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (lane == 0) wcnt[wid] = __popc(bal);
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < wid; ++i) before += (int)wcnt[i];
+    const int rank = taken + before + __popc(bal & ((1u << lane) - 1u));
+    if (tie && rank < sel_need) { const int p = atomicAdd(&emitted, 1); ob[base + p] = t; }
+    __syncthreads();
+    if (threadIdx.x == 0) { int tot = 0; for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += (int)wcnt[i]; taken += tot; }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) st[ST_OUT] = base + emitted;
+}
+
+// sort the emitted positions ascending, pad with -1
+__global__ void __launch_bounds__(1024) tk_sort_out(int* __restrict__ state, int32_t* __restrict__ out, int k) {
+  extern __shared__ unsigned long long sv[];
+  const int b = blockIdx.x;
+  const int n = min(state[b * ST_WORDS + ST_OUT], k);
+  int n2 = 1;
+  while (n2 < k) n2 <<= 1;
+  int32_t* ob = out + (size_t)b * k;
+  // descending sort of (~pos) == ascending positions; padding sorts last
+  for (int i = threadIdx.x; i < n2; i += blockDim.x)
+    sv[i] = i < n ? (unsigned long long)(0xFFFFFFFFu - (uint32_t)ob[i]) : 0ull;
+  __syncthreads();
+  bitonic_desc(sv, n2);
+  for (int i = threadIdx.x; i < k; i += blockDim.x)
+    ob[i] = i < n ? (int)(0xFFFFFFFFu - (uint32_t)sv[i]) : -1;
+}
+
+}  // namespace pkv
+
+size_t pkv_topk_ws_bytes(int B, int k) {
+  (void)k;
+  return (size_t)B * (2 * pkv::TK_BINS * 4 + pkv::ST_WORDS * 4 + PKV_TOPK_CAND * 8) + 256;
+}
+
+cudaError_t pkv_launch_topk(const float* scores, int Lmax, const int32_t* seq_len, int B, int k,
+                            int32_t* out, void* ws, cudaStream_t st) {
+  using namespace pkv;
+  uint8_t* p = (uint8_t*)ws;
+  uint32_t* hist1 = (uint32_t*)p;  p += (size_t)B * TK_BINS * 4;
+  uint32_t* hist2 = (uint32_t*)p;  p += (size_t)B * TK_BINS * 4;
+  int* state = (int*)p;            p += (size_t)B * ST_WORDS * 4;
+  p = (uint8_t*)(((uintptr_t)p + 15) & ~(uintptr_t)15);
+  unsigned long long* cand = (unsigned long long*)p;
+  cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)B * (2 * TK_BINS + ST_WORDS) * 4, st);
+  if (e != cudaSuccess) return e;
+  const int chunks = (Lmax + TK_THREADS * TK_ITEMS - 1) / (TK_THREADS * TK_ITEMS);
+  dim3 grid(chunks > 0 ? chunks : 1, B);
+  int n2 = 1;
+  while (n2 < k) n2 <<= 1;
+  tk_pass1<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, seq_len, hist1);
+  tk_find<<<B, 1024, 0, st>>>(hist1, state, seq_len, Lmax, k, 1);
+  tk_pass2<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, state, hist2, out, k);
+  tk_find<<<B, 1024, 0, st>>>(hist2, state, seq_len, Lmax, k, 2);
+  tk_pass3<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, state, cand, PKV_TOPK_CAND, out, k);
+  tk_finish<<<B, 1024, PKV_TOPK_CAND * 8, st>>>(scores, Lmax, state, cand, PKV_TOPK_CAND, out, k);
+  tk_sort_out<<<B, 1024, (size_t)n2 * 8, st>>>(state, out, k);
+  return cudaGetLastError();
+}

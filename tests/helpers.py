@@ -1,0 +1,64 @@
+"""Shared helpers of the GPU parity tests: oracle-built inputs uploaded to the device.
+
+Inputs flow one way only: seeded rows (workloads) -> oracle quantization ->
+bytes copied to the GPU.  Nothing the CUDA path writes is fed back to the oracle.
+"""
+import math
+
+import numpy as np
+
+import workloads as W
+from oracle import attention as A
+from oracle import cache as C
+from oracle import formats as F
+
+# attention tolerance: |gpu - oracle| <= ATOL + RTOL * |oracle|, element-wise
+ATOL = 2e-3
+RTOL = 1e-2
+
+
+def assert_close(g, r, what, atol=ATOL, rtol=RTOL):
+    g = np.asarray(g, np.float64)
+    r = np.asarray(r, np.float64)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    both_inf = np.isneginf(g) & np.isneginf(r)
+    err = np.where(both_inf, 0.0, np.abs(g - r))
+    lim = atol + rtol * np.where(both_inf, 0.0, np.abs(r))
+    bad = ~(err <= lim)
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err - lim, -np.inf)), g.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {g.size} outside tolerance; worst at {i}: "
+                             f"gpu={g[i]} oracle={r[i]} (max abs err {np.nanmax(err):.3e})")
+
+
+def torch_dev():
+    import torch
+    return torch.device("cuda:0")
+
+
+def upload_cache(Kp, Vp, ts_k, ts_v):
+    import torch
+    import precision_kv_cache_gb300 as P
+    dev = torch_dev()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    return P.KVCache(t(Kp.data), t(Kp.scale), t(Vp.data), t(Vp.scale), float(ts_k), float(ts_v))
+
+
+def window_tensors(wl, tw_k, tw_v, win_len=None):
+    import torch
+    import precision_kv_cache_gb300 as P
+    dev = torch_dev()
+    kw = np.stack([C.window_codes(wl, tw_k, tw_v, b)[0] for b in range(wl.B)])
+    vw = np.stack([C.window_codes(wl, tw_k, tw_v, b)[1] for b in range(wl.B)])
+    wlen = None if win_len is None else torch.tensor(np.asarray(win_len, np.int32), device=dev)
+    return P.Window(torch.from_numpy(kw).to(dev), torch.from_numpy(vw).to(dev), float(tw_k), float(tw_v), wlen), kw, vw
+
+
+def q_tensor(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(torch_dev()).view(torch.bfloat16)
+
+
+def i32(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).to(torch_dev())
