@@ -36,7 +36,7 @@
  *   - Nothing here allocates device memory per call: scratch comes from the
  *     caller through (ws, ws_bytes); pkv_workspace_bytes() gives the size.
  *
- * Cache byte layout (one 64-token page; d = head dim, multiple of 128, <= 512):
+ * Cache byte layout (one 64-token page; d = head dim: 128, 256 or 512):
  *   K-layout (K, index keys):
  *     data  [64][d/2]: channel pair (2j,2j+1) of token t at byte
  *           t*(d/2) + 16*((j/16) ^ (t & s)) + j%16, s = min(8, d/32)-1,
@@ -74,7 +74,7 @@ typedef struct pkv_ctx pkv_ctx;
 
 /* Shapes fixed for the life of a context. */
 typedef struct {
-  int d;              /* head dim of K, V and Q (d_qk = d_v): 128, 256, 384 or 512 */
+  int d;              /* head dim of K, V and Q (d_qk = d_v): 128, 256 or 512 */
   int n_heads;        /* query heads sharing the KV: 1..64 */
   int page_size;      /* tokens per page: must be 64 */
   int window;         /* sliding-window entries: must be 128 */
@@ -119,9 +119,10 @@ enum { PKV_OP_DECODE = 1, PKV_OP_SCORE_TOPK = 2, PKV_OP_REPLAY = 3 };
 pkv_status pkv_init(const pkv_config* cfg, int device, pkv_ctx** out);
 void pkv_destroy(pkv_ctx* ctx);
 
-/* Bytes of scratch the op needs for `batch` sequences (replay: sequences,
- * each with 128 queries) of at most `max_len` tokens each (score_topk: `k` is
- * passed in max_len's place of the selection size only through the call). */
+/* Bytes of scratch (the `ws` argument) an op needs for `batch` sequences.
+ * max_len: PKV_OP_DECODE - max_pages*64 of the page table (sparse path: k);
+ * PKV_OP_REPLAY - max_pages*64 (batch = sequences, 128 queries each);
+ * PKV_OP_SCORE_TOPK - max_pages*64 (the score buffer and radix-select state). */
 size_t pkv_workspace_bytes(const pkv_ctx* ctx, int op, int batch, int max_len);
 
 /* NVFP4 quantize + append ("MegaAttention avec KV compressé NVFP4": the cache
@@ -199,6 +200,14 @@ pkv_status pkv_merge(const float* o_a, const float* lse_a, const float* o_b,
 pkv_status pkv_get_error(pkv_ctx* ctx, void* stream);
 
 const char* pkv_status_str(pkv_status s);
+
+/* Measurement aids (no counterpart in the pages; used by the benchmark).
+ * pkv_set_profile_events: when both are non-NULL cudaEvent_t handles, the next
+ * attention call (decode or replay) records `start` on its stream right before
+ * its main attention kernel and `stop` right after it, then forgets them.
+ * pkv_launch_count: number of kernels this context has launched so far. */
+pkv_status pkv_set_profile_events(pkv_ctx* ctx, void* start, void* stop);
+long long pkv_launch_count(const pkv_ctx* ctx);
 
 #ifdef __cplusplus
 }

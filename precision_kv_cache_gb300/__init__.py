@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             "pkv_merge": (i, [vp, vp, vp, vp, vp, vp, i, i, vp]),
             "pkv_get_error": (i, [vp, vp]),
             "pkv_status_str": (ctypes.c_char_p, [i]),
+            "pkv_set_profile_events": (i, [vp, vp, vp]),
+            "pkv_launch_count": (ctypes.c_longlong, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -234,6 +236,14 @@ class Context:
 
     def pkv_get_error(self, stream=None) -> int:
         return int(lib().pkv_get_error(self.h, _stream(stream)))
+
+    def pkv_set_profile_events(self, start: "torch.cuda.Event", stop: "torch.cuda.Event"):
+        """Record start/stop around the main kernel of the next attention call."""
+        _check(lib().pkv_set_profile_events(self.h, ctypes.c_void_p(start.cuda_event),
+                                            ctypes.c_void_p(stop.cuda_event)), "pkv_set_profile_events")
+
+    def pkv_launch_count(self) -> int:
+        return int(lib().pkv_launch_count(self.h))
 
     def workspace(self, op: int, batch: int, max_len: int) -> torch.Tensor:
         n = self.pkv_workspace_bytes(op, batch, max_len)

@@ -17,6 +17,9 @@ struct pkv_ctx {
   int device;
   int num_sms;
   int* d_err;
+  cudaEvent_t prof_start = nullptr;   // one-shot events around the next attention kernel
+  cudaEvent_t prof_stop = nullptr;
+  long long launches = 0;
 };
 
 namespace {
@@ -146,6 +149,7 @@ pkv_status pkv_append_kv(pkv_ctx* c, const float* k_new, const float* v_new, con
     return PKV_ERR_INVALID_ARG;
   if (!valid_cache(c, cache)) return PKV_ERR_INVALID_ARG;
   DeviceGuard g(c->device);
+  c->launches += 1;
   return cuda_status(pkv_launch_append_kv(c->cfg.d, k_new, v_new, seq_idx, pos, n, *cache, page_table,
                                           max_pages, c->d_err, (cudaStream_t)stream));
 }
@@ -158,6 +162,7 @@ pkv_status pkv_append_index(pkv_ctx* c, const float* x, const int32_t* seq_idx, 
       !aligned16(ic->data) || !aligned16(ic->scale) || ic->num_pages <= 0 || !(ic->ts > 0.f) || !(ic->ts < INFINITY))
     return PKV_ERR_INVALID_ARG;
   DeviceGuard g(c->device);
+  c->launches += 1;
   return cuda_status(pkv_launch_append_index(x, seq_idx, pos, n, *ic, page_table, max_pages, c->d_err,
                                              (cudaStream_t)stream));
 }
@@ -189,6 +194,7 @@ pkv_status pkv_score_topk(pkv_ctx* c, const uint8_t* q_idx, float tq, const floa
   if (!scores) scores = (float*)p;
   p += (size_t)B * Lmax * 4;
   p = (uint8_t*)(((uintptr_t)p + 255) & ~(uintptr_t)255);
+  c->launches += 1 + PKV_TOPK_LAUNCHES;
   cudaError_t e = pkv_launch_score_simple(q_idx, tq, w, *ic, page_table, max_pages, seq_len, B,
                                           c->cfg.n_index_heads, scores, Lmax, c->d_err, st);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
@@ -200,8 +206,12 @@ static pkv_status run_attention(pkv_ctx* c, pkv::AttnArgs& a, int max_entries, f
   const size_t need = attn_ws_bytes(c, a.n_groups, max_entries);
   if (!ws || ws_bytes < need || !aligned16(ws)) return PKV_ERR_WORKSPACE;
   // the tensor-core kernel takes the dense cases it supports
+  cudaEvent_t e0 = c->prof_start, e1 = c->prof_stop;
+  c->prof_start = c->prof_stop = nullptr;
   if (pkv_attn_tc_supported(a, c->cfg.d)) {
-    cudaError_t e = pkv_launch_attn_tc(a, c->num_sms, max_entries, out, out_lse, ws, st);
+    int nl = 0;
+    cudaError_t e = pkv_launch_attn_tc(a, c->num_sms, max_entries, out, out_lse, ws, st, e0, e1, &nl);
+    c->launches += nl;
     return cuda_status(e);
   }
   int ns, ch;
@@ -210,7 +220,10 @@ static pkv_status run_attention(pkv_ctx* c, pkv::AttnArgs& a, int max_entries, f
   a.chunk = ch;
   a.part_o = (float*)ws;
   a.part_lse = (float*)((uint8_t*)ws + (size_t)a.n_groups * ns * a.H * a.D * 4);
+  if (e0 && e1) cudaEventRecord(e0, st);
   cudaError_t e = pkv_launch_attn_simple(c->cfg.d, a, st);
+  if (e0 && e1) cudaEventRecord(e1, st);
+  c->launches += 2;
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return cuda_status(pkv_launch_merge_splits(a.part_o, a.part_lse, ns, a.n_groups, a.H, a.D, out, out_lse, st));
 }
@@ -306,5 +319,14 @@ pkv_status pkv_get_error(pkv_ctx* c, void* stream) {
   if (h & PKV_DEVERR_BAD_PAGE) return PKV_ERR_BAD_PAGE;
   return PKV_OK;
 }
+
+pkv_status pkv_set_profile_events(pkv_ctx* c, void* start, void* stop) {
+  if (!c) return PKV_ERR_INVALID_ARG;
+  c->prof_start = (cudaEvent_t)start;
+  c->prof_stop = (cudaEvent_t)stop;
+  return PKV_OK;
+}
+
+long long pkv_launch_count(const pkv_ctx* c) { return c ? c->launches : 0; }
 
 }  // extern "C"

@@ -8,6 +8,7 @@
 
 #define PKV_TOPK_CAND 4096
 #define PKV_TOPK_MAX_K 4096
+#define PKV_TOPK_LAUNCHES 8   // memset + 7 kernels of the radix select
 
 namespace pkv { struct AttnArgs; }
 
