@@ -22,7 +22,8 @@ def assert_close(g, r, what, atol=ATOL, rtol=RTOL):
     r = np.asarray(r, np.float64)
     assert g.shape == r.shape, (what, g.shape, r.shape)
     both_inf = np.isneginf(g) & np.isneginf(r)
-    err = np.where(both_inf, 0.0, np.abs(g - r))
+    with np.errstate(invalid="ignore"):
+        err = np.where(both_inf, 0.0, np.abs(g - r))
     lim = atol + rtol * np.where(both_inf, 0.0, np.abs(r))
     bad = ~(err <= lim)
     if bad.any():
