@@ -201,6 +201,25 @@ pkv_status pkv_get_error(pkv_ctx* ctx, void* stream);
 
 const char* pkv_status_str(pkv_status s);
 
+/* Decode attention without caller-provided scratch (no counterpart in the
+ * pages: an interface for callers that cannot allocate device memory, e.g.
+ * code running while a CUDA graph is being captured in global mode, where
+ * cudaMalloc is prohibited; plugins inside a framework that owns the device
+ * memory pool; loops that cannot afford cudaMalloc's implicit synchronization).
+ * Same arguments and results as pkv_decode_attn minus (ws, ws_bytes): the
+ * split-K scratch is a fixed array of PKV_NOALLOC_SCRATCH_BYTES inside the
+ * library image, which every GPU that loads the library holds until exit.
+ * Returns PKV_ERR_WORKSPACE when pkv_workspace_bytes(ctx, PKV_OP_DECODE, B,
+ * max_len) exceeds that size.  Allocates nothing.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress), so make it
+ * before any stream capture.  All calls share the array: calls whose kernels
+ * overlap on the GPU race; each call rewrites all scratch it reads. */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+pkv_status pkv_decode_attn_noalloc(pkv_ctx* ctx, const void* q_bf16, const pkv_kv_cache* cache,
+                                   const int32_t* page_table, int max_pages, const int32_t* seq_len,
+                                   int B, const int32_t* sel_idx, int k, const pkv_window* win,
+                                   float softmax_scale, float* out, float* out_lse, void* stream);
+
 /* Measurement aids (no counterpart in the pages; used by the benchmark).
  * pkv_set_profile_events: when both are non-NULL cudaEvent_t handles, the next
  * attention call (decode or replay) records `start` on its stream right before

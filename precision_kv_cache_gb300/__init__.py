@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
             "pkv_get_error": (i, [vp, vp]),
             "pkv_status_str": (ctypes.c_char_p, [i]),
             "pkv_set_profile_events": (i, [vp, vp, vp]),
+            "pkv_decode_attn_noalloc": (i, [vp, vp, ctypes.POINTER(_KVCache), vp, i, vp, i, vp, i,
+                                            ctypes.POINTER(_Window), f, vp, vp, vp]),
             "pkv_launch_count": (ctypes.c_longlong, [vp]),
         }
         for name, (res, args) in sig.items():
@@ -223,6 +225,17 @@ class Context:
                                      _p(seq_len), B, _p(sel_idx), k, ctypes.byref(w), scale, _p(out),
                                      _p(out_lse), _p(ws), ws.numel(), _stream(stream)), "pkv_decode_attn")
 
+    def pkv_decode_attn_noalloc(self, q, cache: KVCache, page_table, seq_len, win: Window, scale, out,
+                                out_lse=None, sel_idx=None, stream=None):
+        """pkv_decode_attn with the library's built-in scratch array instead of a caller buffer."""
+        B = seq_len.shape[0]
+        k = sel_idx.shape[1] if sel_idx is not None else 0
+        c = cache._c()
+        w = win._c()
+        _check(lib().pkv_decode_attn_noalloc(self.h, _p(q), ctypes.byref(c), _p(page_table), page_table.shape[1],
+                                             _p(seq_len), B, _p(sel_idx), k, ctypes.byref(w), scale, _p(out),
+                                             _p(out_lse), _stream(stream)), "pkv_decode_attn_noalloc")
+
     def pkv_replay_attn(self, q, cache: KVCache, page_table, prefix_len, chunk_win: Window, scale, out,
                         out_lse=None, ws=None, stream=None):
         B = prefix_len.shape[0]
@@ -239,6 +252,9 @@ class Context:
 
     def pkv_set_profile_events(self, start: "torch.cuda.Event", stop: "torch.cuda.Event"):
         """Record start/stop around the main kernel of the next attention call."""
+        for ev in (start, stop):
+            if not ev.cuda_event:       # torch creates the CUDA event on first record
+                ev.record()
         _check(lib().pkv_set_profile_events(self.h, ctypes.c_void_p(start.cuda_event),
                                             ctypes.c_void_p(stop.cuda_event)), "pkv_set_profile_events")
 

@@ -83,6 +83,8 @@ size_t attn_ws_bytes(const pkv_ctx* c, int n_groups, int max_entries) {
 
 }  // namespace
 
+int pkv_internal_ctx_device(const pkv_ctx* c) { return c ? c->device : -1; }
+
 extern "C" {
 
 const char* pkv_status_str(pkv_status s) {

@@ -30,3 +30,6 @@ cudaError_t pkv_launch_score_simple(const uint8_t* q_idx, float tq, const float*
 size_t pkv_topk_ws_bytes(int B, int k);
 cudaError_t pkv_launch_topk(const float* scores, int Lmax, const int32_t* seq_len, int B, int k,
                             int32_t* out, void* ws, cudaStream_t st);
+
+// device a context was created on
+int pkv_internal_ctx_device(const pkv_ctx* c);
