@@ -224,9 +224,12 @@ pkv_status pkv_decode_attn_noalloc(pkv_ctx* ctx, const void* q_bf16, const pkv_k
  * pkv_set_profile_events: when both are non-NULL cudaEvent_t handles, the next
  * attention call (decode or replay) records `start` on its stream right before
  * its main attention kernel and `stop` right after it, then forgets them.
- * pkv_launch_count: number of kernels this context has launched so far. */
+ * pkv_launch_count: number of kernels this context has launched so far.
+ * pkv_attn_path: kernel family of the last attention call: 1 = CUDA-core
+ * split-K path, 2 = tensor-core (tcgen05) path, 0 = none yet. */
 pkv_status pkv_set_profile_events(pkv_ctx* ctx, void* start, void* stop);
 long long pkv_launch_count(const pkv_ctx* ctx);
+int pkv_attn_path(const pkv_ctx* ctx);
 
 #ifdef __cplusplus
 }

@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
             "pkv_decode_attn_noalloc": (i, [vp, vp, ctypes.POINTER(_KVCache), vp, i, vp, i, vp, i,
                                             ctypes.POINTER(_Window), f, vp, vp, vp]),
             "pkv_launch_count": (ctypes.c_longlong, [vp]),
+            "pkv_attn_path": (i, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -260,6 +261,10 @@ class Context:
 
     def pkv_launch_count(self) -> int:
         return int(lib().pkv_launch_count(self.h))
+
+    def pkv_attn_path(self) -> int:
+        """1 = CUDA-core attention path, 2 = tensor-core path (last attention call)."""
+        return int(lib().pkv_attn_path(self.h))
 
     def workspace(self, op: int, batch: int, max_len: int) -> torch.Tensor:
         n = self.pkv_workspace_bytes(op, batch, max_len)

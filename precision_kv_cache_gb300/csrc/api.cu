@@ -20,6 +20,7 @@ struct pkv_ctx {
   cudaEvent_t prof_start = nullptr;   // one-shot events around the next attention kernel
   cudaEvent_t prof_stop = nullptr;
   long long launches = 0;
+  int last_path = 0;                  // 1 = CUDA-core attention, 2 = tensor-core attention
 };
 
 namespace {
@@ -214,6 +215,7 @@ static pkv_status run_attention(pkv_ctx* c, pkv::AttnArgs& a, int max_entries, f
     int nl = 0;
     cudaError_t e = pkv_launch_attn_tc(a, c->num_sms, max_entries, out, out_lse, ws, st, e0, e1, &nl);
     c->launches += nl;
+    c->last_path = 2;
     return cuda_status(e);
   }
   int ns, ch;
@@ -222,6 +224,7 @@ static pkv_status run_attention(pkv_ctx* c, pkv::AttnArgs& a, int max_entries, f
   a.chunk = ch;
   a.part_o = (float*)ws;
   a.part_lse = (float*)((uint8_t*)ws + (size_t)a.n_groups * ns * a.H * a.D * 4);
+  c->last_path = 1;
   if (e0 && e1) cudaEventRecord(e0, st);
   cudaError_t e = pkv_launch_attn_simple(c->cfg.d, a, st);
   if (e0 && e1) cudaEventRecord(e1, st);
@@ -330,5 +333,7 @@ pkv_status pkv_set_profile_events(pkv_ctx* c, void* start, void* stop) {
 }
 
 long long pkv_launch_count(const pkv_ctx* c) { return c ? c->launches : 0; }
+
+int pkv_attn_path(const pkv_ctx* c) { return c ? c->last_path : 0; }
 
 }  // extern "C"

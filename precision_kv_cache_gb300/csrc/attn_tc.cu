@@ -1,10 +1,826 @@
-// Tensor-core attention: not enabled yet; every call takes the CUDA-core path.
+// Tensor-core decode / replay attention over the paged NVFP4 global KV and the
+// FP8 window, for sm_103a (tcgen05 MMA with TMEM operands and accumulators).
+//
+// What it computes: for every query row g (a decode sequence, or one replayed
+// token), all H <= 64 query heads attend the same K/V (MQA over one shared
+// latent - vLLM blog "Performances agentiques"): the global tokens of the
+// sequence, stored in NVFP4 64-token pages ("MegaAttention avec KV compressé
+// NVFP4"), then the FP8 window entries ([news] "Les particularités du modèle
+// lui-même"; replay: causal, clipped at s = H-128, "SWA bounded replay").
+// Output: a normalized partial (O, LSE) per (CTA, query row) segment, merged
+// by merge_tc_kernel ("flash-decoding": split along the sequence + LSE merge).
+//
+// Design (one persistent CTA per SM, 640 threads, warp-specialized):
+//   * work = 128-token tiles; each query row has ceil(L/128) NVFP4 tiles plus
+//     one window tile; the concatenated tile list is cut into one contiguous
+//     range per CTA (balanced to one tile).
+//   * warp 0 streams the raw pages of each tile (K and V: codes + scales) into
+//     two 2-slot shared-memory rings with 1-D bulk copies (TMA engine).
+//   * warps 4-7 (thread = token) dequantize K to f16 (exact: E2M1 x E4M3 has
+//     <= 6 significant bits) into TMEM, 64 channels at a time: the A operand of
+//     S^T = K Q^T  (M = 128 tokens, N = 64 heads, K = d).
+//   * warps 8-11 (thread = channel) dequantize V^T to f16 into TMEM, 128
+//     channels x 128 tokens at a time: the A operand of O^T = V^T P
+//     (M = 128 channels, N = 64 heads, K = 128 tokens).
+//   * warp 1 issues the MMAs (Q and P are the shared-memory B operands).
+//   * warps 12-19 run the online softmax on S (FP32, exp2, lazy max update
+//     with threshold 2^8), write P (f16, shared memory) and finally normalize
+//     O and write the partial result.
+// Every wait is bounded; on a timeout the CTA sets the error word, stops all
+// roles, drains its own copies / MMAs and frees its TMEM before returning.
 #include "attn_tc.h"
+#include "launch.h"
+#include "tc_ptx.cuh"
 
-cudaError_t pkv_attn_tc_init(int) { return cudaSuccess; }
-bool pkv_attn_tc_supported(const pkv::AttnArgs&, int) { return false; }
-size_t pkv_attn_tc_ws_bytes(int, int, int, int, int) { return 0; }
-cudaError_t pkv_launch_attn_tc(pkv::AttnArgs&, int, int, float*, float*, void*, cudaStream_t, cudaEvent_t,
-                               cudaEvent_t, int*) {
-  return cudaErrorNotSupported;
+namespace pkv {
+namespace tcattn {
+
+constexpr int TILE = 128;
+constexpr int NH = 64;                 // MMA N: query heads (zero-padded)
+constexpr int NTHREADS = 640;
+constexpr float TAU = 8.f;             // lazy rescale threshold (log2 units)
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+// TMEM columns (512 allocated)
+constexpr uint32_t COL_S = 0;          // S^T tile: 64 columns (fp32)
+constexpr uint32_t COL_O = 64;         // O^T: 4 chunks x 64 columns
+constexpr uint32_t COL_K = 320;        // K tile slots: 2 x 32 columns (64 channels, f16 pairs)
+constexpr uint32_t COL_V = 384;        // V^T tile slots: 2 x 64 columns (128 tokens, f16 pairs)
+
+template <int D>
+struct Cfg {
+  static constexpr int PAGE_DATA = PKV_PAGE * D / 2;
+  static constexpr int PAGE_SCALE = PKV_PAGE * D / 16;
+  static constexpr int PART = 2 * PAGE_DATA + 2 * PAGE_SCALE;     // K (or V) of two pages
+  static constexpr int Q_BYTES = NH * D * 2;
+  static constexpr int P_BYTES = TILE * NH * 2;
+  static constexpr int NKCH = D / 64;                             // K chunks of 64 channels
+  static constexpr int NVCH = D / 128;                            // V chunks of 128 channels
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_P + P_BYTES;                   // 2 K ring slots
+  static constexpr int OFF_V = OFF_K + 2 * PART;                  // 2 V ring slots
+  static constexpr int DYN = OFF_V + 2 * PART + 1024;             // + alignment slack
+  static_assert(PART % 1024 == 0, "ring slots stay 1024-aligned");
+};
+
+struct Shared {
+  uint64_t kfull_ring[2], kempty_ring[2], vfull_ring[2], vempty_ring[2];
+  uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
+  uint64_t s_full, s_empty, p_full, p_empty, q_full, o_empty, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  float m[NH];                 // running max per head (log2 units)
+  float alpha[NH];             // rescale factor of the current tile
+  float red[4][NH];            // cross-warp reductions
+};
+
+// ---------------------------------------------------------------- schedule
+struct Sched {
+  const int* tile_start;       // [n_groups + 1]
+  int n_groups, G;
+  long long T;
+};
+
+__device__ __forceinline__ long long cta_start(long long T, int G, int c) { return (T * c) / G; }
+
+// first group whose tiles reach past x
+__device__ __forceinline__ int group_of(const int* ts, int n, long long x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)ts[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct Unit {            // what a query row sees
+  int b, n_glob, n_win, row;
+  const uint8_t* wk;
+  const uint8_t* wv;
+};
+
+__device__ __forceinline__ Unit unit_of(const AttnArgs& a, int g) {
+  Unit u;
+  int b, ng, nw;
+  const uint8_t *wk, *wv;
+  unit_extent(a, g, &b, &ng, &nw, &wk, &wv);
+  u.b = b; u.n_glob = ng; u.n_win = nw; u.row = g; u.wk = wk; u.wv = wv;
+  return u;
+}
+
+// ---------------------------------------------------------------- plan kernel
+// tile_start[g] = sum over g' < g of (ceil(n_glob(g')/128) + 1); tile_start[n] = total
+__global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, int* tile_start) {
+  __shared__ int wsum[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < a.n_groups; base += 1024) {
+    const int g = base + threadIdx.x;
+    int n = 0;
+    if (g < a.n_groups) {
+      int b, ng, nw;
+      const uint8_t *wk, *wv;
+      unit_extent(a, g, &b, &ng, &nw, &wk, &wv);
+      n = (ng + TILE - 1) / TILE + 1;
+    }
+    int incl = n;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    int pre = carry;
+    for (int i = 0; i < w; ++i) pre += wsum[i];
+    if (g < a.n_groups) tile_start[g] = pre + incl - n;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = pre + incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) tile_start[a.n_groups] = carry;
+}
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
+
+__device__ __forceinline__ void fail(Shared& sh, int* err) {
+  sh.abort_flag = 1;
+  report(err, PKV_DEVERR_TIMEOUT);
+}
+
+// f16x2 of e2m1 byte b (two channels) times the f16x2 scale pair
+__device__ __forceinline__ uint32_t deq_pair(uint32_t byte, uint32_t s2) {
+  return tc::hmul2(tc::e2m1x2_to_f16x2(byte), s2);
+}
+
+__device__ __forceinline__ uint32_t f32_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
+__device__ __forceinline__ float f16_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+// Q of query row g -> shared memory: f16 (from bf16; exact for |q| in [2^-14, 65504]),
+// K-major with the 128-byte swizzle, heads >= H zero.  Called by the 256 softmax threads.
+template <int D>
+__device__ __forceinline__ void load_q(const AttnArgs& a, int g, uint8_t* sQ, int st) {
+  const uint16_t* qg = a.q + (size_t)g * a.H * D;
+  for (int v = st; v < NH * D / 8; v += 256) {
+    const int h = v / (D / 8), c8 = v % (D / 8);      // 8 channels per vector
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (h < a.H) {
+      const uint4 in = __ldg(reinterpret_cast<const uint4*>(qg + (size_t)h * D + 8 * c8));
+      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+      uint32_t r[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        r[i] = f32_to_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+      o = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+    const int atom = c8 >> 3, ch = c8 & 7;
+    *reinterpret_cast<uint4*>(sQ + atom * (NH * 128) + h * 128 + 16 * (ch ^ (h & 7))) = o;
+  }
+  tc::fence_proxy_async_smem();
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const int* __restrict__ tile_start,
+                                                              float* __restrict__ part_o,
+                                                              float* __restrict__ part_lse) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t dyn_raw[];
+  uint8_t* dyn = (uint8_t*)(((uintptr_t)dyn_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ Shared sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int G = gridDim.x, cta = blockIdx.x;
+  const long long T = tile_start[a.n_groups];
+  const long long x0 = cta_start(T, G, cta), x1 = cta_start(T, G, cta + 1);
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sh.kfull_ring[i], 1);
+      tc::mbar_init(&sh.kempty_ring[i], 4);
+      tc::mbar_init(&sh.vfull_ring[i], 1);
+      tc::mbar_init(&sh.vempty_ring[i], 4);
+      tc::mbar_init(&sh.kfull[i], 4);
+      tc::mbar_init(&sh.kempty[i], 1);
+      tc::mbar_init(&sh.vfull[i], 4);
+      tc::mbar_init(&sh.vempty[i], 1);
+    }
+    tc::mbar_init(&sh.s_full, 1);
+    tc::mbar_init(&sh.s_empty, 8);
+    tc::mbar_init(&sh.p_full, 8);
+    tc::mbar_init(&sh.p_empty, 1);
+    tc::mbar_init(&sh.q_full, 8);
+    tc::mbar_init(&sh.o_empty, 8);
+    tc::mbar_init(&sh.drain, 1);
+    sh.abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&sh.tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tbase = sh.tmem_base;
+  volatile int* abort_p = &sh.abort_flag;
+
+  uint8_t* sQ = dyn + C::OFF_Q;
+  uint8_t* sP = dyn + C::OFF_P;
+  uint8_t* sK = dyn + C::OFF_K;
+  uint8_t* sV = dyn + C::OFF_V;
+  const size_t pdb = (size_t)C::PAGE_DATA, psb = (size_t)C::PAGE_SCALE;
+
+  if (x0 < x1) {
+    // ======================================================== producer
+    if (warp == 0) {
+      if (lane == 0) {
+        int kit = 0, vit = 0;   // FP4 tiles whose K / V part was issued
+        bool ok = true;
+        long long x = x0;
+        int g = group_of(tile_start, a.n_groups, x);
+        while (x < x1 && ok) {
+          const Unit u = unit_of(a, g);
+          const int nt = tile_start[g + 1] - tile_start[g];
+          const int j0 = (int)(x - tile_start[g]);
+          const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+          for (int j = j0; j < j1 && ok; ++j) {
+            if (j == nt - 1) continue;      // window tile: read directly by the dequant warps
+            const int s = kit & 1;
+            const uint32_t ph = ((kit >> 1) & 1) ^ 1;
+            int pg[2];
+            const int npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
+            for (int q = 0; q < 2; ++q) {
+              int p = 0;
+              if (q < npg) {
+                p = a.page_table[(size_t)u.b * a.max_pages + 2 * j + q];
+                if (p < 0 || p >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); p = 0; }
+              }
+              pg[q] = p;
+            }
+            const uint32_t bytes = (uint32_t)npg * (C::PAGE_DATA + C::PAGE_SCALE);
+            // K part
+            if (!tc::mbar_wait(&sh.kempty_ring[s], ph, abort_p)) { fail(sh, a.err); ok = false; break; }
+            tc::mbar_arrive_expect_tx(&sh.kfull_ring[s], bytes);
+            uint8_t* dk = sK + s * C::PART;
+            for (int q = 0; q < npg; ++q) {
+              tc::bulk_g2s(dk + q * C::PAGE_DATA, a.cache.k_data + pg[q] * pdb, C::PAGE_DATA, &sh.kfull_ring[s]);
+              tc::bulk_g2s(dk + 2 * C::PAGE_DATA + q * C::PAGE_SCALE, a.cache.k_scale + pg[q] * psb,
+                           C::PAGE_SCALE, &sh.kfull_ring[s]);
+            }
+            ++kit;
+            // V part
+            if (!tc::mbar_wait(&sh.vempty_ring[s], ph, abort_p)) { fail(sh, a.err); ok = false; break; }
+            tc::mbar_arrive_expect_tx(&sh.vfull_ring[s], bytes);
+            uint8_t* dv = sV + s * C::PART;
+            for (int q = 0; q < npg; ++q) {
+              tc::bulk_g2s(dv + q * C::PAGE_DATA, a.cache.v_data + pg[q] * pdb, C::PAGE_DATA, &sh.vfull_ring[s]);
+              tc::bulk_g2s(dv + 2 * C::PAGE_DATA + q * C::PAGE_SCALE, a.cache.v_scale + pg[q] * psb,
+                           C::PAGE_SCALE, &sh.vfull_ring[s]);
+            }
+            ++vit;
+          }
+          x = tile_start[g] + j1;
+          ++g;
+        }
+        // drain: every copy issued must have landed before this CTA may exit
+        // (the last use of each slot; earlier uses were waited for by the consumers)
+        for (int k = (kit > 2 ? kit - 2 : 0); k < kit; ++k)
+          tc::mbar_wait(&sh.kfull_ring[k & 1], (k >> 1) & 1, abort_p, 1LL << 31);
+        for (int k = (vit > 2 ? vit - 2 : 0); k < vit; ++k)
+          tc::mbar_wait(&sh.vfull_ring[k & 1], (k >> 1) & 1, abort_p, 1LL << 31);
+      }
+    }
+    // ======================================================== MMA issuer
+    else if (warp == 1) {
+      if (lane == 0) {
+        const uint32_t idK = tc::idesc_f16(128, NH, false, false);   // B = Q, K-major
+        const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
+        const uint32_t qaddr = tc::smem_u32(sQ), paddr = tc::smem_u32(sP);
+        int kc = 0, vc = 0, ntile = 0, nitem = 0, npv = 0;
+        bool ok = true;
+        long long x = x0;
+        int g = group_of(tile_start, a.n_groups, x);
+        while (x < x1 && ok) {
+          const int nt = tile_start[g + 1] - tile_start[g];
+          const int j0 = (int)(x - tile_start[g]);
+          const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+          if (!tc::mbar_wait(&sh.q_full, nitem & 1, abort_p)) { fail(sh, a.err); ok = false; break; }
+          // software pipeline: QK(i), then PV(i-1)
+          for (int j = j0; j <= j1 && ok; ++j) {
+            if (j < j1) {
+              // ---- S^T = K Q^T
+              if (!tc::mbar_wait(&sh.s_empty, (ntile & 1) ^ 1, abort_p)) { fail(sh, a.err); ok = false; break; }
+              tc::tc_fence_after();
+              for (int c = 0; c < C::NKCH; ++c) {
+                const int slot = kc & 1;
+                if (!tc::mbar_wait(&sh.kfull[slot], (kc >> 1) & 1, abort_p)) { fail(sh, a.err); ok = false; break; }
+                tc::tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t bd = tc::sdesc_sw128(qaddr + c * (NH * 128) + k * 32, 16, 1024);
+                  tc::mma_ts(tbase + COL_S, tbase + COL_K + 32 * slot + 8 * k, bd, idK, (c | k) != 0);
+                }
+                tc::mma_commit(&sh.kempty[slot]);
+                ++kc;
+              }
+              if (!ok) break;
+              tc::mma_commit(&sh.s_full);
+              ++ntile;
+            }
+            if (j > j0) {
+              // ---- O^T += V^T P   for tile j-1
+              if (!tc::mbar_wait(&sh.p_full, npv & 1, abort_p)) { fail(sh, a.err); ok = false; break; }
+              if (j - 1 == j0) {
+                if (!tc::mbar_wait(&sh.o_empty, (nitem & 1) ^ 1, abort_p)) { fail(sh, a.err); ok = false; break; }
+              }
+              tc::tc_fence_after();
+              for (int c = 0; c < C::NVCH; ++c) {
+                const int slot = vc & 1;
+                if (!tc::mbar_wait(&sh.vfull[slot], (vc >> 1) & 1, abort_p)) { fail(sh, a.err); ok = false; break; }
+                tc::tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  const uint64_t bd = tc::sdesc_sw128(paddr + k * 2048, 8192, 1024);
+                  tc::mma_ts(tbase + COL_O + 64 * c, tbase + COL_V + 64 * slot + 8 * k, bd, idV,
+                             (j - 1 != j0) || (k != 0));
+                }
+                tc::mma_commit(&sh.vempty[slot]);
+                ++vc;
+              }
+              if (!ok) break;
+              tc::mma_commit(&sh.p_empty);
+              ++npv;
+            }
+          }
+          ++nitem;
+          x = tile_start[g] + j1;
+          ++g;
+        }
+        // drain outstanding MMAs before TMEM is freed
+        tc::mma_commit(&sh.drain);
+        tc::mbar_wait(&sh.drain, 0, abort_p, 1LL << 31);
+      }
+    }
+    // ======================================================== K dequantizer (thread = token)
+    else if (warp >= 4 && warp < 8) {
+      const int t = tid - 128;                       // token lane 0..127
+      const uint32_t lb = lane_base(warp);
+      int it = 0, kc = 0;
+      bool ok = true;
+      long long x = x0;
+      int g = group_of(tile_start, a.n_groups, x);
+      while (x < x1 && ok) {
+        const Unit u = unit_of(a, g);
+        const int nt = tile_start[g + 1] - tile_start[g];
+        const int j0 = (int)(x - tile_start[g]);
+        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        for (int j = j0; j < j1 && ok; ++j) {
+          const bool win = (j == nt - 1);
+          int s = 0;
+          bool valid;
+          const uint8_t *row = nullptr, *srow = nullptr;
+          int slot = 0;
+          if (!win) {
+            s = it & 1;
+            const bool w_ok = tc::mbar_wait(&sh.kfull_ring[s], (it >> 1) & 1, abort_p);
+            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
+            valid = (TILE * j + t) < u.n_glob;
+            const int q = t >> 6;
+            slot = t & 63;
+            row = sK + s * C::PART + q * C::PAGE_DATA + slot * (D / 2);
+            srow = sK + s * C::PART + 2 * C::PAGE_DATA + q * C::PAGE_SCALE + slot * 8;
+          } else {
+            valid = t < u.n_win;
+            row = u.wk + (size_t)t * D;
+          }
+          for (int c = 0; c < C::NKCH; ++c) {
+            const int ks = kc & 1;
+            const bool w_ok = tc::mbar_wait(&sh.kempty[ks], ((kc >> 1) & 1) ^ 1, abort_p);
+            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
+            uint32_t r[32];
+            if (!valid) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = 0u;
+            } else if (!win) {
+              constexpr int SW = (D / 32 < 8 ? D / 32 : 8) - 1;
+              const uint4 lo = *reinterpret_cast<const uint4*>(row + 16 * ((2 * c) ^ (slot & SW)));
+              const uint4 hi = *reinterpret_cast<const uint4*>(row + 16 * ((2 * c + 1) ^ (slot & SW)));
+              const uint32_t sc = *reinterpret_cast<const uint32_t*>(srow + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
+              const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+              for (int bk = 0; bk < 4; ++bk) {
+                const uint32_t sb = (sc >> (8 * bk)) & 0xFFu;
+                const uint32_t s2 = tc::e4m3x2_to_f16x2(sb | (sb << 8));
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const uint32_t wd = w[2 * bk + (i >> 2)];
+                  r[8 * bk + i] = deq_pair((wd >> (8 * (i & 3))) & 0xFFu, s2);
+                }
+              }
+            } else {
+              const uint4* p4 = reinterpret_cast<const uint4*>(row + 64 * c);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const uint4 v = __ldg(p4 + q4);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  r[8 * q4 + 2 * i] = tc::e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+                  r[8 * q4 + 2 * i + 1] = tc::e4m3x2_to_f16x2(w[i] >> 16);
+                }
+              }
+            }
+            tc::tmem_st32(tbase + lb + COL_K + 32 * ks, r);
+            tc::tc_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.kfull[ks]);
+            ++kc;
+          }
+          if (!ok) break;
+          if (!win) {
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.kempty_ring[s]);
+            ++it;
+          }
+        }
+        x = tile_start[g] + j1;
+        ++g;
+      }
+    }
+    // ======================================================== V dequantizer (thread = channel)
+    else if (warp >= 8 && warp < 12) {
+      const int dl = tid - 256;                      // channel lane 0..127 within a chunk
+      const uint32_t lb = lane_base(warp);
+      int it = 0, vc = 0;
+      bool ok = true;
+      long long x = x0;
+      int g = group_of(tile_start, a.n_groups, x);
+      while (x < x1 && ok) {
+        const Unit u = unit_of(a, g);
+        const int nt = tile_start[g + 1] - tile_start[g];
+        const int j0 = (int)(x - tile_start[g]);
+        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        for (int j = j0; j < j1 && ok; ++j) {
+          const bool win = (j == nt - 1);
+          int s = 0;
+          int nvalid;
+          if (!win) {
+            s = it & 1;
+            const bool w_ok = tc::mbar_wait(&sh.vfull_ring[s], (it >> 1) & 1, abort_p);
+            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
+            nvalid = min(TILE, u.n_glob - TILE * j);
+          } else {
+            nvalid = u.n_win;
+          }
+          for (int c = 0; c < C::NVCH; ++c) {
+            const int vs = vc & 1;
+            const bool w_ok = tc::mbar_wait(&sh.vempty[vs], ((vc >> 1) & 1) ^ 1, abort_p);
+            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
+            const int d = 128 * c + dl;
+            for (int half = 0; half < 2; ++half) {       // tokens 64*half .. 64*half+63
+              uint32_t r[32];
+              if (!win) {
+                const uint8_t* base = sV + s * C::PART;
+                const uint32_t* wd = reinterpret_cast<const uint32_t*>(base + half * C::PAGE_DATA) + d;
+                const uint8_t* sc = base + 2 * C::PAGE_DATA + half * C::PAGE_SCALE + (d >> 4) * PKV_PAGE;
+#pragma unroll
+                for (int o = 0; o < 8; ++o) {
+                  const uint32_t w = wd[o * D];
+                  const uint2 s8 = *reinterpret_cast<const uint2*>(sc + 8 * o);
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const uint32_t sw = (i < 2 ? s8.x : s8.y) >> (16 * (i & 1));
+                    const uint32_t s2 = tc::e4m3x2_to_f16x2(sw & 0xFFFFu);
+                    r[4 * o + i] = deq_pair((w >> (8 * i)) & 0xFFu, s2);
+                  }
+                }
+              } else {
+                const uint8_t* col = u.wv + d;
+#pragma unroll 8
+                for (int i = 0; i < 32; ++i) {
+                  const int e = 64 * half + 2 * i;
+                  const uint32_t b0 = __ldg(col + (size_t)e * D), b1 = __ldg(col + (size_t)(e + 1) * D);
+                  r[i] = tc::e4m3x2_to_f16x2(b0 | (b1 << 8));
+                }
+              }
+              // zero the tokens beyond the valid count (their K rows are zero too)
+              const int t0 = 64 * half;
+              if (t0 + 64 > nvalid) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const int tt = t0 + 2 * i;
+                  if (tt >= nvalid) r[i] = 0u;
+                  else if (tt + 1 >= nvalid) r[i] &= 0xFFFFu;
+                }
+              }
+              tc::tmem_st32(tbase + lb + COL_V + 64 * vs + 32 * half, r);
+            }
+            tc::tc_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
+            ++vc;
+          }
+          if (!ok) break;
+          if (!win) {
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.vempty_ring[s]);
+            ++it;
+          }
+        }
+        x = tile_start[g] + j1;
+        ++g;
+      }
+    }
+    // ======================================================== softmax + epilogue
+    else if (warp >= 12) {
+      const int st = tid - 384;                 // 0..255
+      const int hh = (warp - 12) >> 2;          // head half: heads 32*hh .. 32*hh+31
+      const int q4 = warp & 3;                  // TMEM lane quarter
+      const int t = 32 * q4 + lane;             // token lane (S) / channel lane (O)
+      const uint32_t lb = lane_base(warp);
+      const float ratio = a.tw_v / a.cache.ts_v;
+      int ntile = 0, npv = 0;
+      bool ok = true;
+      long long x = x0;
+      int g = group_of(tile_start, a.n_groups, x);
+      load_q<D>(a, g, sQ, st);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sh.q_full);
+      while (x < x1 && ok) {
+        const Unit u = unit_of(a, g);
+        const int nt = tile_start[g + 1] - tile_start[g];
+        const int j0 = (int)(x - tile_start[g]);
+        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        const long long xn = tile_start[g] + j1;
+        if (st < NH) sh.m[st] = -INFINITY;
+        tc::named_bar(1, 256);
+        float l[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) l[i] = 0.f;
+        for (int j = j0; j < j1; ++j) {
+          const bool win = (j == nt - 1);
+          const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
+          const float zs = a.scale * (win ? a.tw_k : a.cache.ts_k) * LOG2E;
+          // ---- S tile
+          bool w_ok = tc::mbar_wait(&sh.s_full, ntile & 1, abort_p);
+          if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
+          tc::tc_fence_after();
+          float z[32];
+          {
+            uint32_t r[32];
+            tc::tmem_ld32(tbase + lb + COL_S + 32 * hh, r);
+            tc::tc_wait_ld();
+            const bool valid = t < nvalid;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = valid ? __uint_as_float(r[i]) * zs : -INFINITY;
+          }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sh.s_empty);
+          ++ntile;
+          // all S of this item consumed: Q of the next item may replace this one
+          if (j == j1 - 1 && xn < x1) {
+            load_q<D>(a, g + 1, sQ, st);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.q_full);
+          }
+          bool need = false;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) need |= z[i] > sh.m[32 * hh + i] + TAU;
+          const bool any = tc::named_bar_or(2, 256, need);
+          // P.V of the previous tile must be done before O is rescaled or P rewritten
+          if (j > j0) {
+            w_ok = tc::mbar_wait(&sh.p_empty, npv & 1, abort_p);
+            if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
+            ++npv;
+          }
+          if (any) {
+            // tile max per head: over the 32 tokens of the warp, then the 4 lane quarters
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float v = z[i];
+#pragma unroll
+              for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+              if (lane == 0) sh.red[q4][32 * hh + i] = v;
+            }
+            tc::named_bar(1, 256);
+            if (q4 == 0) {
+              const int h = 32 * hh + lane;
+              const float tm = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
+              const float mo = sh.m[h];
+              const float mn = fmaxf(mo, tm);
+              sh.alpha[h] = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
+              sh.m[h] = mn;
+            }
+            tc::named_bar(1, 256);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) l[i] *= sh.alpha[32 * hh + i];
+            if (j > j0) {
+              // O^T columns of this head half, every channel chunk, times alpha
+              tc::tc_fence_after();
+              for (int c = 0; c < C::NVCH; ++c) {
+                uint32_t o[32];
+                tc::tmem_ld32(tbase + lb + COL_O + 64 * c + 32 * hh, o);
+                tc::tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  o[i] = __float_as_uint(__uint_as_float(o[i]) * sh.alpha[32 * hh + i]);
+                tc::tmem_st32(tbase + lb + COL_O + 64 * c + 32 * hh, o);
+              }
+              tc::tc_wait_st();
+            }
+          }
+          // ---- P = exp2(z - m)  (f16; l sums the rounded values)
+          const float pr = win ? ratio : 1.f;
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float m0 = sh.m[32 * hh + 2 * i], m1 = sh.m[32 * hh + 2 * i + 1];
+            const float p0 = z[2 * i] == -INFINITY ? 0.f : exp2f(z[2 * i] - m0);
+            const float p1 = z[2 * i + 1] == -INFINITY ? 0.f : exp2f(z[2 * i + 1] - m1);
+            const uint32_t h2 = f32_to_f16x2(p0, p1);
+            const float q0 = f16_lo(h2), q1 = f16_hi(h2);
+            l[2 * i] += q0;
+            l[2 * i + 1] += q1;
+            pk[i] = win ? f32_to_f16x2(q0 * pr, q1 * pr) : h2;
+          }
+          // row t of P (MN-major, 128-byte swizzle): heads 32*hh .. +31 = 4 chunks of 16 B
+          uint8_t* prow = sP + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(prow + 16 * ((4 * hh + k) ^ (t & 7))) =
+                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          tc::fence_proxy_async_smem();
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sh.p_full);
+        }
+        if (!ok) break;
+        // ---- end of the item: wait for its last P.V, then write the partial
+        bool w_ok = tc::mbar_wait(&sh.p_empty, npv & 1, abort_p);
+        if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
+        ++npv;
+        tc::tc_fence_after();
+        // l over all 128 token lanes
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float v = l[i];
+#pragma unroll
+          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) sh.red[q4][32 * hh + i] = v;
+        }
+        tc::named_bar(1, 256);
+        const size_t prow_i = (size_t)cta + (size_t)g;          // partial row of this segment
+        float* po = part_o + prow_i * a.H * D;
+        for (int c = 0; c < C::NVCH; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(tbase + lb + COL_O + 64 * c + 32 * hh, o);
+          tc::tc_wait_ld();
+          const int d = 128 * c + t;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int h = 32 * hh + i;
+            if (h < a.H) {
+              const float lh = sh.red[0][h] + sh.red[1][h] + sh.red[2][h] + sh.red[3][h];
+              po[(size_t)h * D + d] = lh > 0.f ? __uint_as_float(o[i]) * (a.cache.ts_v / lh) : 0.f;
+            }
+          }
+        }
+        if (st < a.H) {
+          const float lh = sh.red[0][st] + sh.red[1][st] + sh.red[2][st] + sh.red[3][st];
+          part_lse[prow_i * a.H + st] = lh > 0.f ? (sh.m[st] + log2f(lh)) * LN2 : -INFINITY;
+        }
+        tc::tc_fence_before();
+        tc::named_bar(1, 256);                 // sh.red / sh.m reads done before the next item resets them
+        if (lane == 0) tc::mbar_arrive(&sh.o_empty);
+        x = xn;
+        ++g;
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tbase, 512);
+}
+
+// Merge the segment partials of each query row: rows cta+g for every CTA whose
+// (non-empty) tile range meets g's tiles.  One block per (g, h).
+__global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups, int G, int H, int D,
+                                const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                                float* __restrict__ out, float* __restrict__ out_lse) {
+  const int g = blockIdx.x / H, h = blockIdx.x % H;
+  const long long T = tile_start[n_groups];
+  const long long first = tile_start[g], last = tile_start[g + 1] - 1;
+  const int c_lo = (int)(((first + 1) * G - 1) / T), c_hi = (int)(((last + 1) * G - 1) / T);
+  float m = -INFINITY;
+  for (int c = c_lo; c <= c_hi; ++c) {
+    if (cta_start(T, G, c) == cta_start(T, G, c + 1)) continue;
+    m = fmaxf(m, part_lse[((size_t)c + g) * H + h]);
+  }
+  float sum = 0.f;
+  if (m != -INFINITY)
+    for (int c = c_lo; c <= c_hi; ++c) {
+      if (cta_start(T, G, c) == cta_start(T, G, c + 1)) continue;
+      sum += exp2f((part_lse[((size_t)c + g) * H + h] - m) * LOG2E);
+    }
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float acc = 0.f;
+    if (m != -INFINITY) {
+      for (int c = c_lo; c <= c_hi; ++c) {
+        if (cta_start(T, G, c) == cta_start(T, G, c + 1)) continue;
+        const size_t r = (size_t)c + g;
+        const float ls = part_lse[r * H + h];
+        if (ls != -INFINITY) acc += exp2f((ls - m) * LOG2E) * part_o[(r * H + h) * D + d];
+      }
+      acc /= sum;
+    }
+    out[((size_t)g * H + h) * D + d] = acc;
+  }
+  if (threadIdx.x == 0 && out_lse) out_lse[(size_t)g * H + h] = m != -INFINITY ? m + logf(sum) : -INFINITY;
+}
+
+}  // namespace tcattn
+}  // namespace pkv
+
+// ---------------------------------------------------------------- host side
+namespace {
+template <int D>
+cudaError_t set_attrs() {
+  return cudaFuncSetAttribute(pkv::tcattn::attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              pkv::tcattn::Cfg<D>::DYN);
+}
+}  // namespace
+
+cudaError_t pkv_attn_tc_init(int) {
+  cudaError_t e = set_attrs<128>();
+  if (e == cudaSuccess) e = set_attrs<256>();
+  if (e == cudaSuccess) e = set_attrs<512>();
+  return e;
+}
+
+bool pkv_attn_tc_supported(const pkv::AttnArgs& a, int d) {
+  if (a.sel) return false;
+  if (d != 128 && d != 256 && d != 512) return false;
+  if (a.H < 1 || a.H > pkv::tcattn::NH) return false;
+  // the window's V scale is folded into P (f16): keep tw_v / ts_v within 2^+-7
+  const float r = a.tw_v / a.cache.ts_v;
+  if (!(r >= 1.f / 128.f && r <= 128.f)) return false;
+  return true;
+}
+
+// persistent grid: one CTA per SM, or fewer when there are fewer tiles than SMs
+static int tc_grid(int num_sms, int n_groups, int max_entries) {
+  const long long glob = max_entries > PKV_WINDOW ? max_entries - PKV_WINDOW : 0;
+  const long long tmax = (long long)n_groups * ((glob + 127) / 128 + 1);
+  return (int)(tmax < num_sms ? tmax : num_sms);
+}
+
+size_t pkv_attn_tc_ws_bytes(int num_sms, int H, int D, int n_groups, int max_entries) {
+  const size_t rows = (size_t)tc_grid(num_sms, n_groups, max_entries) + n_groups;
+  return 256 + ((size_t)(n_groups + 1) * 4 + 255) / 256 * 256 + rows * H * D * 4 + rows * H * 4 + 256;
+}
+
+cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, float* out, float* out_lse,
+                               void* ws, cudaStream_t st, cudaEvent_t e0, cudaEvent_t e1, int* n_launches) {
+  using namespace pkv::tcattn;
+  uint8_t* p = (uint8_t*)ws;
+  int* tile_start = (int*)p;
+  p += ((size_t)(a.n_groups + 1) * 4 + 255) / 256 * 256;
+  const int G = tc_grid(num_sms, a.n_groups, max_entries);
+  const size_t rows = (size_t)G + a.n_groups;
+  float* part_o = (float*)p;
+  p += rows * a.H * a.D * 4;
+  float* part_lse = (float*)p;
+  plan_kernel<<<1, 1024, 0, st>>>(a, tile_start);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (e0 && e1) cudaEventRecord(e0, st);
+  switch (a.D) {
+    case 128: attn_tc_kernel<128><<<G, NTHREADS, Cfg<128>::DYN, st>>>(a, tile_start, part_o, part_lse); break;
+    case 256: attn_tc_kernel<256><<<G, NTHREADS, Cfg<256>::DYN, st>>>(a, tile_start, part_o, part_lse); break;
+    case 512: attn_tc_kernel<512><<<G, NTHREADS, Cfg<512>::DYN, st>>>(a, tile_start, part_o, part_lse); break;
+    default: return cudaErrorInvalidValue;
+  }
+  e = cudaGetLastError();
+  if (e0 && e1) cudaEventRecord(e1, st);
+  if (e != cudaSuccess) return e;
+  merge_tc_kernel<<<a.n_groups * a.H, 128, 0, st>>>(tile_start, a.n_groups, G, a.H, a.D, part_o, part_lse, out,
+                                                    out_lse);
+  *n_launches = 3;
+  return cudaGetLastError();
 }
