@@ -259,7 +259,7 @@ def run_gpu(args, rank, world, pool):
         wts = torch.from_numpy(wl.index_w()).to(dev)
         sel = torch.empty(B, wl.topk, dtype=torch.int32, device=dev)
         ws_s = ctx.workspace(P.OP_SCORE_TOPK, B, pt.shape[1] * 64)
-        ws = ctx.workspace(P.OP_DECODE, B, wl.topk)
+        ws = ctx.workspace(P.OP_DECODE_SPARSE, B, wl.topk)
     elif not wl.replay:
         ws = ctx.workspace(P.OP_DECODE, B, pt.shape[1] * 64)
     if wl.append:

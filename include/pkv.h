@@ -111,7 +111,7 @@ typedef struct {
 } pkv_window;
 
 /* Operations for pkv_workspace_bytes. */
-enum { PKV_OP_DECODE = 1, PKV_OP_SCORE_TOPK = 2, PKV_OP_REPLAY = 3 };
+enum { PKV_OP_DECODE = 1, PKV_OP_SCORE_TOPK = 2, PKV_OP_REPLAY = 3, PKV_OP_DECODE_SPARSE = 4 };
 
 /* Create a context on CUDA device `device` (made current for the call).
  * Allocates the context's 4-byte device error word.  Returns
@@ -120,9 +120,12 @@ pkv_status pkv_init(const pkv_config* cfg, int device, pkv_ctx** out);
 void pkv_destroy(pkv_ctx* ctx);
 
 /* Bytes of scratch (the `ws` argument) an op needs for `batch` sequences.
- * max_len: PKV_OP_DECODE - max_pages*64 of the page table (sparse path: k);
+ * max_len: PKV_OP_DECODE - max_pages*64 of the page table;
  * PKV_OP_REPLAY - max_pages*64 (batch = sequences, 128 queries each);
- * PKV_OP_SCORE_TOPK - max_pages*64 (the score buffer and radix-select state). */
+ * PKV_OP_SCORE_TOPK - max_pages*64 (the score buffer and radix-select state);
+ * PKV_OP_DECODE_SPARSE - k, the number of selected positions per sequence
+ * (decode over sel_idx: the selected tokens are first gathered into compact
+ * pages inside the workspace). */
 size_t pkv_workspace_bytes(const pkv_ctx* ctx, int op, int batch, int max_len);
 
 /* NVFP4 quantize + append ("MegaAttention avec KV compressé NVFP4": the cache

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, "libpkv.so")
 PAGE = 64
 WINDOW = 128
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_BAD_PAGE, ERR_TIMEOUT, ERR_WORKSPACE = range(7)
-OP_DECODE, OP_SCORE_TOPK, OP_REPLAY = 1, 2, 3
+OP_DECODE, OP_SCORE_TOPK, OP_REPLAY, OP_DECODE_SPARSE = 1, 2, 3, 4
 
 
 class PkvError(RuntimeError):
@@ -219,7 +219,8 @@ class Context:
         B = seq_len.shape[0]
         k = sel_idx.shape[1] if sel_idx is not None else 0
         if ws is None:
-            ws = self.workspace(OP_DECODE, B, k if sel_idx is not None else page_table.shape[1] * PAGE)
+            ws = (self.workspace(OP_DECODE_SPARSE, B, k) if sel_idx is not None
+                  else self.workspace(OP_DECODE, B, page_table.shape[1] * PAGE))
         c = cache._c()
         w = win._c()
         _check(lib().pkv_decode_attn(self.h, _p(q), ctypes.byref(c), _p(page_table), page_table.shape[1],

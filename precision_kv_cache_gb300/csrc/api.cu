@@ -120,7 +120,11 @@ pkv_status pkv_init(const pkv_config* cfg, int device, pkv_ctx** out) {
   }
   if (cudaMalloc(&c->d_err, sizeof(int)) != cudaSuccess) { delete c; return PKV_ERR_CUDA; }
   if (cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) { cudaFree(c->d_err); delete c; return PKV_ERR_CUDA; }
-  if (pkv_attn_tc_init(device) != cudaSuccess) { cudaFree(c->d_err); delete c; return PKV_ERR_CUDA; }
+  if (pkv_attn_tc_init(device) != cudaSuccess || pkv_score_tc_init() != cudaSuccess) {
+    cudaFree(c->d_err);
+    delete c;
+    return PKV_ERR_CUDA;
+  }
   *out = c;
   return PKV_OK;
 }
@@ -137,8 +141,13 @@ size_t pkv_workspace_bytes(const pkv_ctx* c, int op, int batch, int max_len) {
   switch (op) {
     case PKV_OP_DECODE: return attn_ws_bytes(c, batch, max_len + PKV_WINDOW);
     case PKV_OP_REPLAY: return attn_ws_bytes(c, batch * PKV_WINDOW, max_len + PKV_WINDOW);
+    case PKV_OP_DECODE_SPARSE: {
+      const int kp = (max_len + PKV_PAGE - 1) / PKV_PAGE * PKV_PAGE;
+      return pkv_gather_ws_bytes(c->cfg.d, batch, max_len) + 256 + attn_ws_bytes(c, batch, kp + PKV_WINDOW);
+    }
     case PKV_OP_SCORE_TOPK:
-      return (size_t)batch * (size_t)max_len * 4 + pkv_topk_ws_bytes(batch, PKV_TOPK_MAX_K) + 256;
+      return (size_t)batch * (size_t)max_len * 4 + 256 + pkv_score_tc_ws_bytes(batch) +
+             pkv_topk_ws_bytes(batch, PKV_TOPK_MAX_K) + 256;
   }
   return 0;
 }
@@ -197,9 +206,11 @@ pkv_status pkv_score_topk(pkv_ctx* c, const uint8_t* q_idx, float tq, const floa
   if (!scores) scores = (float*)p;
   p += (size_t)B * Lmax * 4;
   p = (uint8_t*)(((uintptr_t)p + 255) & ~(uintptr_t)255);
-  c->launches += 1 + PKV_TOPK_LAUNCHES;
-  cudaError_t e = pkv_launch_score_simple(q_idx, tq, w, *ic, page_table, max_pages, seq_len, B,
-                                          c->cfg.n_index_heads, scores, Lmax, c->d_err, st);
+  void* plan = p;
+  p += pkv_score_tc_ws_bytes(B);
+  c->launches += 2 + PKV_TOPK_LAUNCHES;
+  cudaError_t e = pkv_launch_score_tc(q_idx, tq, w, *ic, page_table, max_pages, seq_len, B, c->cfg.n_index_heads,
+                                      scores, Lmax, plan, c->num_sms, c->d_err, st);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return cuda_status(pkv_launch_topk(scores, Lmax, seq_len, B, k, out_idx, p, st));
 }
@@ -264,7 +275,29 @@ pkv_status pkv_decode_attn(pkv_ctx* c, const void* q, const pkv_kv_cache* cache,
   a.n_groups = B;
   a.replay = 0;
   a.err = c->d_err;
-  const int max_entries = (sel_idx ? k : max_pages * PKV_PAGE) + PKV_WINDOW;
+  if (sel_idx) {
+    // the selected tokens are gathered into compact pages, then attended as a dense segment
+    const size_t need = pkv_workspace_bytes(c, PKV_OP_DECODE_SPARSE, B, k);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return PKV_ERR_WORKSPACE;
+    pkv::AttnArgs ad = a;
+    ad.sel = nullptr;
+    ad.k = 0;
+    const size_t gbytes = (pkv_gather_ws_bytes(c->cfg.d, B, k) + 255) / 256 * 256;
+    pkv_kv_cache compact{};
+    int32_t *cpt = nullptr, *clen = nullptr;
+    int npb = 0;
+    c->launches += 2;
+    cudaError_t e = pkv_launch_gather(c->cfg.d, *cache, page_table, max_pages, sel_idx, B, k, ws, &compact, &cpt,
+                                      &clen, &npb, c->d_err, (cudaStream_t)stream);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    ad.cache = compact;
+    ad.page_table = cpt;
+    ad.max_pages = npb;
+    ad.lens = clen;
+    return run_attention(c, ad, npb * PKV_PAGE + PKV_WINDOW, out, out_lse, (uint8_t*)ws + gbytes, ws_bytes - gbytes,
+                         (cudaStream_t)stream);
+  }
+  const int max_entries = max_pages * PKV_PAGE + PKV_WINDOW;
   return run_attention(c, a, max_entries, out, out_lse, ws, ws_bytes, (cudaStream_t)stream);
 }
 

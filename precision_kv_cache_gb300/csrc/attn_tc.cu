@@ -14,16 +14,16 @@
 //   * work = 128-token tiles; each query row has ceil(L/128) NVFP4 tiles plus
 //     one window tile; the concatenated tile list is cut into one contiguous
 //     range per CTA (balanced to one tile).
-//   * warp 0 streams the raw pages of each tile (K and V: codes + scales) into
+//   * warp 16 streams the raw pages of each tile (K and V: codes + scales) into
 //     two 2-slot shared-memory rings with 1-D bulk copies (TMA engine).
-//   * warps 4-7 (thread = token) dequantize K to f16 (exact: E2M1 x E4M3 has
+//   * warps 0-3 (thread = token) dequantize K to f16 (exact: E2M1 x E4M3 has
 //     <= 6 significant bits) into TMEM, 64 channels at a time: the A operand of
 //     S^T = K Q^T  (M = 128 tokens, N = 64 heads, K = d).
-//   * warps 8-11 (thread = channel) dequantize V^T to f16 into TMEM, 128
+//   * warps 4-7 (thread = channel) dequantize V^T to f16 into TMEM, 128
 //     channels x 128 tokens at a time: the A operand of O^T = V^T P
 //     (M = 128 channels, N = 64 heads, K = 128 tokens).
-//   * warp 1 issues the MMAs (Q and P are the shared-memory B operands).
-//   * warps 12-19 run the online softmax on S (FP32, exp2, lazy max update
+//   * warp 17 issues the MMAs (Q and P are the shared-memory B operands).
+//   * warps 8-15 run the online softmax on S (FP32, exp2, lazy max update
 //     with threshold 2^8), write P (f16, shared memory) and finally normalize
 //     O and write the partial result.
 // Every wait is bounded; on a timeout the CTA sets the error word, stops all
@@ -37,41 +37,44 @@ namespace tcattn {
 
 constexpr int TILE = 128;
 constexpr int NH = 64;                 // MMA N: query heads (zero-padded)
-constexpr int NTHREADS = 640;
+constexpr int NTHREADS = 640;       // 20 warps (5 warpgroups)
 constexpr float TAU = 8.f;             // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
 // TMEM columns (512 allocated)
-constexpr uint32_t COL_S = 0;          // S^T tile: 64 columns (fp32)
-constexpr uint32_t COL_O = 64;         // O^T: 4 chunks x 64 columns
-constexpr uint32_t COL_K = 320;        // K tile slots: 2 x 32 columns (64 channels, f16 pairs)
-constexpr uint32_t COL_V = 384;        // V^T tile slots: 2 x 64 columns (128 tokens, f16 pairs)
+constexpr uint32_t COL_S = 0;          // S^T tiles: 2 slots x 64 columns (fp32)
+constexpr uint32_t COL_O = 128;        // O^T: 4 chunks x 64 columns
+constexpr uint32_t COL_K = 384;        // K tile slots: 2 x 32 columns (64 channels, f16 pairs)
+constexpr uint32_t COL_V = 448;        // V^T tile slots: 2 x 32 columns (64 tokens, f16 pairs)
+
+constexpr int NKR = 3;                 // K ring: page slots
+constexpr int NVR = 4;                 // V ring: page slots
 
 template <int D>
 struct Cfg {
   static constexpr int PAGE_DATA = PKV_PAGE * D / 2;
   static constexpr int PAGE_SCALE = PKV_PAGE * D / 16;
-  static constexpr int PART = 2 * PAGE_DATA + 2 * PAGE_SCALE;     // K (or V) of two pages
+  static constexpr int PSLOT = PAGE_DATA + PAGE_SCALE;            // one page of K (or V): codes + scales
   static constexpr int Q_BYTES = NH * D * 2;
   static constexpr int P_BYTES = TILE * NH * 2;
   static constexpr int NKCH = D / 64;                             // K chunks of 64 channels
   static constexpr int NVCH = D / 128;                            // V chunks of 128 channels
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_P = OFF_Q + Q_BYTES;
-  static constexpr int OFF_K = OFF_P + P_BYTES;                   // 2 K ring slots
-  static constexpr int OFF_V = OFF_K + 2 * PART;                  // 2 V ring slots
-  static constexpr int DYN = OFF_V + 2 * PART + 1024;             // + alignment slack
-  static_assert(PART % 1024 == 0, "ring slots stay 1024-aligned");
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;                   // 2 P buffers
+  static constexpr int OFF_K = OFF_P + 2 * P_BYTES;               // K ring
+  static constexpr int OFF_V = OFF_K + NKR * PSLOT;               // V ring
+  static constexpr int DYN = OFF_V + NVR * PSLOT + 1024;          // + alignment slack
+  static_assert(OFF_K % 1024 == 0, "operand tiles stay 1024-aligned");
 };
 
 struct Shared {
-  uint64_t kfull_ring[2], kempty_ring[2], vfull_ring[2], vempty_ring[2];
+  uint64_t kr_full[NKR], kr_empty[NKR], vr_full[NVR], vr_empty[NVR];
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
-  uint64_t s_full, s_empty, p_full, p_empty, q_full, o_empty, drain;
+  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], q_full, o_empty, drain;
   uint32_t tmem_base;
   int abort_flag;
-  float m[NH];                 // running max per head (log2 units)
+  alignas(16) float m[NH];     // running max per head (log2 units)
   float alpha[NH];             // rescale factor of the current tile
   float red[4][NH];            // cross-warp reductions
 };
@@ -170,7 +173,7 @@ __device__ __forceinline__ float f16_hi(uint32_t v) { return __half2float(__usho
 // Q of query row g -> shared memory: f16 (from bf16; exact for |q| in [2^-14, 65504]),
 // K-major with the 128-byte swizzle, heads >= H zero.  Called by the 256 softmax threads.
 template <int D>
-__device__ __forceinline__ void load_q(const AttnArgs& a, int g, uint8_t* sQ, int st) {
+__device__ __noinline__ void load_q(const AttnArgs& a, int g, uint8_t* sQ, int st) {
   const uint16_t* qg = a.q + (size_t)g * a.H * D;
   for (int v = st; v < NH * D / 8; v += 256) {
     const int h = v / (D / 8), c8 = v % (D / 8);      // 8 channels per vector
@@ -206,27 +209,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   const long long x0 = cta_start(T, G, cta), x1 = cta_start(T, G, cta + 1);
 
   if (tid == 0) {
+    for (int i = 0; i < NKR; ++i) {
+      tc::mbar_init(&sh.kr_full[i], 1);
+      tc::mbar_init(&sh.kr_empty[i], 4);
+    }
+    for (int i = 0; i < NVR; ++i) {
+      tc::mbar_init(&sh.vr_full[i], 1);
+      tc::mbar_init(&sh.vr_empty[i], 4);
+    }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sh.kfull_ring[i], 1);
-      tc::mbar_init(&sh.kempty_ring[i], 4);
-      tc::mbar_init(&sh.vfull_ring[i], 1);
-      tc::mbar_init(&sh.vempty_ring[i], 4);
       tc::mbar_init(&sh.kfull[i], 4);
       tc::mbar_init(&sh.kempty[i], 1);
       tc::mbar_init(&sh.vfull[i], 4);
       tc::mbar_init(&sh.vempty[i], 1);
     }
-    tc::mbar_init(&sh.s_full, 1);
-    tc::mbar_init(&sh.s_empty, 8);
-    tc::mbar_init(&sh.p_full, 8);
-    tc::mbar_init(&sh.p_empty, 1);
+    tc::mbar_init(&sh.s_full[0], 1);
+    tc::mbar_init(&sh.s_full[1], 1);
+    tc::mbar_init(&sh.s_empty[0], 8);
+    tc::mbar_init(&sh.s_empty[1], 8);
+    tc::mbar_init(&sh.p_full[0], 8);
+    tc::mbar_init(&sh.p_full[1], 8);
+    tc::mbar_init(&sh.p_empty[0], 1);
+    tc::mbar_init(&sh.p_empty[1], 1);
     tc::mbar_init(&sh.q_full, 8);
     tc::mbar_init(&sh.o_empty, 8);
     tc::mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 17) {
     tc::tmem_alloc(&sh.tmem_base, 512);
     tc::tmem_relinquish();
   }
@@ -234,6 +245,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tbase = sh.tmem_base;
+
   volatile int* abort_p = &sh.abort_flag;
 
   uint8_t* sQ = dyn + C::OFF_Q;
@@ -243,10 +255,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   const size_t pdb = (size_t)C::PAGE_DATA, psb = (size_t)C::PAGE_SCALE;
 
   if (x0 < x1) {
-    // ======================================================== producer
-    if (warp == 0) {
+    // ======================================================== producers
+    // warp 16 streams K pages (codes + scales) into the K ring, warp 18 V pages
+    // into the V ring, one page per slot, with 1-D bulk copies.
+    if (warp == 16 || warp == 18) {
       if (lane == 0) {
-        int kit = 0, vit = 0;   // FP4 tiles whose K / V part was issued
+        const bool isK = (warp == 16);
+        const int nslot = isK ? NKR : NVR;
+        uint64_t* fullb = isK ? sh.kr_full : sh.vr_full;
+        uint64_t* emptyb = isK ? sh.kr_empty : sh.vr_empty;
+        uint8_t* ring = isK ? sK : sV;
+        const uint8_t* gdata = isK ? a.cache.k_data : a.cache.v_data;
+        const uint8_t* gscale = isK ? a.cache.k_scale : a.cache.v_scale;
+        int pi = 0;     // pages issued
         bool ok = true;
         long long x = x0;
         int g = group_of(tile_start, a.n_groups, x);
@@ -257,116 +278,122 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
           for (int j = j0; j < j1 && ok; ++j) {
             if (j == nt - 1) continue;      // window tile: read directly by the dequant warps
-            const int s = kit & 1;
-            const uint32_t ph = ((kit >> 1) & 1) ^ 1;
-            int pg[2];
             const int npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
-            for (int q = 0; q < 2; ++q) {
-              int p = 0;
-              if (q < npg) {
-                p = a.page_table[(size_t)u.b * a.max_pages + 2 * j + q];
-                if (p < 0 || p >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); p = 0; }
-              }
-              pg[q] = p;
-            }
-            const uint32_t bytes = (uint32_t)npg * (C::PAGE_DATA + C::PAGE_SCALE);
-            // K part
-            if (!tc::mbar_wait(&sh.kempty_ring[s], ph, abort_p)) { fail(sh, a.err); ok = false; break; }
-            tc::mbar_arrive_expect_tx(&sh.kfull_ring[s], bytes);
-            uint8_t* dk = sK + s * C::PART;
             for (int q = 0; q < npg; ++q) {
-              tc::bulk_g2s(dk + q * C::PAGE_DATA, a.cache.k_data + pg[q] * pdb, C::PAGE_DATA, &sh.kfull_ring[s]);
-              tc::bulk_g2s(dk + 2 * C::PAGE_DATA + q * C::PAGE_SCALE, a.cache.k_scale + pg[q] * psb,
-                           C::PAGE_SCALE, &sh.kfull_ring[s]);
+              int p = a.page_table[(size_t)u.b * a.max_pages + 2 * j + q];
+              if (p < 0 || p >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); p = 0; }
+              const int slot = pi % nslot, use = pi / nslot;
+              if (!tc::mbar_wait(&emptyb[slot], (use & 1) ^ 1, abort_p)) { fail(sh, a.err); ok = false; break; }
+              tc::mbar_arrive_expect_tx(&fullb[slot], C::PSLOT);
+              uint8_t* dst = ring + slot * C::PSLOT;
+              tc::bulk_g2s(dst, gdata + (size_t)p * pdb, C::PAGE_DATA, &fullb[slot]);
+              tc::bulk_g2s(dst + C::PAGE_DATA, gscale + (size_t)p * psb, C::PAGE_SCALE, &fullb[slot]);
+              ++pi;
             }
-            ++kit;
-            // V part
-            if (!tc::mbar_wait(&sh.vempty_ring[s], ph, abort_p)) { fail(sh, a.err); ok = false; break; }
-            tc::mbar_arrive_expect_tx(&sh.vfull_ring[s], bytes);
-            uint8_t* dv = sV + s * C::PART;
-            for (int q = 0; q < npg; ++q) {
-              tc::bulk_g2s(dv + q * C::PAGE_DATA, a.cache.v_data + pg[q] * pdb, C::PAGE_DATA, &sh.vfull_ring[s]);
-              tc::bulk_g2s(dv + 2 * C::PAGE_DATA + q * C::PAGE_SCALE, a.cache.v_scale + pg[q] * psb,
-                           C::PAGE_SCALE, &sh.vfull_ring[s]);
-            }
-            ++vit;
           }
           x = tile_start[g] + j1;
           ++g;
         }
         // drain: every copy issued must have landed before this CTA may exit
         // (the last use of each slot; earlier uses were waited for by the consumers)
-        for (int k = (kit > 2 ? kit - 2 : 0); k < kit; ++k)
-          tc::mbar_wait(&sh.kfull_ring[k & 1], (k >> 1) & 1, abort_p, 1LL << 31);
-        for (int k = (vit > 2 ? vit - 2 : 0); k < vit; ++k)
-          tc::mbar_wait(&sh.vfull_ring[k & 1], (k >> 1) & 1, abort_p, 1LL << 31);
+        for (int k = (pi > nslot ? pi - nslot : 0); k < pi; ++k)
+          tc::mbar_wait(&fullb[k % nslot], (k / nslot) & 1, abort_p, 1LL << 31);
       }
     }
     // ======================================================== MMA issuer
-    else if (warp == 1) {
+    // Issues, whenever its inputs are ready, the next S^T = K Q^T chunk (64
+    // channels, 4 MMAs) or the next O^T += V^T P chunk (128 channels x 64
+    // tokens, 4 MMAs); QK runs ahead of PV by up to the two S slots.
+    else if (warp == 17) {
       if (lane == 0) {
         const uint32_t idK = tc::idesc_f16(128, NH, false, false);   // B = Q, K-major
         const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
         const uint32_t qaddr = tc::smem_u32(sQ), paddr = tc::smem_u32(sP);
-        int kc = 0, vc = 0, ntile = 0, nitem = 0, npv = 0;
+        // QK side
+        long long xq = x0;
+        int gq = group_of(tile_start, a.n_groups, xq);
+        int cq = 0, kc = 0, nq = 0, iq = 0;
+        bool qk_open = false, qk_first = true;
+        // PV side
+        long long xp = x0;
+        int gp = gq;
+        int cp = 0, vc = 0, np = 0, ip = 0;
+        bool pv_open = false, pv_first = true;
         bool ok = true;
-        long long x = x0;
-        int g = group_of(tile_start, a.n_groups, x);
-        while (x < x1 && ok) {
-          const int nt = tile_start[g + 1] - tile_start[g];
-          const int j0 = (int)(x - tile_start[g]);
-          const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
-          if (!tc::mbar_wait(&sh.q_full, nitem & 1, abort_p)) { fail(sh, a.err); ok = false; break; }
-          // software pipeline: QK(i), then PV(i-1)
-          for (int j = j0; j <= j1 && ok; ++j) {
-            if (j < j1) {
-              // ---- S^T = K Q^T
-              if (!tc::mbar_wait(&sh.s_empty, (ntile & 1) ^ 1, abort_p)) { fail(sh, a.err); ok = false; break; }
-              tc::tc_fence_after();
-              for (int c = 0; c < C::NKCH; ++c) {
-                const int slot = kc & 1;
-                if (!tc::mbar_wait(&sh.kfull[slot], (kc >> 1) & 1, abort_p)) { fail(sh, a.err); ok = false; break; }
-                tc::tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const uint64_t bd = tc::sdesc_sw128(qaddr + c * (NH * 128) + k * 32, 16, 1024);
-                  tc::mma_ts(tbase + COL_S, tbase + COL_K + 32 * slot + 8 * k, bd, idK, (c | k) != 0);
-                }
-                tc::mma_commit(&sh.kempty[slot]);
-                ++kc;
+        long long last = clock64();
+        while (ok && xp < x1) {
+          bool progressed = false;
+          if (xq < x1) {
+            if (!qk_open) {
+              const bool qg = !qk_first || tc::mbar_test(&sh.q_full, iq & 1);
+              if (qg && tc::mbar_test(&sh.s_empty[nq & 1], ((nq >> 1) & 1) ^ 1)) {
+                qk_open = true;
+                if (qk_first) ++iq;
               }
-              if (!ok) break;
-              tc::mma_commit(&sh.s_full);
-              ++ntile;
             }
-            if (j > j0) {
-              // ---- O^T += V^T P   for tile j-1
-              if (!tc::mbar_wait(&sh.p_full, npv & 1, abort_p)) { fail(sh, a.err); ok = false; break; }
-              if (j - 1 == j0) {
-                if (!tc::mbar_wait(&sh.o_empty, (nitem & 1) ^ 1, abort_p)) { fail(sh, a.err); ok = false; break; }
-              }
+            if (qk_open && tc::mbar_test(&sh.kfull[kc & 1], (kc >> 1) & 1)) {
               tc::tc_fence_after();
-              for (int c = 0; c < C::NVCH; ++c) {
-                const int slot = vc & 1;
-                if (!tc::mbar_wait(&sh.vfull[slot], (vc >> 1) & 1, abort_p)) { fail(sh, a.err); ok = false; break; }
-                tc::tc_fence_after();
+              const int slot = kc & 1;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                  const uint64_t bd = tc::sdesc_sw128(paddr + k * 2048, 8192, 1024);
-                  tc::mma_ts(tbase + COL_O + 64 * c, tbase + COL_V + 64 * slot + 8 * k, bd, idV,
-                             (j - 1 != j0) || (k != 0));
-                }
-                tc::mma_commit(&sh.vempty[slot]);
-                ++vc;
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t bd = tc::sdesc_sw128(qaddr + cq * (NH * 128) + k * 32, 16, 1024);
+                tc::mma_ts(tbase + COL_S + 64 * (nq & 1), tbase + COL_K + 32 * slot + 8 * k, bd, idK,
+                           (cq | k) != 0);
               }
-              if (!ok) break;
-              tc::mma_commit(&sh.p_empty);
-              ++npv;
+              tc::mma_commit(&sh.kempty[slot]);
+              ++kc;
+              progressed = true;
+              if (++cq == C::NKCH) {
+                tc::mma_commit(&sh.s_full[nq & 1]);
+                ++nq;
+                cq = 0;
+                qk_open = false;
+                ++xq;
+                while (gq + 1 <= a.n_groups - 1 && tile_start[gq + 1] <= xq) ++gq;
+                qk_first = (xq == tile_start[gq]);
+              }
             }
           }
-          ++nitem;
-          x = tile_start[g] + j1;
-          ++g;
+          if (xp < xq) {
+            if (!pv_open) {
+              const bool og = !pv_first || tc::mbar_test(&sh.o_empty, (ip & 1) ^ 1);
+              if (og && tc::mbar_test(&sh.p_full[np & 1], (np >> 1) & 1)) {
+                pv_open = true;
+                if (pv_first) ++ip;
+              }
+            }
+            if (pv_open && tc::mbar_test(&sh.vfull[vc & 1], (vc >> 1) & 1)) {
+              tc::tc_fence_after();
+              const int slot = vc & 1, c = cp >> 1, half = cp & 1;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t bd =
+                    tc::sdesc_sw128(paddr + (np & 1) * C::P_BYTES + half * 8192 + k * 2048, 8192, 1024);
+                tc::mma_ts(tbase + COL_O + 64 * c, tbase + COL_V + 32 * slot + 8 * k, bd, idV,
+                           !(pv_first && half == 0 && k == 0));
+              }
+              tc::mma_commit(&sh.vempty[slot]);
+              ++vc;
+              progressed = true;
+              if (++cp == 2 * C::NVCH) {
+                tc::mma_commit(&sh.p_empty[np & 1]);
+                ++np;
+                cp = 0;
+                pv_open = false;
+                ++xp;
+                while (gp + 1 <= a.n_groups - 1 && tile_start[gp + 1] <= xp) ++gp;
+                pv_first = (xp == tile_start[gp]);
+              }
+            }
+          }
+          if (progressed) {
+            last = clock64();
+          } else if (*abort_p || clock64() - last > (1LL << 31)) {
+            fail(sh, a.err);
+            ok = false;
+          } else {
+            __nanosleep(64);     // idle: leave issue slots to the warps doing the work
+          }
         }
         // drain outstanding MMAs before TMEM is freed
         tc::mma_commit(&sh.drain);
@@ -374,10 +401,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       }
     }
     // ======================================================== K dequantizer (thread = token)
-    else if (warp >= 4 && warp < 8) {
-      const int t = tid - 128;                       // token lane 0..127
+    else if (warp < 4) {
+      const int t = tid;                             // token lane 0..127
       const uint32_t lb = lane_base(warp);
-      int it = 0, kc = 0;
+      int kp = 0, kc = 0;       // pages consumed, K chunks produced
       bool ok = true;
       long long x = x0;
       int g = group_of(tile_start, a.n_groups, x);
@@ -388,19 +415,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         for (int j = j0; j < j1 && ok; ++j) {
           const bool win = (j == nt - 1);
-          int s = 0;
+          int npg = 0;
           bool valid;
           const uint8_t *row = nullptr, *srow = nullptr;
           int slot = 0;
           if (!win) {
-            s = it & 1;
-            const bool w_ok = tc::mbar_wait(&sh.kfull_ring[s], (it >> 1) & 1, abort_p);
+            npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
+            bool w_ok = true;
+            for (int q = 0; q < npg; ++q)
+              w_ok = w_ok && tc::mbar_wait(&sh.kr_full[(kp + q) % NKR], ((kp + q) / NKR) & 1, abort_p);
             if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
             valid = (TILE * j + t) < u.n_glob;
-            const int q = t >> 6;
+            const uint8_t* page = sK + ((kp + (t >> 6)) % NKR) * C::PSLOT;
             slot = t & 63;
-            row = sK + s * C::PART + q * C::PAGE_DATA + slot * (D / 2);
-            srow = sK + s * C::PART + 2 * C::PAGE_DATA + q * C::PAGE_SCALE + slot * 8;
+            row = page + slot * (D / 2);
+            srow = page + C::PAGE_DATA + slot * 8;
           } else {
             valid = t < u.n_win;
             row = u.wk + (size_t)t * D;
@@ -452,8 +481,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           if (!ok) break;
           if (!win) {
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.kempty_ring[s]);
-            ++it;
+            if (lane == 0)
+              for (int q = 0; q < npg; ++q) tc::mbar_arrive(&sh.kr_empty[(kp + q) % NKR]);
+            kp += npg;
           }
         }
         x = tile_start[g] + j1;
@@ -461,10 +491,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       }
     }
     // ======================================================== V dequantizer (thread = channel)
-    else if (warp >= 8 && warp < 12) {
-      const int dl = tid - 256;                      // channel lane 0..127 within a chunk
+    else if (warp < 8) {
+      const int dl = tid - 128;                      // channel lane 0..127 within a chunk
       const uint32_t lb = lane_base(warp);
-      int it = 0, vc = 0;
+      int vp = 0, vc = 0;       // pages consumed, V chunks produced
       bool ok = true;
       long long x = x0;
       int g = group_of(tile_start, a.n_groups, x);
@@ -475,27 +505,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         for (int j = j0; j < j1 && ok; ++j) {
           const bool win = (j == nt - 1);
-          int s = 0;
+          int npg = 0;
           int nvalid;
           if (!win) {
-            s = it & 1;
-            const bool w_ok = tc::mbar_wait(&sh.vfull_ring[s], (it >> 1) & 1, abort_p);
+            npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
+            bool w_ok = true;
+            for (int q = 0; q < npg; ++q)
+              w_ok = w_ok && tc::mbar_wait(&sh.vr_full[(vp + q) % NVR], ((vp + q) / NVR) & 1, abort_p);
             if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
             nvalid = min(TILE, u.n_glob - TILE * j);
           } else {
             nvalid = u.n_win;
           }
-          for (int c = 0; c < C::NVCH; ++c) {
-            const int vs = vc & 1;
-            const bool w_ok = tc::mbar_wait(&sh.vempty[vs], ((vc >> 1) & 1) ^ 1, abort_p);
-            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
+          for (int c = 0; c < C::NVCH && ok; ++c) {
             const int d = 128 * c + dl;
             for (int half = 0; half < 2; ++half) {       // tokens 64*half .. 64*half+63
+              const int vs = vc & 1;
+              const bool w_ok = tc::mbar_wait(&sh.vempty[vs], ((vc >> 1) & 1) ^ 1, abort_p);
+              if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
               uint32_t r[32];
-              if (!win) {
-                const uint8_t* base = sV + s * C::PART;
-                const uint32_t* wd = reinterpret_cast<const uint32_t*>(base + half * C::PAGE_DATA) + d;
-                const uint8_t* sc = base + 2 * C::PAGE_DATA + half * C::PAGE_SCALE + (d >> 4) * PKV_PAGE;
+              if (!win && half < npg) {
+                const uint8_t* base = sV + ((vp + half) % NVR) * C::PSLOT;
+                const uint32_t* wd = reinterpret_cast<const uint32_t*>(base) + d;
+                const uint8_t* sc = base + C::PAGE_DATA + (d >> 4) * PKV_PAGE;
 #pragma unroll
                 for (int o = 0; o < 8; ++o) {
                   const uint32_t w = wd[o * D];
@@ -507,14 +539,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                     r[4 * o + i] = deq_pair((w >> (8 * i)) & 0xFFu, s2);
                   }
                 }
-              } else {
+              } else if (win) {
                 const uint8_t* col = u.wv + d;
-#pragma unroll 8
+#pragma unroll
                 for (int i = 0; i < 32; ++i) {
                   const int e = 64 * half + 2 * i;
                   const uint32_t b0 = __ldg(col + (size_t)e * D), b1 = __ldg(col + (size_t)(e + 1) * D);
                   r[i] = tc::e4m3x2_to_f16x2(b0 | (b1 << 8));
                 }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = 0u;      // second page absent: no valid token
               }
               // zero the tokens beyond the valid count (their K rows are zero too)
               const int t0 = 64 * half;
@@ -526,19 +561,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                   else if (tt + 1 >= nvalid) r[i] &= 0xFFFFu;
                 }
               }
-              tc::tmem_st32(tbase + lb + COL_V + 64 * vs + 32 * half, r);
+              tc::tmem_st32(tbase + lb + COL_V + 32 * vs, r);
+              tc::tc_wait_st();
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
+              ++vc;
             }
-            tc::tc_wait_st();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
-            ++vc;
           }
           if (!ok) break;
           if (!win) {
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.vempty_ring[s]);
-            ++it;
+            if (lane == 0)
+              for (int q = 0; q < npg; ++q) tc::mbar_arrive(&sh.vr_empty[(vp + q) % NVR]);
+            vp += npg;
           }
         }
         x = tile_start[g] + j1;
@@ -546,14 +582,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       }
     }
     // ======================================================== softmax + epilogue
-    else if (warp >= 12) {
-      const int st = tid - 384;                 // 0..255
-      const int hh = (warp - 12) >> 2;          // head half: heads 32*hh .. 32*hh+31
+    else if (warp < 16) {
+      const int st = tid - 256;                 // 0..255
+      const int hh = (warp - 8) >> 2;           // head half: heads 32*hh .. 32*hh+31
       const int q4 = warp & 3;                  // TMEM lane quarter
       const int t = 32 * q4 + lane;             // token lane (S) / channel lane (O)
       const uint32_t lb = lane_base(warp);
       const float ratio = a.tw_v / a.cache.ts_v;
-      int ntile = 0, npv = 0;
+      int ntile = 0;
       bool ok = true;
       long long x = x0;
       int g = group_of(tile_start, a.n_groups, x);
@@ -575,105 +611,127 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           const bool win = (j == nt - 1);
           const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
           const float zs = a.scale * (win ? a.tw_k : a.cache.ts_k) * LOG2E;
-          // ---- S tile
-          bool w_ok = tc::mbar_wait(&sh.s_full, ntile & 1, abort_p);
+          const float pr = win ? ratio : 1.f;
+          const bool valid = t < nvalid;
+          // ---- S tile ready?
+          const int sslot = ntile & 1;
+          bool w_ok = tc::mbar_wait(&sh.s_full[sslot], (ntile >> 1) & 1, abort_p);
           if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
           tc::tc_fence_after();
-          float z[32];
-          {
-            uint32_t r[32];
-            tc::tmem_ld32(tbase + lb + COL_S + 32 * hh, r);
-            tc::tc_wait_ld();
-            const bool valid = t < nvalid;
+          // P buffer ntile&1 is free once the P.V of tile ntile-2 is done
+          const int pb = ntile & 1;
+          w_ok = tc::mbar_wait(&sh.p_empty[pb], ((ntile >> 1) & 1) ^ 1, abort_p);
+          if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
+          uint8_t* prow = sP + pb * C::P_BYTES + (t >> 3) * 1024 + (t & 7) * 128;
+          // two passes of 16 heads (keeps 16 logits live instead of 32)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) z[i] = valid ? __uint_as_float(r[i]) * zs : -INFINITY;
-          }
-          tc::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sh.s_empty);
-          ++ntile;
-          // all S of this item consumed: Q of the next item may replace this one
-          if (j == j1 - 1 && xn < x1) {
-            load_q<D>(a, g + 1, sQ, st);
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.q_full);
-          }
-          bool need = false;
+          for (int hq = 0; hq < 2; ++hq) {
+            const int h0 = 32 * hh + 16 * hq;            // first head of this pass
+            float z[16];
+            {
+              uint32_t r[16];
+              tc::tmem_ld16(tbase + lb + COL_S + 64 * sslot + h0, r);
+              tc::tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) need |= z[i] > sh.m[32 * hh + i] + TAU;
-          const bool any = tc::named_bar_or(2, 256, need);
-          // P.V of the previous tile must be done before O is rescaled or P rewritten
-          if (j > j0) {
-            w_ok = tc::mbar_wait(&sh.p_empty, npv & 1, abort_p);
-            if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
-            ++npv;
-          }
-          if (any) {
-            // tile max per head: over the 32 tokens of the warp, then the 4 lane quarters
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              float v = z[i];
-#pragma unroll
-              for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-              if (lane == 0) sh.red[q4][32 * hh + i] = v;
+              for (int i = 0; i < 16; ++i) z[i] = valid ? __uint_as_float(r[i]) * zs : -INFINITY;
             }
-            tc::named_bar(1, 256);
-            if (q4 == 0) {
-              const int h = 32 * hh + lane;
-              const float tm = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
-              const float mo = sh.m[h];
-              const float mn = fmaxf(mo, tm);
-              sh.alpha[h] = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
-              sh.m[h] = mn;
-            }
-            tc::named_bar(1, 256);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) l[i] *= sh.alpha[32 * hh + i];
-            if (j > j0) {
-              // O^T columns of this head half, every channel chunk, times alpha
-              tc::tc_fence_after();
-              for (int c = 0; c < C::NVCH; ++c) {
-                uint32_t o[32];
-                tc::tmem_ld32(tbase + lb + COL_O + 64 * c + 32 * hh, o);
-                tc::tc_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  o[i] = __float_as_uint(__uint_as_float(o[i]) * sh.alpha[32 * hh + i]);
-                tc::tmem_st32(tbase + lb + COL_O + 64 * c + 32 * hh, o);
+            if (hq == 1) {
+              // S fully read by this thread: the next S^T may be computed
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sh.s_empty[sslot]);
+              // all S of this item consumed: Q of the next item may replace this one
+              if (j == j1 - 1 && xn < x1) {
+                load_q<D>(a, g + 1, sQ, st);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&sh.q_full);
               }
-              tc::tc_wait_st();
+            }
+            bool need = false;
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const float4 v = *reinterpret_cast<const float4*>(&sh.m[h0 + 4 * i4]);
+              need |= (z[4 * i4] > v.x + TAU) | (z[4 * i4 + 1] > v.y + TAU) | (z[4 * i4 + 2] > v.z + TAU) |
+                      (z[4 * i4 + 3] > v.w + TAU);
+            }
+            if (tc::named_bar_or(2, 256, need)) {
+              // tile max per head: over the 32 tokens of the warp, then the 4 lane quarters
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float v = z[i];
+#pragma unroll
+                for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                if (lane == 0) sh.red[q4][h0 + i] = v;
+              }
+              tc::named_bar(1, 256);
+              if (q4 == 0 && lane < 16) {
+                const int h = h0 + lane;
+                const float tm = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
+                const float mo = sh.m[h];
+                const float mn = fmaxf(mo, tm);
+                sh.alpha[h] = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
+                sh.m[h] = mn;
+              }
+              tc::named_bar(1, 256);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) l[16 * hq + i] *= sh.alpha[h0 + i];
+              if (j > j0) {
+                // every P.V into O so far (tile ntile-1 and earlier) must be complete
+                const int kp = ntile - 1;
+                const bool pv_ok = tc::mbar_wait(&sh.p_empty[kp & 1], (kp >> 1) & 1, abort_p);
+                if (tc::named_bar_or(3, 256, !pv_ok)) { fail(sh, a.err); ok = false; break; }
+                tc::tc_fence_after();
+                // O^T columns of these 16 heads, every channel chunk, times alpha
+#pragma unroll 1
+                for (int c = 0; c < C::NVCH; ++c) {
+                  uint32_t o[16];
+                  const uint32_t ta = tbase + lb + COL_O + 64 * c + h0;
+                  tc::tmem_ld16(ta, o);
+                  tc::tc_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    o[i] = __float_as_uint(__uint_as_float(o[i]) * sh.alpha[h0 + i]);
+                  tc::tmem_st16(ta, o);
+                }
+                tc::tc_wait_st();
+              }
+            }
+            // ---- P = exp2(z - m) (f16; l sums the rounded values): row t of P
+            // (MN-major, 128-byte swizzle), heads h0 .. h0+15 = two 16-byte chunks
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              uint32_t pk[4];
+              const float4 ma = *reinterpret_cast<const float4*>(&sh.m[h0 + 8 * k]);
+              const float4 mb = *reinterpret_cast<const float4*>(&sh.m[h0 + 8 * k + 4]);
+              const float mk[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+              for (int i2 = 0; i2 < 4; ++i2) {
+                const int i = 4 * k + i2;        // head pair index within the pass
+                const float m0 = mk[2 * i2], m1 = mk[2 * i2 + 1];
+                const float p0 = z[2 * i] == -INFINITY ? 0.f : exp2f(z[2 * i] - m0);
+                const float p1 = z[2 * i + 1] == -INFINITY ? 0.f : exp2f(z[2 * i + 1] - m1);
+                const uint32_t h2 = f32_to_f16x2(p0, p1);
+                const float q0 = f16_lo(h2), q1 = f16_hi(h2);
+                l[16 * hq + 2 * i] += q0;
+                l[16 * hq + 2 * i + 1] += q1;
+                pk[i2] = win ? f32_to_f16x2(q0 * pr, q1 * pr) : h2;
+              }
+              *reinterpret_cast<uint4*>(prow + 16 * (((h0 >> 3) + k) ^ (t & 7))) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
           }
-          // ---- P = exp2(z - m)  (f16; l sums the rounded values)
-          const float pr = win ? ratio : 1.f;
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float m0 = sh.m[32 * hh + 2 * i], m1 = sh.m[32 * hh + 2 * i + 1];
-            const float p0 = z[2 * i] == -INFINITY ? 0.f : exp2f(z[2 * i] - m0);
-            const float p1 = z[2 * i + 1] == -INFINITY ? 0.f : exp2f(z[2 * i + 1] - m1);
-            const uint32_t h2 = f32_to_f16x2(p0, p1);
-            const float q0 = f16_lo(h2), q1 = f16_hi(h2);
-            l[2 * i] += q0;
-            l[2 * i + 1] += q1;
-            pk[i] = win ? f32_to_f16x2(q0 * pr, q1 * pr) : h2;
-          }
-          // row t of P (MN-major, 128-byte swizzle): heads 32*hh .. +31 = 4 chunks of 16 B
-          uint8_t* prow = sP + (t >> 3) * 1024 + (t & 7) * 128;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4*>(prow + 16 * ((4 * hh + k) ^ (t & 7))) =
-                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          if (!ok) break;
           tc::fence_proxy_async_smem();
           tc::tc_fence_before();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sh.p_full);
+          if (lane == 0) tc::mbar_arrive(&sh.p_full[pb]);
+          ++ntile;
         }
         if (!ok) break;
         // ---- end of the item: wait for its last P.V, then write the partial
-        bool w_ok = tc::mbar_wait(&sh.p_empty, npv & 1, abort_p);
+        const int klast = ntile - 1;       // P.V of the item's last tile done -> O complete
+        bool w_ok = tc::mbar_wait(&sh.p_empty[klast & 1], (klast >> 1) & 1, abort_p);
         if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
-        ++npv;
         tc::tc_fence_after();
         // l over all 128 token lanes
 #pragma unroll
@@ -686,17 +744,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         tc::named_bar(1, 256);
         const size_t prow_i = (size_t)cta + (size_t)g;          // partial row of this segment
         float* po = part_o + prow_i * a.H * D;
+#pragma unroll 1
         for (int c = 0; c < C::NVCH; ++c) {
-          uint32_t o[32];
-          tc::tmem_ld32(tbase + lb + COL_O + 64 * c + 32 * hh, o);
-          tc::tc_wait_ld();
           const int d = 128 * c + t;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int h = 32 * hh + i;
-            if (h < a.H) {
-              const float lh = sh.red[0][h] + sh.red[1][h] + sh.red[2][h] + sh.red[3][h];
-              po[(size_t)h * D + d] = lh > 0.f ? __uint_as_float(o[i]) * (a.cache.ts_v / lh) : 0.f;
+          for (int hq = 0; hq < 2; ++hq) {
+            uint32_t o[16];
+            tc::tmem_ld16(tbase + lb + COL_O + 64 * c + 32 * hh + 16 * hq, o);
+            tc::tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int h = 32 * hh + 16 * hq + i;
+              if (h < a.H) {
+                const float lh = sh.red[0][h] + sh.red[1][h] + sh.red[2][h] + sh.red[3][h];
+                po[(size_t)h * D + d] = lh > 0.f ? __uint_as_float(o[i]) * (a.cache.ts_v / lh) : 0.f;
+              }
             }
           }
         }
@@ -715,7 +777,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc(tbase, 512);
+  if (warp == 17) tc::tmem_dealloc(tbase, 512);
 }
 
 // Merge the segment partials of each query row: rows cta+g for every CTA whose

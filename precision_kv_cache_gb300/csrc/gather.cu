@@ -1,0 +1,138 @@
+// Sparse decode support: gather the selected positions of each sequence into a
+// compact paged cache (same byte layouts), so the tensor-core attention kernel
+// can run over them as a dense segment.
+//
+// "Logits MQA creux" (vLLM blog, "Kernels"): decode attention reads only the
+// top-k positions the indexer selected.  Positions sel[b][0..k) are ascending
+// and -1 padded; compact sequence b holds them, in order, in pages
+// b*npb .. b*npb+npb-1 (npb = ceil(k/64)), and seq_len'[b] = number of valid
+// positions.
+#include "pkv_common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+// one block (256 threads) per compact page
+template <int D>
+__global__ void __launch_bounds__(256) gather_kernel(pkv_kv_cache src, const int32_t* __restrict__ page_table,
+                                                     int max_pages, const int32_t* __restrict__ sel, int k,
+                                                     int npb, pkv_kv_cache dst, int32_t* __restrict__ dst_len,
+                                                     int* err) {
+  constexpr int PD = PKV_PAGE * D / 2, PS = PKV_PAGE * D / 16;
+  constexpr int SW = (D / 32 < 8 ? D / 32 : 8) - 1;
+  __shared__ int spage[PKV_PAGE], sslot[PKV_PAGE];
+  const int b = blockIdx.x / npb, jp = blockIdx.x % npb;
+  const int tid = threadIdx.x;
+  if (tid < PKV_PAGE) {
+    const int i = jp * PKV_PAGE + tid;
+    int pg = -1, sl = 0;
+    if (i < k) {
+      const int t = sel[(size_t)b * k + i];
+      if (t >= 0) {
+        const int j = t >> 6;
+        if (j < max_pages) {
+          const int p = page_table[(size_t)b * max_pages + j];
+          if (p >= 0 && p < src.num_pages) { pg = p; sl = t & 63; }
+          else report(err, PKV_DEVERR_BAD_PAGE);
+        } else {
+          report(err, PKV_DEVERR_BAD_PAGE);
+        }
+      }
+    }
+    spage[tid] = pg;
+    sslot[tid] = sl;
+  }
+  // number of valid positions of sequence b (the list is ascending, -1 padded)
+  if (jp == 0 && tid == 32) {
+    int n = 0;
+    while (n < k && sel[(size_t)b * k + n] >= 0) ++n;
+    dst_len[b] = n;
+  }
+  __syncthreads();
+  const size_t op = (size_t)blockIdx.x;
+  // ---- K codes: 16-byte chunks, re-swizzled for the destination slot
+  constexpr int NCH = D / 32;                       // chunks per token row
+  for (int w = tid; w < PKV_PAGE * NCH; w += 256) {
+    const int s = w / NCH, c = w % NCH;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (spage[s] >= 0) {
+      const int ss = sslot[s];
+      v = *reinterpret_cast<const uint4*>(src.k_data + (size_t)spage[s] * PD + ss * (D / 2) + 16 * (c ^ (ss & SW)));
+    }
+    *reinterpret_cast<uint4*>(dst.k_data + op * PD + s * (D / 2) + 16 * (c ^ (s & SW))) = v;
+  }
+  // ---- K scales: 8-byte words ([d/128][64][8])
+  for (int w = tid; w < PKV_PAGE * (D / 128); w += 256) {
+    const int s = w % PKV_PAGE, gq = w / PKV_PAGE;
+    uint2 v = make_uint2(0u, 0u);
+    if (spage[s] >= 0)
+      v = *reinterpret_cast<const uint2*>(src.k_scale + (size_t)spage[s] * PS + ((size_t)gq * PKV_PAGE + sslot[s]) * 8);
+    *reinterpret_cast<uint2*>(dst.k_scale + op * PS + ((size_t)gq * PKV_PAGE + s) * 8) = v;
+  }
+  // ---- V codes: word (octet o, channel c) collects nibble s%8 of its 8 tokens
+  for (int w = tid; w < 8 * D; w += 256) {
+    const int o = w / D, c = w % D;
+    uint32_t word = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int s = 8 * o + i;
+      if (spage[s] >= 0) {
+        const int ss = sslot[s];
+        const uint32_t sw = reinterpret_cast<const uint32_t*>(src.v_data + (size_t)spage[s] * PD)[(ss >> 3) * D + c];
+        word |= ((sw >> (4 * (ss & 7))) & 0xFu) << (4 * i);
+      }
+    }
+    reinterpret_cast<uint32_t*>(dst.v_data + op * PD)[o * D + c] = word;
+  }
+  // ---- V scales: byte (block j, token s)
+  for (int w = tid; w < PKV_PAGE * (D / 16); w += 256) {
+    const int j = w / PKV_PAGE, s = w % PKV_PAGE;
+    uint8_t v = 0;
+    if (spage[s] >= 0) v = src.v_scale[(size_t)spage[s] * PS + j * PKV_PAGE + sslot[s]];
+    dst.v_scale[op * PS + j * PKV_PAGE + s] = v;
+  }
+}
+
+__global__ void identity_table_kernel(int32_t* pt, int B, int npb) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < B * npb) pt[i] = i;
+}
+
+}  // namespace pkv
+
+size_t pkv_gather_ws_bytes(int d, int B, int k) {
+  const size_t npb = (size_t)(k + PKV_PAGE - 1) / PKV_PAGE;
+  const size_t pages = (size_t)B * npb;
+  const size_t pool = pages * (2 * (size_t)PKV_PAGE * d / 2 + 2 * (size_t)PKV_PAGE * d / 16);
+  return pool + pages * 4 + (size_t)B * 4 + 4 * 256;
+}
+
+// Carves the compact cache, page table and lengths out of ws; returns them.
+cudaError_t pkv_launch_gather(int d, const pkv_kv_cache& src, const int32_t* page_table, int max_pages,
+                              const int32_t* sel, int B, int k, void* ws, pkv_kv_cache* dst, int32_t** dst_pt,
+                              int32_t** dst_len, int* npb_out, int* err, cudaStream_t st) {
+  const int npb = (k + PKV_PAGE - 1) / PKV_PAGE;
+  const size_t pages = (size_t)B * npb;
+  const size_t PD = (size_t)PKV_PAGE * d / 2, PS = (size_t)PKV_PAGE * d / 16;
+  uint8_t* p = (uint8_t*)ws;
+  auto take = [&](size_t n) { uint8_t* r = p; p += (n + 255) / 256 * 256; return r; };
+  dst->k_data = take(pages * PD);
+  dst->k_scale = take(pages * PS);
+  dst->v_data = take(pages * PD);
+  dst->v_scale = take(pages * PS);
+  dst->num_pages = (int)pages;
+  dst->ts_k = src.ts_k;
+  dst->ts_v = src.ts_v;
+  *dst_pt = (int32_t*)take(pages * 4);
+  *dst_len = (int32_t*)take((size_t)B * 4);
+  *npb_out = npb;
+  pkv::identity_table_kernel<<<(int)((pages + 255) / 256), 256, 0, st>>>(*dst_pt, B, npb);
+  const int grid = (int)pages;
+  switch (d) {
+    case 128: pkv::gather_kernel<128><<<grid, 256, 0, st>>>(src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err); break;
+    case 256: pkv::gather_kernel<256><<<grid, 256, 0, st>>>(src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err); break;
+    case 512: pkv::gather_kernel<512><<<grid, 256, 0, st>>>(src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}

@@ -59,7 +59,8 @@ extern "C" pkv_status pkv_decode_attn_noalloc(pkv_ctx* ctx, const void* q_bf16,
                                               float softmax_scale, float* out, float* out_lse,
                                               void* stream) {
   if (!ctx || B <= 0 || max_pages <= 0) return PKV_ERR_INVALID_ARG;
-  const size_t need = pkv_workspace_bytes(ctx, PKV_OP_DECODE, B, sel_idx ? k : max_pages * 64);
+  const size_t need = sel_idx ? pkv_workspace_bytes(ctx, PKV_OP_DECODE_SPARSE, B, k)
+                              : pkv_workspace_bytes(ctx, PKV_OP_DECODE, B, max_pages * 64);
   if (need == 0) return PKV_ERR_INVALID_ARG;
   if (need > (size_t)PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
   void* ws = nullptr;
