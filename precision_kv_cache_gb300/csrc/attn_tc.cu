@@ -391,8 +391,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           } else if (*abort_p || clock64() - last > (1LL << 31)) {
             fail(sh, a.err);
             ok = false;
-          } else {
-            __nanosleep(64);     // idle: leave issue slots to the warps doing the work
           }
         }
         // drain outstanding MMAs before TMEM is freed
@@ -405,6 +403,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const int t = tid;                             // token lane 0..127
       const uint32_t lb = lane_base(warp);
       int kp = 0, kc = 0;       // pages consumed, K chunks produced
+      int pend = -1;            // TMEM slot of the last stored chunk not yet signalled
       bool ok = true;
       long long x = x0;
       int g = group_of(tile_start, a.n_groups, x);
@@ -436,8 +435,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           }
           for (int c = 0; c < C::NKCH; ++c) {
             const int ks = kc & 1;
-            const bool w_ok = tc::mbar_wait(&sh.kempty[ks], ((kc >> 1) & 1) ^ 1, abort_p);
-            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
             uint32_t r[32];
             if (!valid) {
 #pragma unroll
@@ -471,14 +468,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 }
               }
             }
+            // the previous chunk's store had this chunk's conversion time to land: signal it now
+            if (pend >= 0) {
+              tc::tc_wait_st();
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sh.kfull[pend]);
+              pend = -1;
+            }
+            const bool w_ok = tc::mbar_wait(&sh.kempty[ks], ((kc >> 1) & 1) ^ 1, abort_p);
+            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
             tc::tmem_st32(tbase + lb + COL_K + 32 * ks, r);
-            tc::tc_wait_st();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.kfull[ks]);
+            pend = ks;
             ++kc;
           }
           if (!ok) break;
+          // last chunk of the tile: signal it now (its K/V tile ends here)
+          if (pend >= 0) {
+            tc::tc_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.kfull[pend]);
+            pend = -1;
+          }
           if (!win) {
             __syncwarp();
             if (lane == 0)
@@ -489,12 +501,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         x = tile_start[g] + j1;
         ++g;
       }
+      tc::tc_wait_st();
+      if (pend >= 0 && ok) {
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sh.kfull[pend]);
+      }
     }
     // ======================================================== V dequantizer (thread = channel)
     else if (warp < 8) {
       const int dl = tid - 128;                      // channel lane 0..127 within a chunk
       const uint32_t lb = lane_base(warp);
       int vp = 0, vc = 0;       // pages consumed, V chunks produced
+      int pend = -1;            // TMEM slot of the last stored chunk not yet signalled
       bool ok = true;
       long long x = x0;
       int g = group_of(tile_start, a.n_groups, x);
@@ -521,8 +540,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             const int d = 128 * c + dl;
             for (int half = 0; half < 2; ++half) {       // tokens 64*half .. 64*half+63
               const int vs = vc & 1;
-              const bool w_ok = tc::mbar_wait(&sh.vempty[vs], ((vc >> 1) & 1) ^ 1, abort_p);
-              if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
               uint32_t r[32];
               if (!win && half < npg) {
                 const uint8_t* base = sV + ((vp + half) % NVR) * C::PSLOT;
@@ -561,15 +578,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                   else if (tt + 1 >= nvalid) r[i] &= 0xFFFFu;
                 }
               }
+              if (pend >= 0) {
+                tc::tc_wait_st();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&sh.vfull[pend]);
+                pend = -1;
+              }
+              const bool w_ok = tc::mbar_wait(&sh.vempty[vs], ((vc >> 1) & 1) ^ 1, abort_p);
+              if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
               tc::tmem_st32(tbase + lb + COL_V + 32 * vs, r);
-              tc::tc_wait_st();
-              tc::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
+              pend = vs;
               ++vc;
             }
           }
           if (!ok) break;
+          // last chunk of the tile: signal it now (its K/V tile ends here)
+          if (pend >= 0) {
+            tc::tc_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.vfull[pend]);
+            pend = -1;
+          }
           if (!win) {
             __syncwarp();
             if (lane == 0)
@@ -579,6 +610,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         }
         x = tile_start[g] + j1;
         ++g;
+      }
+      tc::tc_wait_st();
+      if (pend >= 0 && ok) {
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sh.vfull[pend]);
       }
     }
     // ======================================================== softmax + epilogue
@@ -781,39 +818,62 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
 }
 
 // Merge the segment partials of each query row: rows cta+g for every CTA whose
-// (non-empty) tile range meets g's tiles.  One block per (g, h).
+// (non-empty) tile range meets g's tiles.  One block of D/4 threads per (g, h):
+// warp 0 computes the LSE weights once, every thread combines one float4.
 __global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups, int G, int H, int D,
                                 const float* __restrict__ part_o, const float* __restrict__ part_lse,
                                 float* __restrict__ out, float* __restrict__ out_lse) {
+  __shared__ float wts[1024];
+  __shared__ int nseg_s, cl_s;
+  __shared__ float lse_s;
   const int g = blockIdx.x / H, h = blockIdx.x % H;
   const long long T = tile_start[n_groups];
-  const long long first = tile_start[g], last = tile_start[g + 1] - 1;
-  const int c_lo = (int)(((first + 1) * G - 1) / T), c_hi = (int)(((last + 1) * G - 1) / T);
-  float m = -INFINITY;
-  for (int c = c_lo; c <= c_hi; ++c) {
-    if (cta_start(T, G, c) == cta_start(T, G, c + 1)) continue;
-    m = fmaxf(m, part_lse[((size_t)c + g) * H + h]);
-  }
-  float sum = 0.f;
-  if (m != -INFINITY)
-    for (int c = c_lo; c <= c_hi; ++c) {
-      if (cta_start(T, G, c) == cta_start(T, G, c + 1)) continue;
-      sum += exp2f((part_lse[((size_t)c + g) * H + h] - m) * LOG2E);
+  if (threadIdx.x < 32) {
+    const long long first = tile_start[g], last = tile_start[g + 1] - 1;
+    const int c_lo = (int)(((first + 1) * G - 1) / T), c_hi = (int)(((last + 1) * G - 1) / T);
+    const int n = min(c_hi - c_lo + 1, 1024);
+    float m = -INFINITY;
+    for (int i = threadIdx.x; i < n; i += 32) {
+      const int c = c_lo + i;
+      const bool live = cta_start(T, G, c) != cta_start(T, G, c + 1);
+      const float ls = live ? part_lse[((size_t)c + g) * H + h] : -INFINITY;
+      wts[i] = ls;
+      m = fmaxf(m, ls);
     }
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.f;
-    if (m != -INFINITY) {
-      for (int c = c_lo; c <= c_hi; ++c) {
-        if (cta_start(T, G, c) == cta_start(T, G, c + 1)) continue;
-        const size_t r = (size_t)c + g;
-        const float ls = part_lse[r * H + h];
-        if (ls != -INFINITY) acc += exp2f((ls - m) * LOG2E) * part_o[(r * H + h) * D + d];
-      }
-      acc /= sum;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+    for (int i = threadIdx.x; i < n; i += 32) {
+      const float w = (m == -INFINITY || wts[i] == -INFINITY) ? 0.f : exp2f((wts[i] - m) * LOG2E);
+      wts[i] = w;
+      sum += w;
     }
-    out[((size_t)g * H + h) * D + d] = acc;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    __syncwarp();
+    if (threadIdx.x == 0) {
+      nseg_s = n;
+      cl_s = c_lo;
+      lse_s = m == -INFINITY ? -INFINITY : m + logf(sum);
+    }
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    for (int i = threadIdx.x; i < n; i += 32) wts[i] *= inv;
   }
-  if (threadIdx.x == 0 && out_lse) out_lse[(size_t)g * H + h] = m != -INFINITY ? m + logf(sum) : -INFINITY;
+  __syncthreads();
+  const int n = nseg_s, c_lo = cl_s;
+  for (int d4 = threadIdx.x; d4 < D / 4; d4 += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < n; ++i) {
+      const float w = wts[i];
+      if (w == 0.f) continue;
+      const size_t r = (size_t)(c_lo + i) + g;
+      const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + (r * H + h) * D) + d4);
+      acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+    }
+    reinterpret_cast<float4*>(out + ((size_t)g * H + h) * D)[d4] = acc;
+  }
+  if (threadIdx.x == 0 && out_lse) out_lse[(size_t)g * H + h] = lse_s;
 }
 
 }  // namespace tcattn
@@ -881,8 +941,8 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   e = cudaGetLastError();
   if (e0 && e1) cudaEventRecord(e1, st);
   if (e != cudaSuccess) return e;
-  merge_tc_kernel<<<a.n_groups * a.H, 128, 0, st>>>(tile_start, a.n_groups, G, a.H, a.D, part_o, part_lse, out,
-                                                    out_lse);
+  merge_tc_kernel<<<a.n_groups * a.H, a.D / 4, 0, st>>>(tile_start, a.n_groups, G, a.H, a.D, part_o, part_lse,
+                                                        out, out_lse);
   *n_launches = 3;
   return cudaGetLastError();
 }

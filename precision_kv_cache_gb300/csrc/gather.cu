@@ -12,7 +12,7 @@
 
 namespace pkv {
 
-// one block (256 threads) per compact page
+// one block (256 threads) per (compact page, octet of 8 tokens)
 template <int D>
 __global__ void __launch_bounds__(256) gather_kernel(pkv_kv_cache src, const int32_t* __restrict__ page_table,
                                                      int max_pages, const int32_t* __restrict__ sel, int k,
@@ -20,11 +20,12 @@ __global__ void __launch_bounds__(256) gather_kernel(pkv_kv_cache src, const int
                                                      int* err) {
   constexpr int PD = PKV_PAGE * D / 2, PS = PKV_PAGE * D / 16;
   constexpr int SW = (D / 32 < 8 ? D / 32 : 8) - 1;
-  __shared__ int spage[PKV_PAGE], sslot[PKV_PAGE];
-  const int b = blockIdx.x / npb, jp = blockIdx.x % npb;
+  __shared__ int spage[8], sslot[8];
+  const int page = blockIdx.x >> 3, o = blockIdx.x & 7;
+  const int b = page / npb, jp = page % npb;
   const int tid = threadIdx.x;
-  if (tid < PKV_PAGE) {
-    const int i = jp * PKV_PAGE + tid;
+  if (tid < 8) {
+    const int i = jp * PKV_PAGE + 8 * o + tid;
     int pg = -1, sl = 0;
     if (i < k) {
       const int t = sel[(size_t)b * k + i];
@@ -43,52 +44,53 @@ __global__ void __launch_bounds__(256) gather_kernel(pkv_kv_cache src, const int
     sslot[tid] = sl;
   }
   // number of valid positions of sequence b (the list is ascending, -1 padded)
-  if (jp == 0 && tid == 32) {
-    int n = 0;
-    while (n < k && sel[(size_t)b * k + n] >= 0) ++n;
-    dst_len[b] = n;
+  if (jp == 0 && o == 0 && tid == 32) {
+    int lo = 0, hi = k;                       // first index holding -1
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sel[(size_t)b * k + mid] >= 0) lo = mid + 1; else hi = mid;
+    }
+    dst_len[b] = lo;
   }
   __syncthreads();
-  const size_t op = (size_t)blockIdx.x;
-  // ---- K codes: 16-byte chunks, re-swizzled for the destination slot
-  constexpr int NCH = D / 32;                       // chunks per token row
-  for (int w = tid; w < PKV_PAGE * NCH; w += 256) {
-    const int s = w / NCH, c = w % NCH;
+  const size_t op = (size_t)page;
+  // ---- K codes of the 8 tokens: 16-byte chunks, re-swizzled for the destination slot
+  constexpr int NCH = D / 32;
+  for (int w = tid; w < 8 * NCH; w += 256) {
+    const int i = w / NCH, c = w % NCH, s = 8 * o + i;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (spage[s] >= 0) {
-      const int ss = sslot[s];
-      v = *reinterpret_cast<const uint4*>(src.k_data + (size_t)spage[s] * PD + ss * (D / 2) + 16 * (c ^ (ss & SW)));
+    if (spage[i] >= 0) {
+      const int ss = sslot[i];
+      v = *reinterpret_cast<const uint4*>(src.k_data + (size_t)spage[i] * PD + ss * (D / 2) + 16 * (c ^ (ss & SW)));
     }
     *reinterpret_cast<uint4*>(dst.k_data + op * PD + s * (D / 2) + 16 * (c ^ (s & SW))) = v;
   }
   // ---- K scales: 8-byte words ([d/128][64][8])
-  for (int w = tid; w < PKV_PAGE * (D / 128); w += 256) {
-    const int s = w % PKV_PAGE, gq = w / PKV_PAGE;
+  for (int w = tid; w < 8 * (D / 128); w += 256) {
+    const int i = w % 8, gq = w / 8, s = 8 * o + i;
     uint2 v = make_uint2(0u, 0u);
-    if (spage[s] >= 0)
-      v = *reinterpret_cast<const uint2*>(src.k_scale + (size_t)spage[s] * PS + ((size_t)gq * PKV_PAGE + sslot[s]) * 8);
+    if (spage[i] >= 0)
+      v = *reinterpret_cast<const uint2*>(src.k_scale + (size_t)spage[i] * PS + ((size_t)gq * PKV_PAGE + sslot[i]) * 8);
     *reinterpret_cast<uint2*>(dst.k_scale + op * PS + ((size_t)gq * PKV_PAGE + s) * 8) = v;
   }
-  // ---- V codes: word (octet o, channel c) collects nibble s%8 of its 8 tokens
-  for (int w = tid; w < 8 * D; w += 256) {
-    const int o = w / D, c = w % D;
+  // ---- V codes: word (o, c) collects nibble i of its 8 tokens (coalesced over c)
+  for (int c = tid; c < D; c += 256) {
     uint32_t word = 0u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int s = 8 * o + i;
-      if (spage[s] >= 0) {
-        const int ss = sslot[s];
-        const uint32_t sw = reinterpret_cast<const uint32_t*>(src.v_data + (size_t)spage[s] * PD)[(ss >> 3) * D + c];
+      if (spage[i] >= 0) {
+        const int ss = sslot[i];
+        const uint32_t sw = __ldg(reinterpret_cast<const uint32_t*>(src.v_data + (size_t)spage[i] * PD) + (ss >> 3) * D + c);
         word |= ((sw >> (4 * (ss & 7))) & 0xFu) << (4 * i);
       }
     }
     reinterpret_cast<uint32_t*>(dst.v_data + op * PD)[o * D + c] = word;
   }
   // ---- V scales: byte (block j, token s)
-  for (int w = tid; w < PKV_PAGE * (D / 16); w += 256) {
-    const int j = w / PKV_PAGE, s = w % PKV_PAGE;
+  for (int w = tid; w < 8 * (D / 16); w += 256) {
+    const int j = w / 8, i = w % 8, s = 8 * o + i;
     uint8_t v = 0;
-    if (spage[s] >= 0) v = src.v_scale[(size_t)spage[s] * PS + j * PKV_PAGE + sslot[s]];
+    if (spage[i] >= 0) v = src.v_scale[(size_t)spage[i] * PS + j * PKV_PAGE + sslot[i]];
     dst.v_scale[op * PS + j * PKV_PAGE + s] = v;
   }
 }
@@ -127,7 +129,7 @@ cudaError_t pkv_launch_gather(int d, const pkv_kv_cache& src, const int32_t* pag
   *dst_len = (int32_t*)take((size_t)B * 4);
   *npb_out = npb;
   pkv::identity_table_kernel<<<(int)((pages + 255) / 256), 256, 0, st>>>(*dst_pt, B, npb);
-  const int grid = (int)pages;
+  const int grid = (int)pages * 8;
   switch (d) {
     case 128: pkv::gather_kernel<128><<<grid, 256, 0, st>>>(src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err); break;
     case 256: pkv::gather_kernel<256><<<grid, 256, 0, st>>>(src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err); break;
