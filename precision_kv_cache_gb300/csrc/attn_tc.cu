@@ -10,20 +10,23 @@
 // Output: a normalized partial (O, LSE) per (CTA, query row) segment, merged
 // by merge_tc_kernel ("flash-decoding": split along the sequence + LSE merge).
 //
-// Design (one persistent CTA per SM, 640 threads, warp-specialized):
+// Design (one persistent CTA per SM, 864 threads, warp-specialized):
 //   * work = 128-token tiles; each query row has ceil(L/128) NVFP4 tiles plus
 //     one window tile; the concatenated tile list is cut into one contiguous
 //     range per CTA (balanced to one tile).
-//   * warp 16 streams the raw pages of each tile (K and V: codes + scales) into
-//     two 2-slot shared-memory rings with 1-D bulk copies (TMA engine).
-//   * warps 0-3 (thread = token) dequantize K to f16 (exact: E2M1 x E4M3 has
-//     <= 6 significant bits) into TMEM, 64 channels at a time: the A operand of
+//   * warps 24 (K) and 26 (V) stream the raw pages of each tile (codes +
+//     scales) into two shared-memory page rings with 1-D bulk copies (TMA).
+//   * warps 0-7 (thread = token; two warps per TMEM lane quarter, each one
+//     half of the channels) dequantize K to f16 (exact: E2M1 x E4M3 has <= 6
+//     significant bits) into TMEM, 64 channels at a time: the A operand of
 //     S^T = K Q^T  (M = 128 tokens, N = 64 heads, K = d).
-//   * warps 4-7 (thread = channel) dequantize V^T to f16 into TMEM, 128
-//     channels x 128 tokens at a time: the A operand of O^T = V^T P
-//     (M = 128 channels, N = 64 heads, K = 128 tokens).
-//   * warp 17 issues the MMAs (Q and P are the shared-memory B operands).
-//   * warps 8-15 run the online softmax on S (FP32, exp2, lazy max update
+//   * warps 8-15 (thread = channel; two warps per lane quarter, each one half
+//     of the tokens) dequantize V^T to f16 into TMEM, 128 channels x 64
+//     tokens at a time: the A operand of O^T = V^T P (M = 128 channels,
+//     N = 64 heads, K = tokens).  Each warp converts the E4M3 block scales it
+//     needs once (one per lane) and shares them through shared memory.
+//   * warp 25 issues the MMAs (Q and P are the shared-memory B operands).
+//   * warps 16-23 run the online softmax on S (FP32, exp2, lazy max update
 //     with threshold 2^8), write P (f16, shared memory) and finally normalize
 //     O and write the partial result.
 // Every wait is bounded; on a timeout the CTA sets the error word, stops all
@@ -37,7 +40,15 @@ namespace tcattn {
 
 constexpr int TILE = 128;
 constexpr int NH = 64;                 // MMA N: query heads (zero-padded)
-constexpr int NTHREADS = 640;       // 20 warps (5 warpgroups)
+constexpr int NTHREADS = 864;       // 27 warps
+// warp roles
+constexpr int W_KDEQ = 0;              // 8 warps: K dequantizers
+constexpr int W_VDEQ = 8;              // 8 warps: V dequantizers
+constexpr int W_SMAX = 16;             // 8 warps: softmax + epilogue
+constexpr int W_KPROD = 24;            // K page producer
+constexpr int W_MMA = 25;              // MMA issuer, TMEM owner
+constexpr int W_VPROD = 26;            // V page producer
+constexpr uint32_t NDEQ = 8;           // arrivals per K (V) chunk: one per dequant warp
 constexpr float TAU = 8.f;             // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -77,6 +88,7 @@ struct Shared {
   alignas(16) float m[NH];     // running max per head (log2 units)
   float alpha[NH];             // rescale factor of the current tile
   float red[4][NH];            // cross-warp reductions
+  uint32_t vsc[8][32];         // per V warp: f16x2 block-scale pairs of its current sub-chunk
 };
 
 // ---------------------------------------------------------------- schedule
@@ -167,8 +179,24 @@ __device__ __forceinline__ uint32_t f32_to_f16x2(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ float f16_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
-__device__ __forceinline__ float f16_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+// Sum of v[i] over the 32 lanes of the warp, by reduce-scatter: lane l returns
+// the total of entry (l >> 1) & 15 (the two lanes of a pair hold the same sum).
+__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
+  float a[8], b[4], c[2];
+  const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4, u1 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    a[i] = (u4 ? v[i + 8] : v[i]) + __shfl_xor_sync(0xffffffffu, u4 ? v[i] : v[i + 8], 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    b[i] = (u3 ? a[i + 4] : a[i]) + __shfl_xor_sync(0xffffffffu, u3 ? a[i] : a[i + 4], 8);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    c[i] = (u2 ? b[i + 2] : b[i]) + __shfl_xor_sync(0xffffffffu, u2 ? b[i] : b[i + 2], 4);
+  const float d = (u1 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, u1 ? c[0] : c[1], 2);
+  return d + __shfl_xor_sync(0xffffffffu, d, 1);
+}
 
 // Q of query row g -> shared memory: f16 (from bf16; exact for |q| in [2^-14, 65504]),
 // K-major with the 128-byte swizzle, heads >= H zero.  Called by the 256 softmax threads.
@@ -211,16 +239,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   if (tid == 0) {
     for (int i = 0; i < NKR; ++i) {
       tc::mbar_init(&sh.kr_full[i], 1);
-      tc::mbar_init(&sh.kr_empty[i], 4);
+      tc::mbar_init(&sh.kr_empty[i], NDEQ);
     }
     for (int i = 0; i < NVR; ++i) {
       tc::mbar_init(&sh.vr_full[i], 1);
-      tc::mbar_init(&sh.vr_empty[i], 4);
+      tc::mbar_init(&sh.vr_empty[i], NDEQ);
     }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sh.kfull[i], 4);
+      tc::mbar_init(&sh.kfull[i], NDEQ);
       tc::mbar_init(&sh.kempty[i], 1);
-      tc::mbar_init(&sh.vfull[i], 4);
+      tc::mbar_init(&sh.vfull[i], NDEQ);
       tc::mbar_init(&sh.vempty[i], 1);
     }
     tc::mbar_init(&sh.s_full[0], 1);
@@ -237,7 +265,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     sh.abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 17) {
+  if (warp == W_MMA) {
     tc::tmem_alloc(&sh.tmem_base, 512);
     tc::tmem_relinquish();
   }
@@ -256,11 +284,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
 
   if (x0 < x1) {
     // ======================================================== producers
-    // warp 16 streams K pages (codes + scales) into the K ring, warp 18 V pages
+    // one warp streams K pages (codes + scales) into the K ring, another V pages
     // into the V ring, one page per slot, with 1-D bulk copies.
-    if (warp == 16 || warp == 18) {
+    if (warp == W_KPROD || warp == W_VPROD) {
       if (lane == 0) {
-        const bool isK = (warp == 16);
+        const bool isK = (warp == W_KPROD);
         const int nslot = isK ? NKR : NVR;
         uint64_t* fullb = isK ? sh.kr_full : sh.vr_full;
         uint64_t* emptyb = isK ? sh.kr_empty : sh.vr_empty;
@@ -303,104 +331,112 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     // ======================================================== MMA issuer
     // Issues, whenever its inputs are ready, the next S^T = K Q^T chunk (64
     // channels, 4 MMAs) or the next O^T += V^T P chunk (128 channels x 64
-    // tokens, 4 MMAs); QK runs ahead of PV by up to the two S slots.
-    else if (warp == 17) {
-      if (lane == 0) {
-        const uint32_t idK = tc::idesc_f16(128, NH, false, false);   // B = Q, K-major
-        const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
-        const uint32_t qaddr = tc::smem_u32(sQ), paddr = tc::smem_u32(sP);
-        // QK side
-        long long xq = x0;
-        int gq = group_of(tile_start, a.n_groups, xq);
-        int cq = 0, kc = 0, nq = 0, iq = 0;
-        bool qk_open = false, qk_first = true;
-        // PV side
-        long long xp = x0;
-        int gp = gq;
-        int cp = 0, vc = 0, np = 0, ip = 0;
-        bool pv_open = false, pv_first = true;
-        bool ok = true;
-        long long last = clock64();
-        while (ok && xp < x1) {
-          bool progressed = false;
-          if (xq < x1) {
-            if (!qk_open) {
-              const bool qg = !qk_first || tc::mbar_test(&sh.q_full, iq & 1);
-              if (qg && tc::mbar_test(&sh.s_empty[nq & 1], ((nq >> 1) & 1) ^ 1)) {
-                qk_open = true;
-                if (qk_first) ++iq;
-              }
+    // tokens, 4 MMAs); QK runs ahead of PV by up to the two S slots.  The whole
+    // warp runs the (uniform) schedule and one elected lane issues: this keeps
+    // the operands in uniform registers and issues far faster than a lone lane.
+    else if (warp == W_MMA) {
+      const uint32_t idK = tc::idesc_f16(128, NH, false, false);   // B = Q, K-major
+      const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
+      // descriptor bases; the start-address field (bits 0-13, address >> 4) is advanced by addition
+      const uint64_t dq0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
+      const uint64_t dp0 = tc::sdesc_sw128(tc::smem_u32(sP), 8192, 1024);
+      // QK side
+      long long xq = x0;
+      int gq = group_of(tile_start, a.n_groups, xq);
+      int cq = 0, kc = 0, nq = 0, iq = 0;
+      bool qk_open = false, qk_first = true;
+      // PV side
+      long long xp = x0;
+      int gp = gq;
+      int cp = 0, vc = 0, np = 0, ip = 0;
+      bool pv_open = false, pv_first = true;
+      bool ok = true;
+      long long last = clock64();
+      while (ok && xp < x1) {
+        bool progressed = false;
+        if (xq < x1) {
+          if (!qk_open) {
+            const bool qg = !qk_first || tc::mbar_test(&sh.q_full, iq & 1);
+            if (qg && tc::mbar_test(&sh.s_empty[nq & 1], ((nq >> 1) & 1) ^ 1)) {
+              qk_open = true;
+              if (qk_first) ++iq;
             }
-            if (qk_open && tc::mbar_test(&sh.kfull[kc & 1], (kc >> 1) & 1)) {
-              tc::tc_fence_after();
-              const int slot = kc & 1;
+          }
+          if (qk_open && tc::mbar_test(&sh.kfull[kc & 1], (kc >> 1) & 1)) {
+            tc::tc_fence_after();
+            const int slot = kc & 1;
+            const uint32_t dS = tbase + COL_S + 64 * (nq & 1), aK = tbase + COL_K + 32 * slot;
+            const uint64_t bq = dq0 + (uint64_t)(cq * (NH * 128 / 16));
+            if (tc::elect_one()) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t bd = tc::sdesc_sw128(qaddr + cq * (NH * 128) + k * 32, 16, 1024);
-                tc::mma_ts(tbase + COL_S + 64 * (nq & 1), tbase + COL_K + 32 * slot + 8 * k, bd, idK,
-                           (cq | k) != 0);
-              }
+              for (int k = 0; k < 4; ++k) tc::mma_ts(dS, aK + 8 * k, bq + 2 * k, idK, (cq | k) != 0);
               tc::mma_commit(&sh.kempty[slot]);
-              ++kc;
-              progressed = true;
-              if (++cq == C::NKCH) {
-                tc::mma_commit(&sh.s_full[nq & 1]);
-                ++nq;
-                cq = 0;
-                qk_open = false;
-                ++xq;
-                while (gq + 1 <= a.n_groups - 1 && tile_start[gq + 1] <= xq) ++gq;
-                qk_first = (xq == tile_start[gq]);
-              }
+              if (cq == C::NKCH - 1) tc::mma_commit(&sh.s_full[nq & 1]);
             }
-          }
-          if (xp < xq) {
-            if (!pv_open) {
-              const bool og = !pv_first || tc::mbar_test(&sh.o_empty, (ip & 1) ^ 1);
-              if (og && tc::mbar_test(&sh.p_full[np & 1], (np >> 1) & 1)) {
-                pv_open = true;
-                if (pv_first) ++ip;
-              }
+            __syncwarp();
+            ++kc;
+            progressed = true;
+            if (++cq == C::NKCH) {
+              ++nq;
+              cq = 0;
+              qk_open = false;
+              ++xq;
+              while (gq + 1 <= a.n_groups - 1 && tile_start[gq + 1] <= xq) ++gq;
+              qk_first = (xq == tile_start[gq]);
             }
-            if (pv_open && tc::mbar_test(&sh.vfull[vc & 1], (vc >> 1) & 1)) {
-              tc::tc_fence_after();
-              const int slot = vc & 1, c = cp >> 1, half = cp & 1;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t bd =
-                    tc::sdesc_sw128(paddr + (np & 1) * C::P_BYTES + half * 8192 + k * 2048, 8192, 1024);
-                tc::mma_ts(tbase + COL_O + 64 * c, tbase + COL_V + 32 * slot + 8 * k, bd, idV,
-                           !(pv_first && half == 0 && k == 0));
-              }
-              tc::mma_commit(&sh.vempty[slot]);
-              ++vc;
-              progressed = true;
-              if (++cp == 2 * C::NVCH) {
-                tc::mma_commit(&sh.p_empty[np & 1]);
-                ++np;
-                cp = 0;
-                pv_open = false;
-                ++xp;
-                while (gp + 1 <= a.n_groups - 1 && tile_start[gp + 1] <= xp) ++gp;
-                pv_first = (xp == tile_start[gp]);
-              }
-            }
-          }
-          if (progressed) {
-            last = clock64();
-          } else if (*abort_p || clock64() - last > (1LL << 31)) {
-            fail(sh, a.err);
-            ok = false;
           }
         }
-        // drain outstanding MMAs before TMEM is freed
-        tc::mma_commit(&sh.drain);
-        tc::mbar_wait(&sh.drain, 0, abort_p, 1LL << 31);
+        if (xp < xq) {
+          if (!pv_open) {
+            const bool og = !pv_first || tc::mbar_test(&sh.o_empty, (ip & 1) ^ 1);
+            if (og && tc::mbar_test(&sh.p_full[np & 1], (np >> 1) & 1)) {
+              pv_open = true;
+              if (pv_first) ++ip;
+            }
+          }
+          if (pv_open && tc::mbar_test(&sh.vfull[vc & 1], (vc >> 1) & 1)) {
+            tc::tc_fence_after();
+            const int slot = vc & 1, c = cp >> 1, half = cp & 1;
+            const uint32_t dO = tbase + COL_O + 64 * c, aV = tbase + COL_V + 32 * slot;
+            const uint64_t bp = dp0 + (uint64_t)(((np & 1) * C::P_BYTES + half * 8192) >> 4);
+            if (tc::elect_one()) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                tc::mma_ts(dO, aV + 8 * k, bp + (uint64_t)(k * (2048 >> 4)), idV, !(pv_first && half == 0 && k == 0));
+              tc::mma_commit(&sh.vempty[slot]);
+              if (cp == 2 * C::NVCH - 1) tc::mma_commit(&sh.p_empty[np & 1]);
+            }
+            __syncwarp();
+            ++vc;
+            progressed = true;
+            if (++cp == 2 * C::NVCH) {
+              ++np;
+              cp = 0;
+              pv_open = false;
+              ++xp;
+              while (gp + 1 <= a.n_groups - 1 && tile_start[gp + 1] <= xp) ++gp;
+              pv_first = (xp == tile_start[gp]);
+            }
+          }
+        }
+        if (progressed) {
+          last = clock64();
+        } else if (*abort_p || clock64() - last > (1LL << 31)) {
+          if (lane == 0) fail(sh, a.err);
+          ok = false;
+        }
       }
+      // drain outstanding MMAs before TMEM is freed
+      if (tc::elect_one()) tc::mma_commit(&sh.drain);
+      __syncwarp();
+      tc::mbar_wait(&sh.drain, 0, abort_p, 1LL << 31);
     }
     // ======================================================== K dequantizer (thread = token)
-    else if (warp < 4) {
-      const int t = tid;                             // token lane 0..127
+    // warp pair (w, w+4) shares a TMEM lane quarter; warp w/4 == kh takes
+    // channels 32*kh .. 32*kh+31 of every 64-channel chunk (16 TMEM columns).
+    else if (warp < W_VDEQ) {
+      const int t = 32 * (warp & 3) + lane;          // token lane 0..127
+      const int kh = (warp - W_KDEQ) >> 2;           // channel half of each chunk
       const uint32_t lb = lane_base(warp);
       int kp = 0, kc = 0;       // pages consumed, K chunks produced
       int pend = -1;            // TMEM slot of the last stored chunk not yet signalled
@@ -428,25 +464,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             const uint8_t* page = sK + ((kp + (t >> 6)) % NKR) * C::PSLOT;
             slot = t & 63;
             row = page + slot * (D / 2);
-            srow = page + C::PAGE_DATA + slot * 8;
+            srow = page + C::PAGE_DATA + slot * 8 + 2 * kh;
           } else {
             valid = t < u.n_win;
-            row = u.wk + (size_t)t * D;
+            row = u.wk + (size_t)t * D + 32 * kh;
           }
+#pragma unroll 1
           for (int c = 0; c < C::NKCH; ++c) {
             const int ks = kc & 1;
-            uint32_t r[32];
+            uint32_t r[16];
             if (!valid) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = 0u;
+              for (int i = 0; i < 16; ++i) r[i] = 0u;
             } else if (!win) {
               constexpr int SW = (D / 32 < 8 ? D / 32 : 8) - 1;
-              const uint4 lo = *reinterpret_cast<const uint4*>(row + 16 * ((2 * c) ^ (slot & SW)));
-              const uint4 hi = *reinterpret_cast<const uint4*>(row + 16 * ((2 * c + 1) ^ (slot & SW)));
-              const uint32_t sc = *reinterpret_cast<const uint32_t*>(srow + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
-              const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+              // 16 bytes = channels 64c + 32kh .. +31 (two scale blocks)
+              const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * ((2 * c + kh) ^ (slot & SW)));
+              const uint32_t sc = *reinterpret_cast<const uint16_t*>(srow + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int bk = 0; bk < 4; ++bk) {
+              for (int bk = 0; bk < 2; ++bk) {
                 const uint32_t sb = (sc >> (8 * bk)) & 0xFFu;
                 const uint32_t s2 = tc::e4m3x2_to_f16x2(sb | (sb << 8));
 #pragma unroll
@@ -458,13 +495,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             } else {
               const uint4* p4 = reinterpret_cast<const uint4*>(row + 64 * c);
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                const uint4 v = __ldg(p4 + q4);
+              for (int h4 = 0; h4 < 2; ++h4) {
+                const uint4 v = __ldg(p4 + h4);
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                  r[8 * q4 + 2 * i] = tc::e4m3x2_to_f16x2(w[i] & 0xFFFFu);
-                  r[8 * q4 + 2 * i + 1] = tc::e4m3x2_to_f16x2(w[i] >> 16);
+                  r[8 * h4 + 2 * i] = tc::e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+                  r[8 * h4 + 2 * i + 1] = tc::e4m3x2_to_f16x2(w[i] >> 16);
                 }
               }
             }
@@ -478,7 +515,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             }
             const bool w_ok = tc::mbar_wait(&sh.kempty[ks], ((kc >> 1) & 1) ^ 1, abort_p);
             if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-            tc::tmem_st32(tbase + lb + COL_K + 32 * ks, r);
+            tc::tmem_st16(tbase + lb + COL_K + 32 * ks + 16 * kh, r);
             pend = ks;
             ++kc;
           }
@@ -509,9 +546,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       }
     }
     // ======================================================== V dequantizer (thread = channel)
-    else if (warp < 8) {
-      const int dl = tid - 128;                      // channel lane 0..127 within a chunk
+    // warp pair (w, w+4) shares a TMEM lane quarter; warp (w-8)/4 == vh takes
+    // tokens 32*vh .. 32*vh+31 of every 64-token sub-chunk (16 TMEM columns).
+    else if (warp < W_SMAX) {
+      const int vw = warp - W_VDEQ;                  // 0..7
+      const int dl = 32 * (vw & 3) + lane;           // channel lane 0..127 within a chunk
+      const int vh = vw >> 2;                        // token half of each sub-chunk
       const uint32_t lb = lane_base(warp);
+      uint32_t* vsc = sh.vsc[vw];
       int vp = 0, vc = 0;       // pages consumed, V chunks produced
       int pend = -1;            // TMEM slot of the last stored chunk not yet signalled
       bool ok = true;
@@ -536,43 +578,51 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           } else {
             nvalid = u.n_win;
           }
-          for (int c = 0; c < C::NVCH && ok; ++c) {
+#pragma unroll 1
+          for (int c = 0; c < C::NVCH; ++c) {
             const int d = 128 * c + dl;
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {       // tokens 64*half .. 64*half+63
               const int vs = vc & 1;
-              uint32_t r[32];
+              uint32_t r[16];
               if (!win && half < npg) {
                 const uint8_t* base = sV + ((vp + half) % NVR) * C::PSLOT;
-                const uint32_t* wd = reinterpret_cast<const uint32_t*>(base) + d;
-                const uint8_t* sc = base + C::PAGE_DATA + (d >> 4) * PKV_PAGE;
+                // block scales of this warp's two channel blocks x 32 tokens: lane
+                // converts the token pair (lane & 15) of block (lane >> 4) once
+                const int blk = ((128 * c + 32 * (vw & 3)) >> 4) + (lane >> 4);
+                const uint32_t s16 =
+                    *reinterpret_cast<const uint16_t*>(base + C::PAGE_DATA + blk * PKV_PAGE + 32 * vh + 2 * (lane & 15));
+                const uint32_t s2 = tc::e4m3x2_to_f16x2(s16);
+                __syncwarp();                            // previous readers of vsc are done
+                vsc[lane] = s2;
+                __syncwarp();
+                const uint4* sp = reinterpret_cast<const uint4*>(vsc + 16 * (lane >> 4));
+                const uint32_t* wd = reinterpret_cast<const uint32_t*>(base) + 4 * vh * D + d;
 #pragma unroll
-                for (int o = 0; o < 8; ++o) {
+                for (int o = 0; o < 4; ++o) {              // octet 4*vh + o of the page
                   const uint32_t w = wd[o * D];
-                  const uint2 s8 = *reinterpret_cast<const uint2*>(sc + 8 * o);
+                  const uint4 s4 = sp[o];
+                  const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    const uint32_t sw = (i < 2 ? s8.x : s8.y) >> (16 * (i & 1));
-                    const uint32_t s2 = tc::e4m3x2_to_f16x2(sw & 0xFFFFu);
-                    r[4 * o + i] = deq_pair((w >> (8 * i)) & 0xFFu, s2);
-                  }
+                  for (int i = 0; i < 4; ++i) r[4 * o + i] = deq_pair((w >> (8 * i)) & 0xFFu, sv[i]);
                 }
               } else if (win) {
                 const uint8_t* col = u.wv + d;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const int e = 64 * half + 2 * i;
+                for (int i = 0; i < 16; ++i) {
+                  const int e = 64 * half + 32 * vh + 2 * i;
                   const uint32_t b0 = __ldg(col + (size_t)e * D), b1 = __ldg(col + (size_t)(e + 1) * D);
                   r[i] = tc::e4m3x2_to_f16x2(b0 | (b1 << 8));
                 }
               } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = 0u;      // second page absent: no valid token
+                for (int i = 0; i < 16; ++i) r[i] = 0u;      // second page absent: no valid token
               }
               // zero the tokens beyond the valid count (their K rows are zero too)
-              const int t0 = 64 * half;
-              if (t0 + 64 > nvalid) {
+              const int t0 = 64 * half + 32 * vh;
+              if (t0 + 32 > nvalid) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 16; ++i) {
                   const int tt = t0 + 2 * i;
                   if (tt >= nvalid) r[i] = 0u;
                   else if (tt + 1 >= nvalid) r[i] &= 0xFFFFu;
@@ -587,10 +637,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               }
               const bool w_ok = tc::mbar_wait(&sh.vempty[vs], ((vc >> 1) & 1) ^ 1, abort_p);
               if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-              tc::tmem_st32(tbase + lb + COL_V + 32 * vs, r);
+              tc::tmem_st16(tbase + lb + COL_V + 32 * vs + 16 * vh, r);
               pend = vs;
               ++vc;
             }
+            if (!ok) break;
           }
           if (!ok) break;
           // last chunk of the tile: signal it now (its K/V tile ends here)
@@ -619,9 +670,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       }
     }
     // ======================================================== softmax + epilogue
-    else if (warp < 16) {
-      const int st = tid - 256;                 // 0..255
-      const int hh = (warp - 8) >> 2;           // head half: heads 32*hh .. 32*hh+31
+    else if (warp < W_KPROD) {
+      const int st = tid - 32 * W_SMAX;         // 0..255
+      const int hh = (warp - W_SMAX) >> 2;      // head half: heads 32*hh .. 32*hh+31
       const int q4 = warp & 3;                  // TMEM lane quarter
       const int t = 32 * q4 + lane;             // token lane (S) / channel lane (O)
       const uint32_t lb = lane_base(warp);
@@ -641,9 +692,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const long long xn = tile_start[g] + j1;
         if (st < NH) sh.m[st] = -INFINITY;
         tc::named_bar(1, 256);
-        float l[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) l[i] = 0.f;
+        // l of head 32*hh + 16*hq + hs over this warp's 32 tokens (both lanes of a pair hold it)
+        const int hs = (lane >> 1) & 15;
+        float l[2] = {0.f, 0.f};
         for (int j = j0; j < j1; ++j) {
           const bool win = (j == nt - 1);
           const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
@@ -710,8 +761,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 sh.m[h] = mn;
               }
               tc::named_bar(1, 256);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) l[16 * hq + i] *= sh.alpha[h0 + i];
+              l[hq] *= sh.alpha[h0 + hs];
               if (j > j0) {
                 // every P.V into O so far (tile ntile-1 and earlier) must be complete
                 const int kp = ntile - 1;
@@ -733,8 +783,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 tc::tc_wait_st();
               }
             }
-            // ---- P = exp2(z - m) (f16; l sums the rounded values): row t of P
-            // (MN-major, 128-byte swizzle), heads h0 .. h0+15 = two 16-byte chunks
+            // ---- P = exp2(z - m) (f16): row t of P (MN-major, 128-byte swizzle),
+            // heads h0 .. h0+15 = two 16-byte chunks; l sums the FP32 values
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               uint32_t pk[4];
@@ -744,18 +794,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
 #pragma unroll
               for (int i2 = 0; i2 < 4; ++i2) {
                 const int i = 4 * k + i2;        // head pair index within the pass
-                const float m0 = mk[2 * i2], m1 = mk[2 * i2 + 1];
-                const float p0 = z[2 * i] == -INFINITY ? 0.f : exp2f(z[2 * i] - m0);
-                const float p1 = z[2 * i + 1] == -INFINITY ? 0.f : exp2f(z[2 * i + 1] - m1);
-                const uint32_t h2 = f32_to_f16x2(p0, p1);
-                const float q0 = f16_lo(h2), q1 = f16_hi(h2);
-                l[16 * hq + 2 * i] += q0;
-                l[16 * hq + 2 * i + 1] += q1;
-                pk[i2] = win ? f32_to_f16x2(q0 * pr, q1 * pr) : h2;
+                const float p0 = z[2 * i] == -INFINITY ? 0.f : exp2f(z[2 * i] - mk[2 * i2]);
+                const float p1 = z[2 * i + 1] == -INFINITY ? 0.f : exp2f(z[2 * i + 1] - mk[2 * i2 + 1]);
+                z[2 * i] = p0;
+                z[2 * i + 1] = p1;
+                pk[i2] = win ? f32_to_f16x2(p0 * pr, p1 * pr) : f32_to_f16x2(p0, p1);
               }
               *reinterpret_cast<uint4*>(prow + 16 * (((h0 >> 3) + k) ^ (t & 7))) =
                   make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
+            l[hq] += warp_sum16(z, lane);
           }
           if (!ok) break;
           tc::fence_proxy_async_smem();
@@ -770,13 +818,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         bool w_ok = tc::mbar_wait(&sh.p_empty[klast & 1], (klast >> 1) & 1, abort_p);
         if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
         tc::tc_fence_after();
-        // l over all 128 token lanes
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = l[i];
-#pragma unroll
-          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == 0) sh.red[q4][32 * hh + i] = v;
+        // l over all 128 token lanes: the four lane quarters are summed below
+        if ((lane & 1) == 0) {
+          sh.red[q4][32 * hh + hs] = l[0];
+          sh.red[q4][32 * hh + 16 + hs] = l[1];
         }
         tc::named_bar(1, 256);
         const size_t prow_i = (size_t)cta + (size_t)g;          // partial row of this segment
@@ -814,7 +859,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 17) tc::tmem_dealloc(tbase, 512);
+  if (warp == W_MMA) tc::tmem_dealloc(tbase, 512);
 }
 
 // Merge the segment partials of each query row: rows cta+g for every CTA whose
