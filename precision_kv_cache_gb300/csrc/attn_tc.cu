@@ -10,7 +10,7 @@
 // Output: a normalized partial (O, LSE) per (CTA, query row) segment, merged
 // by merge_tc_kernel ("flash-decoding": split along the sequence + LSE merge).
 //
-// Design (one persistent CTA per SM, 864 threads, warp-specialized):
+// Design (one persistent CTA per SM, 896 threads, warp-specialized):
 //   * work = 128-token tiles; each query row has ceil(L/128) NVFP4 tiles plus
 //     one window tile; the concatenated tile list is cut into one contiguous
 //     range per CTA (balanced to one tile).
@@ -25,7 +25,8 @@
 //     tokens at a time: the A operand of O^T = V^T P (M = 128 channels,
 //     N = 64 heads, K = tokens).  Each warp converts the E4M3 block scales it
 //     needs once (one per lane) and shares them through shared memory.
-//   * warp 25 issues the MMAs (Q and P are the shared-memory B operands).
+//   * warp 25 issues the QK MMAs, warp 27 the PV MMAs (Q and P are the
+//     shared-memory B operands).
 //   * warps 16-23 run the online softmax on S (FP32, exp2, lazy max update
 //     with threshold 2^8), write P (f16, shared memory) and finally normalize
 //     O and write the partial result.
@@ -40,14 +41,15 @@ namespace tcattn {
 
 constexpr int TILE = 128;
 constexpr int NH = 64;                 // MMA N: query heads (zero-padded)
-constexpr int NTHREADS = 864;       // 27 warps
+constexpr int NTHREADS = 896;       // 28 warps
 // warp roles
 constexpr int W_KDEQ = 0;              // 8 warps: K dequantizers
 constexpr int W_VDEQ = 8;              // 8 warps: V dequantizers
 constexpr int W_SMAX = 16;             // 8 warps: softmax + epilogue
 constexpr int W_KPROD = 24;            // K page producer
-constexpr int W_MMA = 25;              // MMA issuer, TMEM owner
+constexpr int W_MMA = 25;              // QK MMA issuer, TMEM owner
 constexpr int W_VPROD = 26;            // V page producer
+constexpr int W_MMA2 = 27;             // PV MMA issuer
 constexpr uint32_t NDEQ = 8;           // arrivals per K (V) chunk: one per dequant warp
 constexpr float TAU = 8.f;             // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
@@ -82,7 +84,7 @@ struct Cfg {
 struct Shared {
   uint64_t kr_full[NKR], kr_empty[NKR], vr_full[NVR], vr_empty[NVR];
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
-  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], q_full, o_empty, drain;
+  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], q_full, o_empty, drain, drain2;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float m[NH];     // running max per head (log2 units)
@@ -262,6 +264,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     tc::mbar_init(&sh.q_full, 8);
     tc::mbar_init(&sh.o_empty, 8);
     tc::mbar_init(&sh.drain, 1);
+    tc::mbar_init(&sh.drain2, 1);
     sh.abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -328,108 +331,97 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           tc::mbar_wait(&fullb[k % nslot], (k / nslot) & 1, abort_p, 1LL << 31);
       }
     }
-    // ======================================================== MMA issuer
-    // Issues, whenever its inputs are ready, the next S^T = K Q^T chunk (64
-    // channels, 4 MMAs) or the next O^T += V^T P chunk (128 channels x 64
-    // tokens, 4 MMAs); QK runs ahead of PV by up to the two S slots.  The whole
-    // warp runs the (uniform) schedule and one elected lane issues: this keeps
-    // the operands in uniform registers and issues far faster than a lone lane.
+    // ======================================================== MMA issuers
+    // One warp issues S^T = K Q^T (per 64-channel K chunk: 4 MMAs), another
+    // O^T += V^T P (per 128-channel x 64-token V chunk: 4 MMAs), each in the
+    // fixed order of its inputs with blocking waits.  The whole warp runs the
+    // schedule and one elected lane issues (operands stay warp-uniform).
     else if (warp == W_MMA) {
       const uint32_t idK = tc::idesc_f16(128, NH, false, false);   // B = Q, K-major
-      const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
-      // descriptor bases; the start-address field (bits 0-13, address >> 4) is advanced by addition
+      // descriptor base; the start-address field (bits 0-13, address >> 4) is advanced by addition
       const uint64_t dq0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
-      const uint64_t dp0 = tc::sdesc_sw128(tc::smem_u32(sP), 8192, 1024);
-      // QK side
-      long long xq = x0;
-      int gq = group_of(tile_start, a.n_groups, xq);
-      int cq = 0, kc = 0, nq = 0, iq = 0;
-      bool qk_open = false, qk_first = true;
-      // PV side
-      long long xp = x0;
-      int gp = gq;
-      int cp = 0, vc = 0, np = 0, ip = 0;
-      bool pv_open = false, pv_first = true;
+      int kc = 0, nq = 0, iq = 0;
       bool ok = true;
-      long long last = clock64();
-      while (ok && xp < x1) {
-        bool progressed = false;
-        if (xq < x1) {
-          if (!qk_open) {
-            const bool qg = !qk_first || tc::mbar_test(&sh.q_full, iq & 1);
-            if (qg && tc::mbar_test(&sh.s_empty[nq & 1], ((nq >> 1) & 1) ^ 1)) {
-              qk_open = true;
-              if (qk_first) ++iq;
-            }
-          }
-          if (qk_open && tc::mbar_test(&sh.kfull[kc & 1], (kc >> 1) & 1)) {
-            tc::tc_fence_after();
+      long long x = x0;
+      int g = group_of(tile_start, a.n_groups, x);
+      while (x < x1 && ok) {
+        const int j1 = (int)min((long long)(tile_start[g + 1] - tile_start[g]), x1 - tile_start[g]);
+        // Q of this item in shared memory
+        ok = tc::mbar_wait(&sh.q_full, iq & 1, abort_p);
+        ++iq;
+        for (int j = (int)(x - tile_start[g]); j < j1 && ok; ++j) {
+          // S slot free (its previous tile read by the softmax)
+          ok = tc::mbar_wait(&sh.s_empty[nq & 1], ((nq >> 1) & 1) ^ 1, abort_p);
+          const uint32_t dS = tbase + COL_S + 64 * (nq & 1);
+          for (int c = 0; c < C::NKCH && ok; ++c) {
             const int slot = kc & 1;
-            const uint32_t dS = tbase + COL_S + 64 * (nq & 1), aK = tbase + COL_K + 32 * slot;
-            const uint64_t bq = dq0 + (uint64_t)(cq * (NH * 128 / 16));
+            ok = tc::mbar_wait(&sh.kfull[slot], (kc >> 1) & 1, abort_p);
+            if (!ok) break;
+            tc::tc_fence_after();
+            const uint32_t aK = tbase + COL_K + 32 * slot;
+            const uint64_t bq = dq0 + (uint64_t)(c * (NH * 128 / 16));
             if (tc::elect_one()) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) tc::mma_ts(dS, aK + 8 * k, bq + 2 * k, idK, (cq | k) != 0);
+              for (int k = 0; k < 4; ++k) tc::mma_ts(dS, aK + 8 * k, bq + 2 * k, idK, (c | k) != 0);
               tc::mma_commit(&sh.kempty[slot]);
-              if (cq == C::NKCH - 1) tc::mma_commit(&sh.s_full[nq & 1]);
+              if (c == C::NKCH - 1) tc::mma_commit(&sh.s_full[nq & 1]);
             }
             __syncwarp();
             ++kc;
-            progressed = true;
-            if (++cq == C::NKCH) {
-              ++nq;
-              cq = 0;
-              qk_open = false;
-              ++xq;
-              while (gq + 1 <= a.n_groups - 1 && tile_start[gq + 1] <= xq) ++gq;
-              qk_first = (xq == tile_start[gq]);
-            }
           }
+          ++nq;
         }
-        if (xp < xq) {
-          if (!pv_open) {
-            const bool og = !pv_first || tc::mbar_test(&sh.o_empty, (ip & 1) ^ 1);
-            if (og && tc::mbar_test(&sh.p_full[np & 1], (np >> 1) & 1)) {
-              pv_open = true;
-              if (pv_first) ++ip;
-            }
-          }
-          if (pv_open && tc::mbar_test(&sh.vfull[vc & 1], (vc >> 1) & 1)) {
-            tc::tc_fence_after();
+        x = tile_start[g] + j1;
+        ++g;
+      }
+      if (!ok && lane == 0) fail(sh, a.err);
+      // drain outstanding MMAs before TMEM is freed
+      if (tc::elect_one()) tc::mma_commit(&sh.drain);
+      __syncwarp();
+      tc::mbar_wait(&sh.drain, 0, abort_p, 1LL << 31);
+    }
+    else if (warp == W_MMA2) {
+      const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
+      const uint64_t dp0 = tc::sdesc_sw128(tc::smem_u32(sP), 8192, 1024);
+      int vc = 0, np = 0, ip = 0;
+      bool ok = true;
+      long long x = x0;
+      int g = group_of(tile_start, a.n_groups, x);
+      while (x < x1 && ok) {
+        const int j0 = (int)(x - tile_start[g]);
+        const int j1 = (int)min((long long)(tile_start[g + 1] - tile_start[g]), x1 - tile_start[g]);
+        // O of the previous item read out by the epilogue
+        ok = tc::mbar_wait(&sh.o_empty, (ip & 1) ^ 1, abort_p);
+        ++ip;
+        for (int j = j0; j < j1 && ok; ++j) {
+          ok = tc::mbar_wait(&sh.p_full[np & 1], (np >> 1) & 1, abort_p);
+          const uint64_t bpn = dp0 + (uint64_t)(((np & 1) * C::P_BYTES) >> 4);
+          for (int cp = 0; cp < 2 * C::NVCH && ok; ++cp) {
             const int slot = vc & 1, c = cp >> 1, half = cp & 1;
+            ok = tc::mbar_wait(&sh.vfull[slot], (vc >> 1) & 1, abort_p);
+            if (!ok) break;
+            tc::tc_fence_after();
             const uint32_t dO = tbase + COL_O + 64 * c, aV = tbase + COL_V + 32 * slot;
-            const uint64_t bp = dp0 + (uint64_t)(((np & 1) * C::P_BYTES + half * 8192) >> 4);
+            const uint64_t bp = bpn + (uint64_t)((half * 8192) >> 4);
             if (tc::elect_one()) {
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                tc::mma_ts(dO, aV + 8 * k, bp + (uint64_t)(k * (2048 >> 4)), idV, !(pv_first && half == 0 && k == 0));
+                tc::mma_ts(dO, aV + 8 * k, bp + (uint64_t)(k * (2048 >> 4)), idV, !(j == j0 && half == 0 && k == 0));
               tc::mma_commit(&sh.vempty[slot]);
               if (cp == 2 * C::NVCH - 1) tc::mma_commit(&sh.p_empty[np & 1]);
             }
             __syncwarp();
             ++vc;
-            progressed = true;
-            if (++cp == 2 * C::NVCH) {
-              ++np;
-              cp = 0;
-              pv_open = false;
-              ++xp;
-              while (gp + 1 <= a.n_groups - 1 && tile_start[gp + 1] <= xp) ++gp;
-              pv_first = (xp == tile_start[gp]);
-            }
           }
+          ++np;
         }
-        if (progressed) {
-          last = clock64();
-        } else if (*abort_p || clock64() - last > (1LL << 31)) {
-          if (lane == 0) fail(sh, a.err);
-          ok = false;
-        }
+        x = tile_start[g] + j1;
+        ++g;
       }
-      // drain outstanding MMAs before TMEM is freed
-      if (tc::elect_one()) tc::mma_commit(&sh.drain);
+      if (!ok && lane == 0) fail(sh, a.err);
+      if (tc::elect_one()) tc::mma_commit(&sh.drain2);
       __syncwarp();
-      tc::mbar_wait(&sh.drain, 0, abort_p, 1LL << 31);
+      tc::mbar_wait(&sh.drain2, 0, abort_p, 1LL << 31);
     }
     // ======================================================== K dequantizer (thread = token)
     // warp pair (w, w+4) shares a TMEM lane quarter; warp w/4 == kh takes
