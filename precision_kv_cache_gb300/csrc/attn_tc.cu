@@ -182,6 +182,13 @@ __device__ __forceinline__ uint32_t f32_to_f16x2(float lo, float hi) {
 }
 
 
+// 2^x, one approximate-unit instruction (relative error ~2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Sum of v[i] over the 32 lanes of the warp, by reduce-scatter: lane l returns
 // the total of entry (l >> 1) & 15 (the two lanes of a pair hold the same sum).
 __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
@@ -444,7 +451,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           const bool win = (j == nt - 1);
           int npg = 0;
           bool valid;
-          const uint8_t *row = nullptr, *srow = nullptr;
+          const uint8_t* row = nullptr;
+          uint32_t srow_s = 0, ssc_s = 0;     // shared addresses: token row, its scale bytes
           int slot = 0;
           if (!win) {
             npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
@@ -453,10 +461,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               w_ok = w_ok && tc::mbar_wait(&sh.kr_full[(kp + q) % NKR], ((kp + q) / NKR) & 1, abort_p);
             if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
             valid = (TILE * j + t) < u.n_glob;
-            const uint8_t* page = sK + ((kp + (t >> 6)) % NKR) * C::PSLOT;
+            const uint32_t page = tc::smem_u32(sK) + ((kp + (t >> 6)) % NKR) * C::PSLOT;
             slot = t & 63;
-            row = page + slot * (D / 2);
-            srow = page + C::PAGE_DATA + slot * 8 + 2 * kh;
+            srow_s = page + slot * (D / 2);
+            ssc_s = page + C::PAGE_DATA + slot * 8 + 2 * kh;
           } else {
             valid = t < u.n_win;
             row = u.wk + (size_t)t * D + 32 * kh;
@@ -471,8 +479,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             } else if (!win) {
               constexpr int SW = (D / 32 < 8 ? D / 32 : 8) - 1;
               // 16 bytes = channels 64c + 32kh .. +31 (two scale blocks)
-              const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * ((2 * c + kh) ^ (slot & SW)));
-              const uint32_t sc = *reinterpret_cast<const uint16_t*>(srow + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
+              const uint4 v = tc::lds128(srow_s + 16 * ((2 * c + kh) ^ (slot & SW)));
+              const uint32_t sc = tc::lds16(ssc_s + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
               const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
               for (int bk = 0; bk < 2; ++bk) {
@@ -545,7 +553,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const int dl = 32 * (vw & 3) + lane;           // channel lane 0..127 within a chunk
       const int vh = vw >> 2;                        // token half of each sub-chunk
       const uint32_t lb = lane_base(warp);
-      uint32_t* vsc = sh.vsc[vw];
+      const uint32_t vsc_s = tc::smem_u32(sh.vsc[vw]);
       int vp = 0, vc = 0;       // pages consumed, V chunks produced
       int pend = -1;            // TMEM slot of the last stored chunk not yet signalled
       bool ok = true;
@@ -578,22 +586,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               const int vs = vc & 1;
               uint32_t r[16];
               if (!win && half < npg) {
-                const uint8_t* base = sV + ((vp + half) % NVR) * C::PSLOT;
+                const uint32_t base = tc::smem_u32(sV) + ((vp + half) % NVR) * C::PSLOT;
                 // block scales of this warp's two channel blocks x 32 tokens: lane
                 // converts the token pair (lane & 15) of block (lane >> 4) once
                 const int blk = ((128 * c + 32 * (vw & 3)) >> 4) + (lane >> 4);
-                const uint32_t s16 =
-                    *reinterpret_cast<const uint16_t*>(base + C::PAGE_DATA + blk * PKV_PAGE + 32 * vh + 2 * (lane & 15));
+                const uint32_t s16 = tc::lds16(base + C::PAGE_DATA + blk * PKV_PAGE + 32 * vh + 2 * (lane & 15));
                 const uint32_t s2 = tc::e4m3x2_to_f16x2(s16);
                 __syncwarp();                            // previous readers of vsc are done
-                vsc[lane] = s2;
+                tc::sts32(vsc_s + 4 * lane, s2);
                 __syncwarp();
-                const uint4* sp = reinterpret_cast<const uint4*>(vsc + 16 * (lane >> 4));
-                const uint32_t* wd = reinterpret_cast<const uint32_t*>(base) + 4 * vh * D + d;
+                const uint32_t sp = vsc_s + 64 * (lane >> 4);
+                const uint32_t wd = base + 4 * (4 * vh * D + d);
 #pragma unroll
                 for (int o = 0; o < 4; ++o) {              // octet 4*vh + o of the page
-                  const uint32_t w = wd[o * D];
-                  const uint4 s4 = sp[o];
+                  const uint32_t w = tc::lds32(wd + 4 * o * D);
+                  const uint4 s4 = tc::lds128(sp + 16 * o);
                   const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
                   for (int i = 0; i < 4; ++i) r[4 * o + i] = deq_pair((w >> (8 * i)) & 0xFFu, sv[i]);
@@ -669,6 +676,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const int t = 32 * q4 + lane;             // token lane (S) / channel lane (O)
       const uint32_t lb = lane_base(warp);
       const float ratio = a.tw_v / a.cache.ts_v;
+      const uint32_t m_s = tc::smem_u32(sh.m);
       int ntile = 0;
       bool ok = true;
       long long x = x0;
@@ -702,18 +710,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           const int pb = ntile & 1;
           w_ok = tc::mbar_wait(&sh.p_empty[pb], ((ntile >> 1) & 1) ^ 1, abort_p);
           if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
-          uint8_t* prow = sP + pb * C::P_BYTES + (t >> 3) * 1024 + (t & 7) * 128;
+          const uint32_t prow = tc::smem_u32(sP) + pb * C::P_BYTES + (t >> 3) * 1024 + (t & 7) * 128;
           // two passes of 16 heads (keeps 16 logits live instead of 32)
 #pragma unroll
           for (int hq = 0; hq < 2; ++hq) {
             const int h0 = 32 * hh + 16 * hq;            // first head of this pass
-            float z[16];
+            // raw S^T of this token for heads h0 .. h0+15 (scaled below: d = S * zs - m)
+            float sv[16];
             {
               uint32_t r[16];
               tc::tmem_ld16(tbase + lb + COL_S + 64 * sslot + h0, r);
               tc::tc_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) z[i] = valid ? __uint_as_float(r[i]) * zs : -INFINITY;
+              for (int i = 0; i < 16; ++i) sv[i] = __uint_as_float(r[i]);
             }
             if (hq == 1) {
               // S fully read by this thread: the next S^T may be computed
@@ -727,18 +736,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 if (lane == 0) tc::mbar_arrive(&sh.q_full);
               }
             }
+            // does any logit exceed its running max by more than TAU?
             bool need = false;
+            if (valid) {
 #pragma unroll
-            for (int i4 = 0; i4 < 4; ++i4) {
-              const float4 v = *reinterpret_cast<const float4*>(&sh.m[h0 + 4 * i4]);
-              need |= (z[4 * i4] > v.x + TAU) | (z[4 * i4 + 1] > v.y + TAU) | (z[4 * i4 + 2] > v.z + TAU) |
-                      (z[4 * i4 + 3] > v.w + TAU);
+              for (int i4 = 0; i4 < 4; ++i4) {
+                const uint4 mb = tc::lds128(m_s + 4 * (h0 + 4 * i4));
+                need |= (fmaf(sv[4 * i4], zs, -__uint_as_float(mb.x)) > TAU) |
+                        (fmaf(sv[4 * i4 + 1], zs, -__uint_as_float(mb.y)) > TAU) |
+                        (fmaf(sv[4 * i4 + 2], zs, -__uint_as_float(mb.z)) > TAU) |
+                        (fmaf(sv[4 * i4 + 3], zs, -__uint_as_float(mb.w)) > TAU);
+              }
             }
             if (tc::named_bar_or(2, 256, need)) {
               // tile max per head: over the 32 tokens of the warp, then the 4 lane quarters
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
-                float v = z[i];
+                float v = valid ? sv[i] * zs : -INFINITY;
 #pragma unroll
                 for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
                 if (lane == 0) sh.red[q4][h0 + i] = v;
@@ -775,27 +789,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 tc::tc_wait_st();
               }
             }
-            // ---- P = exp2(z - m) (f16): row t of P (MN-major, 128-byte swizzle),
-            // heads h0 .. h0+15 = two 16-byte chunks; l sums the FP32 values
+            // ---- P = exp2(S * zs - m) (f16): row t of P (MN-major, 128-byte swizzle),
+            // heads h0 .. h0+15 = two 16-byte chunks; l sums the FP32 values.  The
+            // arguments are <= TAU, so the approximate exp2 stays in range.
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               uint32_t pk[4];
-              const float4 ma = *reinterpret_cast<const float4*>(&sh.m[h0 + 8 * k]);
-              const float4 mb = *reinterpret_cast<const float4*>(&sh.m[h0 + 8 * k + 4]);
-              const float mk[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+              const uint4 ma = tc::lds128(m_s + 4 * (h0 + 8 * k));
+              const uint4 mb = tc::lds128(m_s + 4 * (h0 + 8 * k + 4));
+              const float mk[8] = {__uint_as_float(ma.x), __uint_as_float(ma.y), __uint_as_float(ma.z),
+                                   __uint_as_float(ma.w), __uint_as_float(mb.x), __uint_as_float(mb.y),
+                                   __uint_as_float(mb.z), __uint_as_float(mb.w)};
 #pragma unroll
               for (int i2 = 0; i2 < 4; ++i2) {
                 const int i = 4 * k + i2;        // head pair index within the pass
-                const float p0 = z[2 * i] == -INFINITY ? 0.f : exp2f(z[2 * i] - mk[2 * i2]);
-                const float p1 = z[2 * i + 1] == -INFINITY ? 0.f : exp2f(z[2 * i + 1] - mk[2 * i2 + 1]);
-                z[2 * i] = p0;
-                z[2 * i + 1] = p1;
-                pk[i2] = win ? f32_to_f16x2(p0 * pr, p1 * pr) : f32_to_f16x2(p0, p1);
+                const float p0 = ex2_approx(valid ? fmaf(sv[2 * i], zs, -mk[2 * i2]) : -INFINITY);
+                const float p1 = ex2_approx(valid ? fmaf(sv[2 * i + 1], zs, -mk[2 * i2 + 1]) : -INFINITY);
+                sv[2 * i] = p0;
+                sv[2 * i + 1] = p1;
+                pk[i2] = f32_to_f16x2(p0 * pr, p1 * pr);
               }
-              *reinterpret_cast<uint4*>(prow + 16 * (((h0 >> 3) + k) ^ (t & 7))) =
-                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              tc::sts128(prow + 16 * (((h0 >> 3) + k) ^ (t & 7)), make_uint4(pk[0], pk[1], pk[2], pk[3]));
             }
-            l[hq] += warp_sum16(z, lane);
+            l[hq] += warp_sum16(sv, lane);
           }
           if (!ok) break;
           tc::fence_proxy_async_smem();
