@@ -56,10 +56,13 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
 // TMEM columns (512 allocated)
-constexpr uint32_t COL_S = 0;          // S^T tiles: 2 slots x 64 columns (fp32)
-constexpr uint32_t COL_O = 128;        // O^T: 4 chunks x 64 columns
-constexpr uint32_t COL_K = 384;        // K tile slots: 2 x 32 columns (64 channels, f16 pairs)
-constexpr uint32_t COL_V = 448;        // V^T tile slots: 2 x 32 columns (64 tokens, f16 pairs)
+constexpr int NKS = 3;                 // K chunk slots
+constexpr int NVS = 3;                 // V chunk slots
+constexpr uint32_t COL_S = 0;          // S^T tile: 64 columns (fp32); the softmax copies it out at once
+constexpr uint32_t COL_K = 64;         // K chunk slots: NKS x 32 columns (64 channels, f16 pairs)
+constexpr uint32_t COL_V = 160;        // V^T chunk slots: NVS x 32 columns (64 tokens, f16 pairs)
+constexpr uint32_t COL_O = 256;        // O^T: 4 chunks x 64 columns
+static_assert(COL_K == COL_S + 64 && COL_V == COL_K + 32 * NKS && COL_O >= COL_V + 32 * NVS, "TMEM map");
 
 constexpr int NKR = 3;                 // K ring: page slots
 constexpr int NVR = 4;                 // V ring: page slots
@@ -83,8 +86,8 @@ struct Cfg {
 
 struct Shared {
   uint64_t kr_full[NKR], kr_empty[NKR], vr_full[NVR], vr_empty[NVR];
-  uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
-  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], q_full, o_empty, drain, drain2;
+  uint64_t kfull[NKS], kempty[NKS], vfull[NVS], vempty[NVS];
+  uint64_t s_full, s_empty, p_full[2], p_empty[2], q_full, o_empty, drain, drain2;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float m[NH];     // running max per head (log2 units)
@@ -170,10 +173,6 @@ __device__ __forceinline__ void fail(Shared& sh, int* err) {
   report(err, PKV_DEVERR_TIMEOUT);
 }
 
-// f16x2 of e2m1 byte b (two channels) times the f16x2 scale pair
-__device__ __forceinline__ uint32_t deq_pair(uint32_t byte, uint32_t s2) {
-  return tc::hmul2(tc::e2m1x2_to_f16x2(byte), s2);
-}
 
 __device__ __forceinline__ uint32_t f32_to_f16x2(float lo, float hi) {
   uint32_t r;
@@ -254,16 +253,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       tc::mbar_init(&sh.vr_full[i], 1);
       tc::mbar_init(&sh.vr_empty[i], NDEQ);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NKS; ++i) {
       tc::mbar_init(&sh.kfull[i], NDEQ);
       tc::mbar_init(&sh.kempty[i], 1);
+    }
+    for (int i = 0; i < NVS; ++i) {
       tc::mbar_init(&sh.vfull[i], NDEQ);
       tc::mbar_init(&sh.vempty[i], 1);
     }
-    tc::mbar_init(&sh.s_full[0], 1);
-    tc::mbar_init(&sh.s_full[1], 1);
-    tc::mbar_init(&sh.s_empty[0], 8);
-    tc::mbar_init(&sh.s_empty[1], 8);
+    tc::mbar_init(&sh.s_full, 1);
+    tc::mbar_init(&sh.s_empty, 8);
     tc::mbar_init(&sh.p_full[0], 8);
     tc::mbar_init(&sh.p_full[1], 8);
     tc::mbar_init(&sh.p_empty[0], 1);
@@ -347,7 +346,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const uint32_t idK = tc::idesc_f16(128, NH, false, false);   // B = Q, K-major
       // descriptor base; the start-address field (bits 0-13, address >> 4) is advanced by addition
       const uint64_t dq0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
-      int kc = 0, nq = 0, iq = 0;
+      int ks = 0, nq = 0, iq = 0;
+      uint32_t kph = 0;          // K slot ring: slot, phase
       bool ok = true;
       long long x = x0;
       int g = group_of(tile_start, a.n_groups, x);
@@ -357,12 +357,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         ok = tc::mbar_wait(&sh.q_full, iq & 1, abort_p);
         ++iq;
         for (int j = (int)(x - tile_start[g]); j < j1 && ok; ++j) {
-          // S slot free (its previous tile read by the softmax)
-          ok = tc::mbar_wait(&sh.s_empty[nq & 1], ((nq >> 1) & 1) ^ 1, abort_p);
-          const uint32_t dS = tbase + COL_S + 64 * (nq & 1);
+          // S free (the previous tile copied out by the softmax)
+          ok = tc::mbar_wait(&sh.s_empty, (nq & 1) ^ 1, abort_p);
+          const uint32_t dS = tbase + COL_S;
           for (int c = 0; c < C::NKCH && ok; ++c) {
-            const int slot = kc & 1;
-            ok = tc::mbar_wait(&sh.kfull[slot], (kc >> 1) & 1, abort_p);
+            const int slot = ks;
+            ok = tc::mbar_wait(&sh.kfull[slot], kph, abort_p);
             if (!ok) break;
             tc::tc_fence_after();
             const uint32_t aK = tbase + COL_K + 32 * slot;
@@ -371,10 +371,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
 #pragma unroll
               for (int k = 0; k < 4; ++k) tc::mma_ts(dS, aK + 8 * k, bq + 2 * k, idK, (c | k) != 0);
               tc::mma_commit(&sh.kempty[slot]);
-              if (c == C::NKCH - 1) tc::mma_commit(&sh.s_full[nq & 1]);
+              if (c == C::NKCH - 1) tc::mma_commit(&sh.s_full);
             }
             __syncwarp();
-            ++kc;
+            if (++ks == NKS) { ks = 0; kph ^= 1; }
           }
           ++nq;
         }
@@ -390,7 +390,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     else if (warp == W_MMA2) {
       const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
       const uint64_t dp0 = tc::sdesc_sw128(tc::smem_u32(sP), 8192, 1024);
-      int vc = 0, np = 0, ip = 0;
+      int vs = 0, np = 0, ip = 0;
+      uint32_t vph = 0;          // V slot ring: slot, phase
       bool ok = true;
       long long x = x0;
       int g = group_of(tile_start, a.n_groups, x);
@@ -403,9 +404,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         for (int j = j0; j < j1 && ok; ++j) {
           ok = tc::mbar_wait(&sh.p_full[np & 1], (np >> 1) & 1, abort_p);
           const uint64_t bpn = dp0 + (uint64_t)(((np & 1) * C::P_BYTES) >> 4);
+          // chunk order: page half 0 for every channel chunk, then page half 1
           for (int cp = 0; cp < 2 * C::NVCH && ok; ++cp) {
-            const int slot = vc & 1, c = cp >> 1, half = cp & 1;
-            ok = tc::mbar_wait(&sh.vfull[slot], (vc >> 1) & 1, abort_p);
+            const int slot = vs, half = cp / C::NVCH, c = cp % C::NVCH;
+            ok = tc::mbar_wait(&sh.vfull[slot], vph, abort_p);
             if (!ok) break;
             tc::tc_fence_after();
             const uint32_t dO = tbase + COL_O + 64 * c, aV = tbase + COL_V + 32 * slot;
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               if (cp == 2 * C::NVCH - 1) tc::mma_commit(&sh.p_empty[np & 1]);
             }
             __syncwarp();
-            ++vc;
+            if (++vs == NVS) { vs = 0; vph ^= 1; }
           }
           ++np;
         }
@@ -437,7 +439,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const int t = 32 * (warp & 3) + lane;          // token lane 0..127
       const int kh = (warp - W_KDEQ) >> 2;           // channel half of each chunk
       const uint32_t lb = lane_base(warp);
-      int kp = 0, kc = 0;       // pages consumed, K chunks produced
+      int kp = 0, ks = 0;       // pages consumed; K chunk slot ring: slot, phase
+      uint32_t kph = 0;
       int pend = -1;            // TMEM slot of the last stored chunk not yet signalled
       bool ok = true;
       long long x = x0;
@@ -471,7 +474,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           }
 #pragma unroll 1
           for (int c = 0; c < C::NKCH; ++c) {
-            const int ks = kc & 1;
             uint32_t r[16];
             if (!valid) {
 #pragma unroll
@@ -482,15 +484,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               const uint4 v = tc::lds128(srow_s + 16 * ((2 * c + kh) ^ (slot & SW)));
               const uint32_t sc = tc::lds16(ssc_s + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
               const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+              // scale pairs (s0, s0) and (s1, s1) of the two blocks
+              const uint32_t s2[2] = {tc::e4m3x2_to_f16x2((sc & 0xFFu) * 0x101u), tc::e4m3x2_to_f16x2((sc >> 8) * 0x101u)};
 #pragma unroll
-              for (int bk = 0; bk < 2; ++bk) {
-                const uint32_t sb = (sc >> (8 * bk)) & 0xFFu;
-                const uint32_t s2 = tc::e4m3x2_to_f16x2(sb | (sb << 8));
+              for (int q = 0; q < 4; ++q) {              // word q: channels 8q .. 8q+7 of this half-chunk
+                uint32_t e[4];
+                tc::e2m1x8_to_f16x2x4(w[q], e);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const uint32_t wd = w[2 * bk + (i >> 2)];
-                  r[8 * bk + i] = deq_pair((wd >> (8 * (i & 3))) & 0xFFu, s2);
-                }
+                for (int i = 0; i < 4; ++i) r[4 * q + i] = tc::hmul2(e[i], s2[q >> 1]);
               }
             } else {
               const uint4* p4 = reinterpret_cast<const uint4*>(row + 64 * c);
@@ -499,10 +500,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 const uint4 v = __ldg(p4 + h4);
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  r[8 * h4 + 2 * i] = tc::e4m3x2_to_f16x2(w[i] & 0xFFFFu);
-                  r[8 * h4 + 2 * i + 1] = tc::e4m3x2_to_f16x2(w[i] >> 16);
-                }
+                for (int i = 0; i < 4; ++i) tc::e4m3x4_to_f16x2x2(w[i], &r[8 * h4 + 2 * i]);
               }
             }
             // the previous chunk's store had this chunk's conversion time to land: signal it now
@@ -513,11 +511,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               if (lane == 0) tc::mbar_arrive(&sh.kfull[pend]);
               pend = -1;
             }
-            const bool w_ok = tc::mbar_wait(&sh.kempty[ks], ((kc >> 1) & 1) ^ 1, abort_p);
+            const bool w_ok = tc::mbar_wait(&sh.kempty[ks], kph ^ 1, abort_p);
             if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
             tc::tmem_st16(tbase + lb + COL_K + 32 * ks + 16 * kh, r);
             pend = ks;
-            ++kc;
+            if (++ks == NKS) { ks = 0; kph ^= 1; }
           }
           if (!ok) break;
           // last chunk of the tile: signal it now (its K/V tile ends here)
@@ -554,7 +552,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const int vh = vw >> 2;                        // token half of each sub-chunk
       const uint32_t lb = lane_base(warp);
       const uint32_t vsc_s = tc::smem_u32(sh.vsc[vw]);
-      int vp = 0, vc = 0;       // pages consumed, V chunks produced
+      int vp = 0, vs = 0;       // pages consumed; V chunk slot ring: slot, phase
+      uint32_t vph = 0;
       int pend = -1;            // TMEM slot of the last stored chunk not yet signalled
       bool ok = true;
       long long x = x0;
@@ -566,27 +565,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         for (int j = j0; j < j1 && ok; ++j) {
           const bool win = (j == nt - 1);
-          int npg = 0;
-          int nvalid;
-          if (!win) {
-            npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
-            bool w_ok = true;
-            for (int q = 0; q < npg; ++q)
-              w_ok = w_ok && tc::mbar_wait(&sh.vr_full[(vp + q) % NVR], ((vp + q) / NVR) & 1, abort_p);
-            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-            nvalid = min(TILE, u.n_glob - TILE * j);
-          } else {
-            nvalid = u.n_win;
-          }
+          const int npg = win ? 0 : ((TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1);
+          const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
+          // page-major: every channel chunk of page half 0, then of half 1, so that
+          // a page is released as soon as its codes are read
 #pragma unroll 1
-          for (int c = 0; c < C::NVCH; ++c) {
-            const int d = 128 * c + dl;
+          for (int half = 0; half < 2 && ok; ++half) {       // tokens 64*half .. 64*half+63
+            const bool paged = half < npg;
+            if (paged) {
+              const bool w_ok = tc::mbar_wait(&sh.vr_full[(vp + half) % NVR], ((vp + half) / NVR) & 1, abort_p);
+              if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
+            }
+            const uint32_t base = tc::smem_u32(sV) + ((vp + half) % NVR) * C::PSLOT;
 #pragma unroll 1
-            for (int half = 0; half < 2; ++half) {       // tokens 64*half .. 64*half+63
-              const int vs = vc & 1;
+            for (int c = 0; c < C::NVCH; ++c) {
+              const int d = 128 * c + dl;
               uint32_t r[16];
-              if (!win && half < npg) {
-                const uint32_t base = tc::smem_u32(sV) + ((vp + half) % NVR) * C::PSLOT;
+              if (paged) {
                 // block scales of this warp's two channel blocks x 32 tokens: lane
                 // converts the token pair (lane & 15) of block (lane >> 4) once
                 const int blk = ((128 * c + 32 * (vw & 3)) >> 4) + (lane >> 4);
@@ -602,8 +597,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                   const uint32_t w = tc::lds32(wd + 4 * o * D);
                   const uint4 s4 = tc::lds128(sp + 16 * o);
                   const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+                  uint32_t e[4];
+                  tc::e2m1x8_to_f16x2x4(w, e);
 #pragma unroll
-                  for (int i = 0; i < 4; ++i) r[4 * o + i] = deq_pair((w >> (8 * i)) & 0xFFu, sv[i]);
+                  for (int i = 0; i < 4; ++i) r[4 * o + i] = tc::hmul2(e[i], sv[i]);
                 }
               } else if (win) {
                 const uint8_t* col = u.wv + d;
@@ -634,13 +631,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 if (lane == 0) tc::mbar_arrive(&sh.vfull[pend]);
                 pend = -1;
               }
-              const bool w_ok = tc::mbar_wait(&sh.vempty[vs], ((vc >> 1) & 1) ^ 1, abort_p);
+              const bool w_ok = tc::mbar_wait(&sh.vempty[vs], vph ^ 1, abort_p);
               if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
               tc::tmem_st16(tbase + lb + COL_V + 32 * vs + 16 * vh, r);
               pend = vs;
-              ++vc;
+              if (++vs == NVS) { vs = 0; vph ^= 1; }
             }
             if (!ok) break;
+            if (paged) {
+              // every code of this page is in registers / TMEM now: release it
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sh.vr_empty[(vp + half) % NVR]);
+            }
           }
           if (!ok) break;
           // last chunk of the tile: signal it now (its K/V tile ends here)
@@ -651,12 +653,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             if (lane == 0) tc::mbar_arrive(&sh.vfull[pend]);
             pend = -1;
           }
-          if (!win) {
-            __syncwarp();
-            if (lane == 0)
-              for (int q = 0; q < npg; ++q) tc::mbar_arrive(&sh.vr_empty[(vp + q) % NVR]);
-            vp += npg;
-          }
+          vp += npg;
         }
         x = tile_start[g] + j1;
         ++g;
@@ -701,11 +698,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           const float zs = a.scale * (win ? a.tw_k : a.cache.ts_k) * LOG2E;
           const float pr = win ? ratio : 1.f;
           const bool valid = t < nvalid;
-          // ---- S tile ready?
-          const int sslot = ntile & 1;
-          bool w_ok = tc::mbar_wait(&sh.s_full[sslot], (ntile >> 1) & 1, abort_p);
+          // ---- S tile ready?  Copy this token's 32 logits out of TMEM at once and
+          // free S for the next tile's QK.
+          bool w_ok = tc::mbar_wait(&sh.s_full, ntile & 1, abort_p);
           if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
           tc::tc_fence_after();
+          float sa[32];
+          {
+            uint32_t r[32];
+            tc::tmem_ld32(tbase + lb + COL_S + 32 * hh, r);
+            tc::tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sa[i] = __uint_as_float(r[i]);
+          }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sh.s_empty);
+          // all S of this item consumed: Q of the next item may replace this one
+          if (j == j1 - 1 && xn < x1) {
+            load_q<D>(a, g + 1, sQ, st);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.q_full);
+          }
           // P buffer ntile&1 is free once the P.V of tile ntile-2 is done
           const int pb = ntile & 1;
           w_ok = tc::mbar_wait(&sh.p_empty[pb], ((ntile >> 1) & 1) ^ 1, abort_p);
@@ -717,25 +731,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             const int h0 = 32 * hh + 16 * hq;            // first head of this pass
             // raw S^T of this token for heads h0 .. h0+15 (scaled below: d = S * zs - m)
             float sv[16];
-            {
-              uint32_t r[16];
-              tc::tmem_ld16(tbase + lb + COL_S + 64 * sslot + h0, r);
-              tc::tc_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) sv[i] = __uint_as_float(r[i]);
-            }
-            if (hq == 1) {
-              // S fully read by this thread: the next S^T may be computed
-              tc::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) tc::mbar_arrive(&sh.s_empty[sslot]);
-              // all S of this item consumed: Q of the next item may replace this one
-              if (j == j1 - 1 && xn < x1) {
-                load_q<D>(a, g + 1, sQ, st);
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&sh.q_full);
-              }
-            }
+            for (int i = 0; i < 16; ++i) sv[i] = sa[16 * hq + i];
             // does any logit exceed its running max by more than TAU?
             bool need = false;
             if (valid) {
@@ -776,15 +773,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 tc::tc_fence_after();
                 // O^T columns of these 16 heads, every channel chunk, times alpha
 #pragma unroll 1
-                for (int c = 0; c < C::NVCH; ++c) {
-                  uint32_t o[16];
-                  const uint32_t ta = tbase + lb + COL_O + 64 * c + h0;
-                  tc::tmem_ld16(ta, o);
+                for (int c8 = 0; c8 < 2 * C::NVCH; ++c8) {
+                  uint32_t o[8];
+                  const int hb = h0 + 8 * (c8 & 1);
+                  const uint32_t ta = tbase + lb + COL_O + 64 * (c8 >> 1) + hb;
+                  tc::tmem_ld8(ta, o);
                   tc::tc_wait_ld();
 #pragma unroll
-                  for (int i = 0; i < 16; ++i)
-                    o[i] = __float_as_uint(__uint_as_float(o[i]) * sh.alpha[h0 + i]);
-                  tc::tmem_st16(ta, o);
+                  for (int i = 0; i < 8; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * sh.alpha[hb + i]);
+                  tc::tmem_st8(ta, o);
                 }
                 tc::tc_wait_st();
               }

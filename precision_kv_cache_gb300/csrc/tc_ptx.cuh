@@ -261,6 +261,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];" : PKV_R8(0) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), PKV_W8(0)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- conversions
 // two E2M1 codes (low nibble -> low half) -> f16x2
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
@@ -271,6 +279,27 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
       : "=r"(out)
       : "r"(byte));
   return out;
+}
+// the four bytes of w (eight E2M1 codes, low nibble first) -> four f16x2; the
+// word is split into byte registers once instead of shifting and masking per byte
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t* o) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+// the four bytes of w (E4M3 codes) -> two f16x2 (bytes 0,1 and bytes 2,3)
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t* o) {
+  asm("{\n\t.reg .b16 h0, h1;\n\t"
+      "mov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+      : "=r"(o[0]), "=r"(o[1])
+      : "r"(w));
 }
 // two E4M3 codes (low byte -> low half) -> f16x2
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
