@@ -50,7 +50,8 @@ constexpr int W_KPROD = 24;            // K page producer
 constexpr int W_MMA = 25;              // QK MMA issuer, TMEM owner
 constexpr int W_VPROD = 26;            // V page producer
 constexpr int W_MMA2 = 27;             // PV MMA issuer
-constexpr uint32_t NDEQ = 8;           // arrivals per K (V) chunk: one per dequant warp
+constexpr uint32_t NDEQ = 8;           // arrivals per K (V) page release: one per dequant warp
+constexpr uint32_t NGRP = 4;           // arrivals per K (V) chunk: one per warp of a group
 constexpr float TAU = 8.f;             // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -93,7 +94,7 @@ struct Shared {
   alignas(16) float m[NH];     // running max per head (log2 units)
   float alpha[NH];             // rescale factor of the current tile
   float red[4][NH];            // cross-warp reductions
-  uint32_t vsc[8][32];         // per V warp: f16x2 block-scale pairs of its current sub-chunk
+  uint32_t vsc[8][64];         // per V warp: f16x2 block-scale pairs of its current chunk (2 blocks x 32)
 };
 
 // ---------------------------------------------------------------- schedule
@@ -254,11 +255,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       tc::mbar_init(&sh.vr_empty[i], NDEQ);
     }
     for (int i = 0; i < NKS; ++i) {
-      tc::mbar_init(&sh.kfull[i], NDEQ);
+      tc::mbar_init(&sh.kfull[i], NGRP);
       tc::mbar_init(&sh.kempty[i], 1);
     }
     for (int i = 0; i < NVS; ++i) {
-      tc::mbar_init(&sh.vfull[i], NDEQ);
+      tc::mbar_init(&sh.vfull[i], NGRP);
       tc::mbar_init(&sh.vempty[i], 1);
     }
     tc::mbar_init(&sh.s_full, 1);
@@ -363,6 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           for (int c = 0; c < C::NKCH && ok; ++c) {
             const int slot = ks;
             ok = tc::mbar_wait(&sh.kfull[slot], kph, abort_p);
+            tc::compiler_fence();          // issue strictly after the wait (measured: large effect)
             if (!ok) break;
             tc::tc_fence_after();
             const uint32_t aK = tbase + COL_K + 32 * slot;
@@ -408,6 +410,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           for (int cp = 0; cp < 2 * C::NVCH && ok; ++cp) {
             const int slot = vs, half = cp / C::NVCH, c = cp % C::NVCH;
             ok = tc::mbar_wait(&sh.vfull[slot], vph, abort_p);
+            tc::compiler_fence();
             if (!ok) break;
             tc::tc_fence_after();
             const uint32_t dO = tbase + COL_O + 64 * c, aV = tbase + COL_V + 32 * slot;
@@ -433,15 +436,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       tc::mbar_wait(&sh.drain2, 0, abort_p, 1LL << 31);
     }
     // ======================================================== K dequantizer (thread = token)
-    // warp pair (w, w+4) shares a TMEM lane quarter; warp w/4 == kh takes
-    // channels 32*kh .. 32*kh+31 of every 64-channel chunk (16 TMEM columns).
+    // Two groups of four warps (one warp per TMEM lane quarter); group kg
+    // converts the 64-channel chunks c = kg, kg+2, ... of every tile, a full
+    // 32-column slot per chunk.  Chunks are numbered across tiles and use the
+    // slot ring in order; a group advances two chunks at a time.
     else if (warp < W_VDEQ) {
       const int t = 32 * (warp & 3) + lane;          // token lane 0..127
-      const int kh = (warp - W_KDEQ) >> 2;           // channel half of each chunk
+      const int kg = (warp - W_KDEQ) >> 2;           // chunk parity of this group
       const uint32_t lb = lane_base(warp);
-      int kp = 0, ks = 0;       // pages consumed; K chunk slot ring: slot, phase
-      uint32_t kph = 0;
-      int pend = -1;            // TMEM slot of the last stored chunk not yet signalled
+      int kp = 0;               // pages consumed
+      int ks = kg;              // slot of this group's next chunk (chunk number kg, kg+2, ...)
+      uint32_t kph = 0;         // its phase
       bool ok = true;
       long long x = x0;
       int g = group_of(tile_start, a.n_groups, x);
@@ -467,65 +472,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             const uint32_t page = tc::smem_u32(sK) + ((kp + (t >> 6)) % NKR) * C::PSLOT;
             slot = t & 63;
             srow_s = page + slot * (D / 2);
-            ssc_s = page + C::PAGE_DATA + slot * 8 + 2 * kh;
+            ssc_s = page + C::PAGE_DATA + slot * 8;
           } else {
             valid = t < u.n_win;
-            row = u.wk + (size_t)t * D + 32 * kh;
+            row = u.wk + (size_t)t * D;
           }
 #pragma unroll 1
-          for (int c = 0; c < C::NKCH; ++c) {
-            uint32_t r[16];
+          for (int c = kg; c < C::NKCH; c += 2) {
+            uint32_t r[32];
             if (!valid) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) r[i] = 0u;
+              for (int i = 0; i < 32; ++i) r[i] = 0u;
             } else if (!win) {
               constexpr int SW = (D / 32 < 8 ? D / 32 : 8) - 1;
-              // 16 bytes = channels 64c + 32kh .. +31 (two scale blocks)
-              const uint4 v = tc::lds128(srow_s + 16 * ((2 * c + kh) ^ (slot & SW)));
-              const uint32_t sc = tc::lds16(ssc_s + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
-              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-              // scale pairs (s0, s0) and (s1, s1) of the two blocks
-              const uint32_t s2[2] = {tc::e4m3x2_to_f16x2((sc & 0xFFu) * 0x101u), tc::e4m3x2_to_f16x2((sc >> 8) * 0x101u)};
+              // channels 64c .. 64c+63: two 16-byte pieces, four scale blocks
+              const uint4 v0 = tc::lds128(srow_s + 16 * ((2 * c) ^ (slot & SW)));
+              const uint4 v1 = tc::lds128(srow_s + 16 * ((2 * c + 1) ^ (slot & SW)));
+              const uint32_t sc = tc::lds32(ssc_s + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
+              const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {              // word q: channels 8q .. 8q+7 of this half-chunk
+              for (int q = 0; q < 8; ++q) {              // word q: channels 8q .. 8q+7 of the chunk
+                const uint32_t s2 = tc::e4m3x2_to_f16x2(((sc >> (8 * (q >> 1))) & 0xFFu) * 0x101u);
                 uint32_t e[4];
                 tc::e2m1x8_to_f16x2x4(w[q], e);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) r[4 * q + i] = tc::hmul2(e[i], s2[q >> 1]);
+                for (int i = 0; i < 4; ++i) r[4 * q + i] = tc::hmul2(e[i], s2);
               }
             } else {
               const uint4* p4 = reinterpret_cast<const uint4*>(row + 64 * c);
 #pragma unroll
-              for (int h4 = 0; h4 < 2; ++h4) {
+              for (int h4 = 0; h4 < 4; ++h4) {
                 const uint4 v = __ldg(p4 + h4);
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) tc::e4m3x4_to_f16x2x2(w[i], &r[8 * h4 + 2 * i]);
               }
             }
-            // the previous chunk's store had this chunk's conversion time to land: signal it now
-            if (pend >= 0) {
-              tc::tc_wait_st();
-              tc::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) tc::mbar_arrive(&sh.kfull[pend]);
-              pend = -1;
-            }
+            tc::reg_fence32(r);               // conversion done before the (blocking) slot wait
             const bool w_ok = tc::mbar_wait(&sh.kempty[ks], kph ^ 1, abort_p);
             if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-            tc::tmem_st16(tbase + lb + COL_K + 32 * ks + 16 * kh, r);
-            pend = ks;
-            if (++ks == NKS) { ks = 0; kph ^= 1; }
-          }
-          if (!ok) break;
-          // last chunk of the tile: signal it now (its K/V tile ends here)
-          if (pend >= 0) {
+            tc::tmem_st32(tbase + lb + COL_K + 32 * ks, r);
             tc::tc_wait_st();
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.kfull[pend]);
-            pend = -1;
+            if (lane == 0) tc::mbar_arrive(&sh.kfull[ks]);
+            ks += 2;
+            if (ks >= NKS) { ks -= NKS; kph ^= 1; }
           }
+          if (!ok) break;
           if (!win) {
             __syncwarp();
             if (lane == 0)
@@ -536,25 +530,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         x = tile_start[g] + j1;
         ++g;
       }
-      tc::tc_wait_st();
-      if (pend >= 0 && ok) {
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sh.kfull[pend]);
-      }
     }
     // ======================================================== V dequantizer (thread = channel)
-    // warp pair (w, w+4) shares a TMEM lane quarter; warp (w-8)/4 == vh takes
-    // tokens 32*vh .. 32*vh+31 of every 64-token sub-chunk (16 TMEM columns).
+    // Two groups of four warps (one warp per TMEM lane quarter); the V^T chunks
+    // of a tile (128 channels x 64 tokens) are taken page-major - every channel
+    // chunk of page half 0, then of half 1 - and group vg converts the chunks of
+    // parity vg, a full 32-column slot each.  Each warp converts the E4M3 block
+    // scales it needs once (two per lane) and shares them through shared memory.
     else if (warp < W_SMAX) {
       const int vw = warp - W_VDEQ;                  // 0..7
       const int dl = 32 * (vw & 3) + lane;           // channel lane 0..127 within a chunk
-      const int vh = vw >> 2;                        // token half of each sub-chunk
+      const int vg = vw >> 2;                        // chunk parity of this group
       const uint32_t lb = lane_base(warp);
       const uint32_t vsc_s = tc::smem_u32(sh.vsc[vw]);
-      int vp = 0, vs = 0;       // pages consumed; V chunk slot ring: slot, phase
-      uint32_t vph = 0;
-      int pend = -1;            // TMEM slot of the last stored chunk not yet signalled
+      int vp = 0;               // pages consumed
+      int vs = vg;              // slot of this group's next chunk
+      uint32_t vph = 0;         // its phase
       bool ok = true;
       long long x = x0;
       int g = group_of(tile_start, a.n_groups, x);
@@ -567,8 +558,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           const bool win = (j == nt - 1);
           const int npg = win ? 0 : ((TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1);
           const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
-          // page-major: every channel chunk of page half 0, then of half 1, so that
-          // a page is released as soon as its codes are read
 #pragma unroll 1
           for (int half = 0; half < 2 && ok; ++half) {       // tokens 64*half .. 64*half+63
             const bool paged = half < npg;
@@ -577,23 +566,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
             }
             const uint32_t base = tc::smem_u32(sV) + ((vp + half) % NVR) * C::PSLOT;
+            // chunk cp = half * NVCH + c belongs to group cp & 1
 #pragma unroll 1
-            for (int c = 0; c < C::NVCH; ++c) {
+            for (int c = (vg ^ (half * C::NVCH)) & 1; c < C::NVCH; c += 2) {
               const int d = 128 * c + dl;
-              uint32_t r[16];
+              uint32_t r[32];
               if (paged) {
-                // block scales of this warp's two channel blocks x 32 tokens: lane
-                // converts the token pair (lane & 15) of block (lane >> 4) once
+                // block scales of this warp's two channel blocks x 64 tokens: lane
+                // converts token pairs (lane & 15) and 16 + (lane & 15) of block (lane >> 4)
                 const int blk = ((128 * c + 32 * (vw & 3)) >> 4) + (lane >> 4);
-                const uint32_t s16 = tc::lds16(base + C::PAGE_DATA + blk * PKV_PAGE + 32 * vh + 2 * (lane & 15));
-                const uint32_t s2 = tc::e4m3x2_to_f16x2(s16);
+                const uint32_t sb = base + C::PAGE_DATA + blk * PKV_PAGE + 2 * (lane & 15);
+                const uint32_t s2a = tc::e4m3x2_to_f16x2(tc::lds16(sb));
+                const uint32_t s2b = tc::e4m3x2_to_f16x2(tc::lds16(sb + 32));
                 __syncwarp();                            // previous readers of vsc are done
-                tc::sts32(vsc_s + 4 * lane, s2);
+                tc::sts32(vsc_s + 4 * (lane >> 4) * 32 + 4 * (lane & 15), s2a);
+                tc::sts32(vsc_s + 4 * (lane >> 4) * 32 + 64 + 4 * (lane & 15), s2b);
                 __syncwarp();
-                const uint32_t sp = vsc_s + 64 * (lane >> 4);
-                const uint32_t wd = base + 4 * (4 * vh * D + d);
+                const uint32_t sp = vsc_s + 128 * (lane >> 4);   // this channel's block: 32 pairs
+                const uint32_t wd = base + 4 * d;
 #pragma unroll
-                for (int o = 0; o < 4; ++o) {              // octet 4*vh + o of the page
+                for (int o = 0; o < 8; ++o) {              // octet o of the page: tokens 8o .. 8o+7
                   const uint32_t w = tc::lds32(wd + 4 * o * D);
                   const uint4 s4 = tc::lds128(sp + 16 * o);
                   const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
@@ -605,64 +597,48 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               } else if (win) {
                 const uint8_t* col = u.wv + d;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const int e = 64 * half + 32 * vh + 2 * i;
+                for (int i = 0; i < 32; ++i) {
+                  const int e = 64 * half + 2 * i;
                   const uint32_t b0 = __ldg(col + (size_t)e * D), b1 = __ldg(col + (size_t)(e + 1) * D);
                   r[i] = tc::e4m3x2_to_f16x2(b0 | (b1 << 8));
                 }
               } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) r[i] = 0u;      // second page absent: no valid token
+                for (int i = 0; i < 32; ++i) r[i] = 0u;      // second page absent: no valid token
               }
               // zero the tokens beyond the valid count (their K rows are zero too)
-              const int t0 = 64 * half + 32 * vh;
-              if (t0 + 32 > nvalid) {
+              const int t0 = 64 * half;
+              if (t0 + 64 > nvalid) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 32; ++i) {
                   const int tt = t0 + 2 * i;
                   if (tt >= nvalid) r[i] = 0u;
                   else if (tt + 1 >= nvalid) r[i] &= 0xFFFFu;
                 }
               }
-              if (pend >= 0) {
-                tc::tc_wait_st();
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&sh.vfull[pend]);
-                pend = -1;
-              }
+              tc::reg_fence32(r);             // conversion done before the (blocking) slot wait
               const bool w_ok = tc::mbar_wait(&sh.vempty[vs], vph ^ 1, abort_p);
               if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-              tc::tmem_st16(tbase + lb + COL_V + 32 * vs + 16 * vh, r);
-              pend = vs;
-              if (++vs == NVS) { vs = 0; vph ^= 1; }
+              tc::tmem_st32(tbase + lb + COL_V + 32 * vs, r);
+              tc::tc_wait_st();
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
+              vs += 2;
+              if (vs >= NVS) { vs -= NVS; vph ^= 1; }
             }
             if (!ok) break;
             if (paged) {
-              // every code of this page is in registers / TMEM now: release it
+              // every code of this page this warp needs is in TMEM now: release it
               __syncwarp();
               if (lane == 0) tc::mbar_arrive(&sh.vr_empty[(vp + half) % NVR]);
             }
           }
           if (!ok) break;
-          // last chunk of the tile: signal it now (its K/V tile ends here)
-          if (pend >= 0) {
-            tc::tc_wait_st();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.vfull[pend]);
-            pend = -1;
-          }
           vp += npg;
         }
         x = tile_start[g] + j1;
         ++g;
-      }
-      tc::tc_wait_st();
-      if (pend >= 0 && ok) {
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sh.vfull[pend]);
       }
     }
     // ======================================================== softmax + epilogue
