@@ -132,8 +132,9 @@ __device__ __forceinline__ Unit unit_of(const AttnArgs& a, int g) {
 }
 
 // ---------------------------------------------------------------- plan kernel
-// tile_start[g] = sum over g' < g of (ceil(n_glob(g')/128) + 1); tile_start[n] = total
-__global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, int* tile_start) {
+// tile_start[g] = sum over g' < g of (ceil(n_glob(g')/128) + 1); tile_start[n] = total;
+// then tile_start[n + 1 + c] = the query row where CTA c (of G) starts.
+__global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, int* tile_start, int G) {
   __shared__ int wsum[32];
   __shared__ int carry;
   if (threadIdx.x == 0) carry = 0;
@@ -164,6 +165,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, int* tile_start)
     __syncthreads();
   }
   if (threadIdx.x == 0) tile_start[a.n_groups] = carry;
+  __syncthreads();
+  const long long T = carry;
+  for (int c = threadIdx.x; c < G; c += 1024) tile_start[a.n_groups + 1 + c] = group_of(tile_start, a.n_groups, cta_start(T, G, c));
 }
 
 // ---------------------------------------------------------------- helpers
@@ -211,21 +215,32 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
 // K-major with the 128-byte swizzle, heads >= H zero.  Called by the 256 softmax threads.
 template <int D>
 __device__ __noinline__ void load_q(const AttnArgs& a, int g, uint8_t* sQ, int st) {
+  constexpr int NV = NH * D / 8 / 256;                // 16-byte vectors per thread
+  constexpr int NB = 4;                               // loads in flight per thread
+  static_assert(NV % NB == 0, "Q vectors per thread");
   const uint16_t* qg = a.q + (size_t)g * a.H * D;
-  for (int v = st; v < NH * D / 8; v += 256) {
-    const int h = v / (D / 8), c8 = v % (D / 8);      // 8 channels per vector
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (h < a.H) {
-      const uint4 in = __ldg(reinterpret_cast<const uint4*>(qg + (size_t)h * D + 8 * c8));
-      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  const uint32_t sq = tc::smem_u32(sQ);
+#pragma unroll 1
+  for (int b0 = 0; b0 < NV; b0 += NB) {
+    uint4 in[NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int v = st + 256 * (b0 + k);
+      const int h = v / (D / 8), c8 = v % (D / 8);    // 8 channels per vector
+      in[k] = h < a.H ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)h * D + 8 * c8)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int v = st + 256 * (b0 + k);
+      const int h = v / (D / 8), c8 = v % (D / 8);
+      const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
       uint32_t r[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         r[i] = f32_to_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-      o = make_uint4(r[0], r[1], r[2], r[3]);
+      const int atom = c8 >> 3, ch = c8 & 7;
+      tc::sts128(sq + atom * (NH * 128) + h * 128 + 16 * (ch ^ (h & 7)), make_uint4(r[0], r[1], r[2], r[3]));
     }
-    const int atom = c8 >> 3, ch = c8 & 7;
-    *reinterpret_cast<uint4*>(sQ + atom * (NH * 128) + h * 128 + 16 * (ch ^ (h & 7))) = o;
   }
   tc::fence_proxy_async_smem();
 }
@@ -244,6 +259,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   const int G = gridDim.x, cta = blockIdx.x;
   const long long T = tile_start[a.n_groups];
   const long long x0 = cta_start(T, G, cta), x1 = cta_start(T, G, cta + 1);
+  const int g0 = tile_start[a.n_groups + 1 + cta];     // query row of tile x0 (from the plan)
 
   if (tid == 0) {
     for (int i = 0; i < NKR; ++i) {
@@ -308,12 +324,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         int pi = 0;     // pages issued
         bool ok = true;
         long long x = x0;
-        int g = group_of(tile_start, a.n_groups, x);
+        int g = g0;
+        const uint8_t* last_win = nullptr;
         while (x < x1 && ok) {
           const Unit u = unit_of(a, g);
           const int nt = tile_start[g + 1] - tile_start[g];
           const int j0 = (int)(x - tile_start[g]);
           const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+          // the window tile (last of the row) is read from global memory by the
+          // dequant warps: warm L2 with it while the paged tiles stream
+          // the next query row's Q (loaded by the softmax at this row's end): warm L2
+          if (isK && j0 == 0 && x1 > tile_start[g + 1] && g + 1 < a.n_groups &&
+              ((uintptr_t)a.q & 15u) == 0)
+            tc::bulk_prefetch_l2(a.q + (size_t)(g + 1) * a.H * D, (uint32_t)(a.H * D * 2));
+          if (isK && j1 == nt && u.wk != last_win &&
+              (((uintptr_t)u.wk | (uintptr_t)u.wv) & 15u) == 0) {
+            tc::bulk_prefetch_l2(u.wk, (uint32_t)(PKV_WINDOW * D));    // window buffers are [B][128][d]
+            tc::bulk_prefetch_l2(u.wv, (uint32_t)(PKV_WINDOW * D));
+            last_win = u.wk;
+          }
           for (int j = j0; j < j1 && ok; ++j) {
             if (j == nt - 1) continue;      // window tile: read directly by the dequant warps
             const int npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
@@ -351,7 +380,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       uint32_t kph = 0;          // K slot ring: slot, phase
       bool ok = true;
       long long x = x0;
-      int g = group_of(tile_start, a.n_groups, x);
+      int g = g0;
       while (x < x1 && ok) {
         const int j1 = (int)min((long long)(tile_start[g + 1] - tile_start[g]), x1 - tile_start[g]);
         // Q of this item in shared memory
@@ -396,7 +425,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       uint32_t vph = 0;          // V slot ring: slot, phase
       bool ok = true;
       long long x = x0;
-      int g = group_of(tile_start, a.n_groups, x);
+      int g = g0;
       while (x < x1 && ok) {
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)(tile_start[g + 1] - tile_start[g]), x1 - tile_start[g]);
@@ -449,7 +478,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       uint32_t kph = 0;         // its phase
       bool ok = true;
       long long x = x0;
-      int g = group_of(tile_start, a.n_groups, x);
+      int g = g0;
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
         const int nt = tile_start[g + 1] - tile_start[g];
@@ -548,7 +577,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       uint32_t vph = 0;         // its phase
       bool ok = true;
       long long x = x0;
-      int g = group_of(tile_start, a.n_groups, x);
+      int g = g0;
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
         const int nt = tile_start[g + 1] - tile_start[g];
@@ -653,7 +682,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       int ntile = 0;
       bool ok = true;
       long long x = x0;
-      int g = group_of(tile_start, a.n_groups, x);
+      int g = g0;
       load_q<D>(a, g, sQ, st);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh.q_full);
@@ -690,12 +719,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sh.s_empty);
-          // all S of this item consumed: Q of the next item may replace this one
-          if (j == j1 - 1 && xn < x1) {
-            load_q<D>(a, g + 1, sQ, st);
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.q_full);
-          }
           // P buffer ntile&1 is free once the P.V of tile ntile-2 is done
           const int pb = ntile & 1;
           w_ok = tc::mbar_wait(&sh.p_empty[pb], ((ntile >> 1) & 1) ^ 1, abort_p);
@@ -792,6 +815,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sh.p_full[pb]);
           ++ntile;
+          // all S of this item consumed: Q of the next item may replace this one
+          // (done here, where few registers are live across the call)
+          if (j == j1 - 1 && xn < x1) {
+            load_q<D>(a, g + 1, sQ, st);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.q_full);
+          }
         }
         if (!ok) break;
         // ---- end of the item: wait for its last P.V, then write the partial
@@ -806,28 +836,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         }
         tc::named_bar(1, 256);
         const size_t prow_i = (size_t)cta + (size_t)g;          // partial row of this segment
+        // per head: output factor ts_v / l (0 when l = 0) and the partial LSE
+        if (st < NH) {
+          const float lh = sh.red[0][st] + sh.red[1][st] + sh.red[2][st] + sh.red[3][st];
+          sh.alpha[st] = lh > 0.f ? a.cache.ts_v / lh : 0.f;
+          if (st < a.H) part_lse[prow_i * a.H + st] = lh > 0.f ? (sh.m[st] + log2f(lh)) * LN2 : -INFINITY;
+        }
+        tc::named_bar(1, 256);
         float* po = part_o + prow_i * a.H * D;
+        const uint32_t al_s = tc::smem_u32(sh.alpha);
 #pragma unroll 1
         for (int c = 0; c < C::NVCH; ++c) {
           const int d = 128 * c + t;
-#pragma unroll
+#pragma unroll 1
           for (int hq = 0; hq < 2; ++hq) {
+            const int hb = 32 * hh + 16 * hq;
             uint32_t o[16];
-            tc::tmem_ld16(tbase + lb + COL_O + 64 * c + 32 * hh + 16 * hq, o);
+            tc::tmem_ld16(tbase + lb + COL_O + 64 * c + hb, o);
             tc::tc_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int h = 32 * hh + 16 * hq + i;
-              if (h < a.H) {
-                const float lh = sh.red[0][h] + sh.red[1][h] + sh.red[2][h] + sh.red[3][h];
-                po[(size_t)h * D + d] = lh > 0.f ? __uint_as_float(o[i]) * (a.cache.ts_v / lh) : 0.f;
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const uint4 f = tc::lds128(al_s + 4 * (hb + 4 * i4));
+              const float fv[4] = {__uint_as_float(f.x), __uint_as_float(f.y), __uint_as_float(f.z), __uint_as_float(f.w)};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int h = hb + 4 * i4 + i;
+                if (h < a.H) po[(size_t)h * D + d] = __uint_as_float(o[4 * i4 + i]) * fv[i];
               }
             }
           }
-        }
-        if (st < a.H) {
-          const float lh = sh.red[0][st] + sh.red[1][st] + sh.red[2][st] + sh.red[3][st];
-          part_lse[prow_i * a.H + st] = lh > 0.f ? (sh.m[st] + log2f(lh)) * LN2 : -INFINITY;
         }
         tc::tc_fence_before();
         tc::named_bar(1, 256);                 // sh.red / sh.m reads done before the next item resets them
@@ -940,7 +977,8 @@ static int tc_grid(int num_sms, int n_groups, int max_entries) {
 
 size_t pkv_attn_tc_ws_bytes(int num_sms, int H, int D, int n_groups, int max_entries) {
   const size_t rows = (size_t)tc_grid(num_sms, n_groups, max_entries) + n_groups;
-  return 256 + ((size_t)(n_groups + 1) * 4 + 255) / 256 * 256 + rows * H * D * 4 + rows * H * 4 + 256;
+  const size_t plan = (size_t)(n_groups + 1 + tc_grid(num_sms, n_groups, max_entries)) * 4;
+  return 256 + (plan + 255) / 256 * 256 + rows * H * D * 4 + rows * H * 4 + 256;
 }
 
 cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, float* out, float* out_lse,
@@ -948,13 +986,13 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   using namespace pkv::tcattn;
   uint8_t* p = (uint8_t*)ws;
   int* tile_start = (int*)p;
-  p += ((size_t)(a.n_groups + 1) * 4 + 255) / 256 * 256;
   const int G = tc_grid(num_sms, a.n_groups, max_entries);
+  p += ((size_t)(a.n_groups + 1 + G) * 4 + 255) / 256 * 256;
   const size_t rows = (size_t)G + a.n_groups;
   float* part_o = (float*)p;
   p += rows * a.H * a.D * 4;
   float* part_lse = (float*)p;
-  plan_kernel<<<1, 1024, 0, st>>>(a, tile_start);
+  plan_kernel<<<1, 1024, 0, st>>>(a, tile_start, G);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (e0 && e1) cudaEventRecord(e0, st);
