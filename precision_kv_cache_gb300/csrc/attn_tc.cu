@@ -519,13 +519,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               const uint4 v1 = tc::lds128(srow_s + 16 * ((2 * c + 1) ^ (slot & SW)));
               const uint32_t sc = tc::lds32(ssc_s + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
               const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+              uint32_t s4[2];                            // f16 scales: (s0, s1), (s2, s3)
+              tc::e4m3x4_to_f16x2x2(sc, s4);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {              // word q: channels 8q .. 8q+7 of the chunk
-                const uint32_t s2 = tc::e4m3x2_to_f16x2(((sc >> (8 * (q >> 1))) & 0xFFu) * 0x101u);
+              for (int q = 0; q < 8; ++q) {              // word q: channels 8q .. 8q+7 of the chunk (block q/2)
                 uint32_t e[4];
                 tc::e2m1x8_to_f16x2x4(w[q], e);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) r[4 * q + i] = tc::hmul2(e[i], s2);
+                for (int i = 0; i < 4; ++i)
+                  r[4 * q + i] = (q & 2) ? tc::hmul2_hi(e[i], s4[q >> 2]) : tc::hmul2_lo(e[i], s4[q >> 2]);
               }
             } else {
               const uint4* p4 = reinterpret_cast<const uint4*>(row + 64 * c);

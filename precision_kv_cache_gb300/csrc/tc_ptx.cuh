@@ -328,6 +328,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
       : "r"(two_bytes));
   return out;
 }
+// a * (lo half of s, lo half of s) and a * (hi, hi): f16x2 products by one broadcast scale
+__device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t s) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 t;\n\tmov.b32 {l, h}, %2;\n\tmov.b32 t, {l, l};\n\t"
+      "mul.rn.f16x2 %0, %1, t;\n\t}" : "=r"(d) : "r"(a), "r"(s));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmul2_hi(uint32_t a, uint32_t s) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 t;\n\tmov.b32 {l, h}, %2;\n\tmov.b32 t, {h, h};\n\t"
+      "mul.rn.f16x2 %0, %1, t;\n\t}" : "=r"(d) : "r"(a), "r"(s));
+  return d;
+}
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
