@@ -146,7 +146,7 @@ size_t pkv_workspace_bytes(const pkv_ctx* c, int op, int batch, int max_len) {
       return pkv_gather_ws_bytes(c->cfg.d, batch, max_len) + 256 + attn_ws_bytes(c, batch, kp + PKV_WINDOW);
     }
     case PKV_OP_SCORE_TOPK:
-      return (size_t)batch * (size_t)max_len * 4 + 256 + pkv_score_tc_ws_bytes(batch) +
+      return (size_t)batch * (size_t)max_len * 4 + 256 + pkv_score_tc_ws_bytes(batch, c->num_sms) +
              pkv_topk_ws_bytes(batch, PKV_TOPK_MAX_K) + 256;
   }
   return 0;
@@ -207,7 +207,7 @@ pkv_status pkv_score_topk(pkv_ctx* c, const uint8_t* q_idx, float tq, const floa
   p += (size_t)B * Lmax * 4;
   p = (uint8_t*)(((uintptr_t)p + 255) & ~(uintptr_t)255);
   void* plan = p;
-  p += pkv_score_tc_ws_bytes(B);
+  p += pkv_score_tc_ws_bytes(B, c->num_sms);
   c->launches += 2 + PKV_TOPK_LAUNCHES;
   cudaError_t e = pkv_launch_score_tc(q_idx, tq, w, *ic, page_table, max_pages, seq_len, B, c->cfg.n_index_heads,
                                       scores, Lmax, plan, c->num_sms, c->d_err, st);

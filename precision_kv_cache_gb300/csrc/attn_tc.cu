@@ -313,59 +313,70 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     // one warp streams K pages (codes + scales) into the K ring, another V pages
     // into the V ring, one page per slot, with 1-D bulk copies.
     if (warp == W_KPROD || warp == W_VPROD) {
-      if (lane == 0) {
-        const bool isK = (warp == W_KPROD);
-        const int nslot = isK ? NKR : NVR;
-        uint64_t* fullb = isK ? sh.kr_full : sh.vr_full;
-        uint64_t* emptyb = isK ? sh.kr_empty : sh.vr_empty;
-        uint8_t* ring = isK ? sK : sV;
-        const uint8_t* gdata = isK ? a.cache.k_data : a.cache.v_data;
-        const uint8_t* gscale = isK ? a.cache.k_scale : a.cache.v_scale;
-        int pi = 0;     // pages issued
-        bool ok = true;
-        long long x = x0;
-        int g = g0;
-        const uint8_t* last_win = nullptr;
-        while (x < x1 && ok) {
-          const Unit u = unit_of(a, g);
-          const int nt = tile_start[g + 1] - tile_start[g];
-          const int j0 = (int)(x - tile_start[g]);
-          const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+      // The whole warp walks the pages; page-table entries are read 32 at a time
+      // (one per lane, coalesced) and lane 0 issues the copies.
+      const bool isK = (warp == W_KPROD);
+      const int nslot = isK ? NKR : NVR;
+      uint64_t* fullb = isK ? sh.kr_full : sh.vr_full;
+      uint64_t* emptyb = isK ? sh.kr_empty : sh.vr_empty;
+      uint8_t* ring = isK ? sK : sV;
+      const uint8_t* gdata = isK ? a.cache.k_data : a.cache.v_data;
+      const uint8_t* gscale = isK ? a.cache.k_scale : a.cache.v_scale;
+      int pi = 0;     // pages issued
+      bool ok = true;
+      long long x = x0;
+      int g = g0;
+      const uint8_t* last_win = nullptr;
+      while (x < x1 && ok) {
+        const Unit u = unit_of(a, g);
+        const int nt = tile_start[g + 1] - tile_start[g];
+        const int j0 = (int)(x - tile_start[g]);
+        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        if (lane == 0) {
+          // the next query row's Q (loaded by the softmax at this row's end): warm L2
+          if (isK && j0 == 0 && x1 > tile_start[g + 1] && g + 1 < a.n_groups && ((uintptr_t)a.q & 15u) == 0)
+            tc::bulk_prefetch_l2(a.q + (size_t)(g + 1) * a.H * D, (uint32_t)(a.H * D * 2));
           // the window tile (last of the row) is read from global memory by the
           // dequant warps: warm L2 with it while the paged tiles stream
-          // the next query row's Q (loaded by the softmax at this row's end): warm L2
-          if (isK && j0 == 0 && x1 > tile_start[g + 1] && g + 1 < a.n_groups &&
-              ((uintptr_t)a.q & 15u) == 0)
-            tc::bulk_prefetch_l2(a.q + (size_t)(g + 1) * a.H * D, (uint32_t)(a.H * D * 2));
-          if (isK && j1 == nt && u.wk != last_win &&
-              (((uintptr_t)u.wk | (uintptr_t)u.wv) & 15u) == 0) {
+          if (isK && j1 == nt && u.wk != last_win && (((uintptr_t)u.wk | (uintptr_t)u.wv) & 15u) == 0) {
             tc::bulk_prefetch_l2(u.wk, (uint32_t)(PKV_WINDOW * D));    // window buffers are [B][128][d]
             tc::bulk_prefetch_l2(u.wv, (uint32_t)(PKV_WINDOW * D));
             last_win = u.wk;
           }
-          for (int j = j0; j < j1 && ok; ++j) {
-            if (j == nt - 1) continue;      // window tile: read directly by the dequant warps
-            const int npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
-            for (int q = 0; q < npg; ++q) {
-              int p = a.page_table[(size_t)u.b * a.max_pages + 2 * j + q];
+        }
+        // pages [2*j0, pend) of the row: those of its NVFP4 tiles in this CTA's range
+        const int jp = min(j1, nt - 1);
+        const int pend = min(2 * jp, (u.n_glob + PKV_PAGE - 1) / PKV_PAGE);
+        for (int pb = 2 * j0; pb < pend && ok; pb += 32) {
+          int pl = -1;
+          if (pb + lane < pend) pl = a.page_table[(size_t)u.b * a.max_pages + pb + lane];
+          const int cnt = min(32, pend - pb);
+          for (int q = 0; q < cnt; ++q) {
+            int p = __shfl_sync(0xffffffffu, pl, q);
+            if (lane == 0) {
               if (p < 0 || p >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); p = 0; }
               const int slot = pi % nslot, use = pi / nslot;
-              if (!tc::mbar_wait(&emptyb[slot], (use & 1) ^ 1, abort_p)) { fail(sh, a.err); ok = false; break; }
-              tc::mbar_arrive_expect_tx(&fullb[slot], C::PSLOT);
-              uint8_t* dst = ring + slot * C::PSLOT;
-              tc::bulk_g2s(dst, gdata + (size_t)p * pdb, C::PAGE_DATA, &fullb[slot]);
-              tc::bulk_g2s(dst + C::PAGE_DATA, gscale + (size_t)p * psb, C::PAGE_SCALE, &fullb[slot]);
-              ++pi;
+              if (!tc::mbar_wait(&emptyb[slot], (use & 1) ^ 1, abort_p)) { fail(sh, a.err); ok = false; }
+              if (ok) {
+                tc::mbar_arrive_expect_tx(&fullb[slot], C::PSLOT);
+                uint8_t* dst = ring + slot * C::PSLOT;
+                tc::bulk_g2s(dst, gdata + (size_t)p * pdb, C::PAGE_DATA, &fullb[slot]);
+                tc::bulk_g2s(dst + C::PAGE_DATA, gscale + (size_t)p * psb, C::PAGE_SCALE, &fullb[slot]);
+              }
             }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ++pi;
           }
-          x = tile_start[g] + j1;
-          ++g;
         }
-        // drain: every copy issued must have landed before this CTA may exit
-        // (the last use of each slot; earlier uses were waited for by the consumers)
+        x = tile_start[g] + j1;
+        ++g;
+      }
+      // drain: every copy issued must have landed before this CTA may exit
+      // (the last use of each slot; earlier uses were waited for by the consumers)
+      if (lane == 0)
         for (int k = (pi > nslot ? pi - nslot : 0); k < pi; ++k)
           tc::mbar_wait(&fullb[k % nslot], (k / nslot) & 1, abort_p, 1LL << 31);
-      }
     }
     // ======================================================== MMA issuers
     // One warp issues S^T = K Q^T (per 64-channel K chunk: 4 MMAs), another

@@ -2,13 +2,19 @@
 // vLLM blog "Kernels"):  score_t = sum_h w_h * ReLU(q_h . k_t)  over the
 // 128-channel NVFP4 index keys, for every position of every sequence.
 //
-// One persistent CTA per SM, 384 threads, warp-specialized like the attention
-// kernel: warp 0 streams the 64-token key pages into a shared-memory ring
-// (bulk copies), warps 4-7 (thread = token) dequantize a 128-token tile to f16
-// into TMEM (exact: E2M1 x E4M3), warp 1 issues S^T = K Q^T on tcgen05
-// (M = 128 tokens, N = 64 index heads, K = 128; Q = the FP8 index queries,
-// exact in f16, in shared memory), warps 8-11 read S^T back, apply ReLU, the
-// head weights and the two tensor scales, and store one FP32 score per token.
+// One persistent CTA per SM, 512 threads, warp-specialized:
+//   * warp 0 streams the 64-token key pages into a 24-page shared-memory ring
+//     (1-D bulk copies);
+//   * warps 4-11: two groups of four (one warp per TMEM lane quarter, thread =
+//     token) that take alternate 128-token tiles and dequantize them to f16
+//     into TMEM (exact: E2M1 x E4M3 has <= 6 significant bits);
+//   * warp 1 issues S^T = K Q^T on tcgen05 (M = 128 tokens, N = 64 index heads,
+//     K = 128; Q = the FP8 index queries, exact in f16, in shared memory), the
+//     whole warp running the schedule and one elected lane issuing;
+//   * warps 12-19: two groups of four that take alternate tiles, read S^T back,
+//     apply ReLU, the head weights and the two tensor scales, and store one
+//     FP32 score per token.
+// TMEM holds 4 K tiles and 4 S^T tiles (512 columns).
 #include "attn_tc.h"
 #include "launch.h"
 #include "tc_ptx.cuh"
@@ -19,8 +25,10 @@ namespace tcscore {
 constexpr int TILE = 128;
 constexpr int NH = 64;
 constexpr int D = 128;
-constexpr int NTHREADS = 384;
-constexpr int NR = 6;                                  // key ring: page slots
+constexpr int NTHREADS = 640;                          // 20 warps
+constexpr int W_PROD = 0, W_MMA = 1, W_DEQ = 4, W_EPI = 12;
+constexpr int NR = 24;                                 // key ring: page slots
+constexpr int NS = 4;                                  // K / S^T tile slots in TMEM
 constexpr int PAGE_DATA = PKV_PAGE * D / 2;            // 4096
 constexpr int PAGE_SCALE = PKV_PAGE * D / 16;          // 512
 constexpr int PSLOT = PAGE_DATA + PAGE_SCALE;          // 4608
@@ -28,15 +36,15 @@ constexpr int Q_BYTES = NH * D * 2;                    // 16 KB
 constexpr int OFF_Q = 0;
 constexpr int OFF_R = OFF_Q + Q_BYTES;
 constexpr int DYN = OFF_R + NR * PSLOT + 1024;
-constexpr uint32_t COL_S = 0;                          // 2 x 64 columns
-constexpr uint32_t COL_K = 128;                        // 2 x 64 columns
+constexpr uint32_t COL_S = 0;                          // NS x 64 columns
+constexpr uint32_t COL_K = 256;                        // NS x 64 columns
 
 struct Shared {
   uint64_t r_full[NR], r_empty[NR];
-  uint64_t kfull[2], kempty[2], s_full[2], s_empty[2], q_full, drain;
+  uint64_t kfull[NS], kempty[NS], s_full[NS], s_empty[NS], q_full, drain;
   uint32_t tmem_base;
   int abort_flag;
-  float w[NH];
+  alignas(16) float w[NH];
 };
 
 struct Args {
@@ -58,7 +66,20 @@ __device__ __forceinline__ int seq_tokens(const Args& a, int b) {
   return L < 0 ? 0 : L;
 }
 
-__global__ void __launch_bounds__(1024) plan_kernel(Args a, int* tile_start) {
+__device__ __forceinline__ long long cta_start(long long T, int G, int c) { return (T * c) / G; }
+
+__device__ __forceinline__ int group_of(const int* ts, int n, long long x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)ts[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// tile_start[b] = sum over b' < b of ceil(L(b')/128); tile_start[B] = total;
+// then tile_start[B + 1 + c] = the sequence where CTA c (of G) starts.
+__global__ void __launch_bounds__(1024) plan_kernel(Args a, int* tile_start, int G) {
   __shared__ int wsum[32];
   __shared__ int carry;
   if (threadIdx.x == 0) carry = 0;
@@ -83,17 +104,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a, int* tile_start) {
     __syncthreads();
   }
   if (threadIdx.x == 0) tile_start[a.B] = carry;
-}
-
-__device__ __forceinline__ long long cta_start(long long T, int G, int c) { return (T * c) / G; }
-
-__device__ __forceinline__ int group_of(const int* ts, int n, long long x) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((long long)ts[mid] <= x) lo = mid; else hi = mid - 1;
-  }
-  return lo;
+  __syncthreads();
+  const long long T = carry;
+  for (int c = threadIdx.x; c < G; c += 1024) tile_start[a.B + 1 + c] = group_of(tile_start, a.B, cta_start(T, G, c));
 }
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
@@ -104,18 +117,25 @@ __device__ __forceinline__ void fail(Shared& sh, int* err) {
 }
 
 // FP8 index queries of sequence b -> f16, K-major 128-byte swizzle; weights -> sh.w
+// (128 threads; all loads of a thread are issued before the conversions)
 __device__ __noinline__ void load_q(const Args& a, int b, uint8_t* sQ, float* sw, int tid) {
   const uint8_t* qb = a.q + (size_t)b * a.Hi * D;
-  for (int v = tid; v < NH * D / 8; v += 128) {
-    const int h = v / (D / 8), c8 = v % (D / 8);
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (h < a.Hi) {
-      const uint2 in = *reinterpret_cast<const uint2*>(qb + (size_t)h * D + 8 * c8);
-      o = make_uint4(tc::e4m3x2_to_f16x2(in.x & 0xFFFFu), tc::e4m3x2_to_f16x2(in.x >> 16),
-                     tc::e4m3x2_to_f16x2(in.y & 0xFFFFu), tc::e4m3x2_to_f16x2(in.y >> 16));
-    }
+  const uint32_t sq = tc::smem_u32(sQ);
+  constexpr int NV = NH * D / 8 / 128;                  // 8 vectors of 8 channels per thread
+  uint2 in[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int v = tid + 128 * k, h = v / (D / 8), c8 = v % (D / 8);
+    in[k] = h < a.Hi ? *reinterpret_cast<const uint2*>(qb + (size_t)h * D + 8 * c8) : make_uint2(0u, 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int v = tid + 128 * k, h = v / (D / 8), c8 = v % (D / 8);
+    uint32_t o[4];
+    tc::e4m3x4_to_f16x2x2(in[k].x, &o[0]);
+    tc::e4m3x4_to_f16x2x2(in[k].y, &o[2]);
     const int atom = c8 >> 3, ch = c8 & 7;
-    *reinterpret_cast<uint4*>(sQ + atom * (NH * 128) + h * 128 + 16 * (ch ^ (h & 7))) = o;
+    tc::sts128(sq + atom * (NH * 128) + h * 128 + 16 * (ch ^ (h & 7)), make_uint4(o[0], o[1], o[2], o[3]));
   }
   if (tid < NH) sw[tid] = tid < a.Hi ? a.w[(size_t)b * a.Hi + tid] : 0.f;
   tc::fence_proxy_async_smem();
@@ -129,12 +149,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
   const int G = gridDim.x, cta = blockIdx.x;
   const long long T = tile_start[a.B];
   const long long x0 = cta_start(T, G, cta), x1 = cta_start(T, G, cta + 1);
+  const int g0 = tile_start[a.B + 1 + cta];
   if (tid == 0) {
     for (int i = 0; i < NR; ++i) {
       tc::mbar_init(&sh.r_full[i], 1);
       tc::mbar_init(&sh.r_empty[i], 4);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NS; ++i) {
       tc::mbar_init(&sh.kfull[i], 4);
       tc::mbar_init(&sh.kempty[i], 1);
       tc::mbar_init(&sh.s_full[i], 1);
@@ -145,8 +166,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
     sh.abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 1) {
-    tc::tmem_alloc(&sh.tmem_base, 256);
+  if (warp == W_MMA) {
+    tc::tmem_alloc(&sh.tmem_base, 512);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -158,118 +179,139 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
   uint8_t* ring = dyn + OFF_R;
 
   if (x0 < x1) {
-    if (warp == 0) {
+    if (warp == W_PROD) {
       // ======================================================== producer
-      if (lane == 0) {
-        int pi = 0;
-        bool ok = true;
-        long long x = x0;
-        int g = group_of(tile_start, a.B, x);
-        while (x < x1 && ok) {
-          const int L = seq_tokens(a, g);
-          const int nt = tile_start[g + 1] - tile_start[g];
-          const int j0 = (int)(x - tile_start[g]);
-          const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
-          for (int j = j0; j < j1 && ok; ++j) {
-            const int npg = (TILE * j + PKV_PAGE < L) ? 2 : 1;
-            for (int q = 0; q < npg; ++q) {
-              int p = a.page_table[(size_t)g * a.max_pages + 2 * j + q];
-              if (p < 0 || p >= a.ic.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); p = 0; }
-              const int slot = pi % NR, use = pi / NR;
-              if (!tc::mbar_wait(&sh.r_empty[slot], (use & 1) ^ 1, abort_p)) { fail(sh, a.err); ok = false; break; }
-              tc::mbar_arrive_expect_tx(&sh.r_full[slot], PSLOT);
-              uint8_t* dst = ring + slot * PSLOT;
-              tc::bulk_g2s(dst, a.ic.data + (size_t)p * PAGE_DATA, PAGE_DATA, &sh.r_full[slot]);
-              tc::bulk_g2s(dst + PAGE_DATA, a.ic.scale + (size_t)p * PAGE_SCALE, PAGE_SCALE, &sh.r_full[slot]);
-              ++pi;
-            }
-          }
-          x = tile_start[g] + j1;
-          ++g;
-        }
-        for (int k = (pi > NR ? pi - NR : 0); k < pi; ++k)
-          tc::mbar_wait(&sh.r_full[k % NR], (k / NR) & 1, abort_p, 1LL << 31);
-      }
-    } else if (warp == 1) {
-      // ======================================================== MMA issuer
-      if (lane == 0) {
-        const uint32_t idq = tc::idesc_f16(128, NH, false, false);
-        const uint32_t qaddr = tc::smem_u32(sQ);
-        int n = 0, item = 0;
-        bool ok = true;
-        long long x = x0;
-        int g = group_of(tile_start, a.B, x);
-        while (x < x1 && ok) {
-          const int nt = tile_start[g + 1] - tile_start[g];
-          const int j0 = (int)(x - tile_start[g]);
-          const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
-          if (j1 > j0) {
-            if (!tc::mbar_wait(&sh.q_full, item & 1, abort_p)) { fail(sh, a.err); ok = false; break; }
-            ++item;
-          }
-          for (int j = j0; j < j1 && ok; ++j) {
-            const int s = n & 1;
-            if (!tc::mbar_wait(&sh.s_empty[s], ((n >> 1) & 1) ^ 1, abort_p) ||
-                !tc::mbar_wait(&sh.kfull[s], (n >> 1) & 1, abort_p)) {
-              fail(sh, a.err);
-              ok = false;
-              break;
-            }
-            tc::tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint64_t bd = tc::sdesc_sw128(qaddr + (k >> 2) * (NH * 128) + (k & 3) * 32, 16, 1024);
-              tc::mma_ts(tbase + COL_S + 64 * s, tbase + COL_K + 64 * s + 8 * k, bd, idq, k != 0);
-            }
-            tc::mma_commit(&sh.kempty[s]);
-            tc::mma_commit(&sh.s_full[s]);
-            ++n;
-          }
-          x = tile_start[g] + j1;
-          ++g;
-        }
-        tc::mma_commit(&sh.drain);
-        tc::mbar_wait(&sh.drain, 0, abort_p, 1LL << 31);
-      }
-    } else if (warp >= 4 && warp < 8) {
-      // ======================================================== key dequantizer (thread = token)
-      const int t = tid - 128;
-      const uint32_t lb = lane_base(warp);
-      int pc = 0, n = 0;
+      // The whole warp walks the pages; each lane reads one page-table entry and
+      // issues that page's copies, so copies of consecutive pages go out in parallel.
+      int pi = 0;
       bool ok = true;
       long long x = x0;
-      int g = group_of(tile_start, a.B, x);
+      int g = g0;
       while (x < x1 && ok) {
         const int L = seq_tokens(a, g);
         const int nt = tile_start[g + 1] - tile_start[g];
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        // pages [2*j0, pend) of sequence g
+        const int pend = min(2 * j1, (L + PKV_PAGE - 1) / PKV_PAGE);
+        // up to 16 pages at a time, one lane each (16 <= NR: distinct ring slots)
+        for (int pb = 2 * j0; pb < pend && ok; pb += 16) {
+          const int cnt = min(16, pend - pb);
+          bool lok = true;
+          if (lane < cnt) {
+            int p = a.page_table[(size_t)g * a.max_pages + pb + lane];
+            if (p < 0 || p >= a.ic.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); p = 0; }
+            const int k = pi + lane, slot = k % NR, use = k / NR;
+            if (!tc::mbar_wait(&sh.r_empty[slot], (use & 1) ^ 1, abort_p)) {
+              fail(sh, a.err);
+              lok = false;
+            } else {
+              tc::mbar_arrive_expect_tx(&sh.r_full[slot], PSLOT);
+              uint8_t* dst = ring + slot * PSLOT;
+              tc::bulk_g2s(dst, a.ic.data + (size_t)p * PAGE_DATA, PAGE_DATA, &sh.r_full[slot]);
+              tc::bulk_g2s(dst + PAGE_DATA, a.ic.scale + (size_t)p * PAGE_SCALE, PAGE_SCALE, &sh.r_full[slot]);
+            }
+          }
+          ok = __all_sync(0xffffffffu, lok);
+          pi += cnt;
+        }
+        x = tile_start[g] + j1;
+        ++g;
+      }
+      if (lane == 0)
+        for (int k = (pi > NR ? pi - NR : 0); k < pi; ++k)
+          tc::mbar_wait(&sh.r_full[k % NR], (k / NR) & 1, abort_p, 1LL << 31);
+    } else if (warp == W_MMA) {
+      // ======================================================== MMA issuer (whole warp, one elected lane issues)
+      const uint32_t idq = tc::idesc_f16(128, NH, false, false);
+      const uint64_t dq0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
+      int s = 0, item = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      long long x = x0;
+      int g = g0;
+      while (x < x1 && ok) {
+        const int nt = tile_start[g + 1] - tile_start[g];
+        const int j0 = (int)(x - tile_start[g]);
+        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        if (j1 > j0) {
+          ok = tc::mbar_wait(&sh.q_full, item & 1, abort_p);
+          ++item;
+        }
         for (int j = j0; j < j1 && ok; ++j) {
+          ok = tc::mbar_wait(&sh.kfull[s], ph, abort_p) && tc::mbar_wait(&sh.s_empty[s], ph ^ 1, abort_p);
+          tc::compiler_fence();
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint32_t dS = tbase + COL_S + 64 * s, aK = tbase + COL_K + 64 * s;
+          if (tc::elect_one()) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              tc::mma_ts(dS, aK + 8 * k, dq0 + (uint64_t)((k >> 2) * (NH * 128 / 16) + (k & 3) * 2), idq, k != 0);
+            tc::mma_commit(&sh.kempty[s]);
+            tc::mma_commit(&sh.s_full[s]);
+          }
+          __syncwarp();
+          if (++s == NS) { s = 0; ph ^= 1; }
+        }
+        x = tile_start[g] + j1;
+        ++g;
+      }
+      if (!ok && lane == 0) fail(sh, a.err);
+      if (tc::elect_one()) tc::mma_commit(&sh.drain);
+      __syncwarp();
+      tc::mbar_wait(&sh.drain, 0, abort_p, 1LL << 31);
+    } else if (warp >= W_DEQ && warp < W_EPI) {
+      // ======================================================== key dequantizer (thread = token)
+      // group kg takes the tiles n = kg, kg+2, ... of this CTA (n counted from x0)
+      const int t = 32 * (warp & 3) + lane;
+      const int kg = (warp - W_DEQ) >> 2;
+      const uint32_t lb = lane_base(warp);
+      const uint32_t ring_s = tc::smem_u32(ring);
+      int pc = 0, n = 0;
+      bool ok = true;
+      long long x = x0;
+      int g = g0;
+      while (x < x1 && ok) {
+        const int L = seq_tokens(a, g);
+        const int nt = tile_start[g + 1] - tile_start[g];
+        const int j0 = (int)(x - tile_start[g]);
+        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        for (int j = j0; j < j1 && ok; ++j, ++n) {
           const int npg = (TILE * j + PKV_PAGE < L) ? 2 : 1;
-          const int s = n & 1;
-          bool w_ok = tc::mbar_wait(&sh.kempty[s], ((n >> 1) & 1) ^ 1, abort_p);
+          if ((n & 1) != kg) { pc += npg; continue; }
+          const int s = n % NS;
+          const uint32_t ph = (n / NS) & 1;
+          bool w_ok = tc::mbar_wait(&sh.kempty[s], ph ^ 1, abort_p);
           for (int q = 0; q < npg; ++q)
             w_ok = w_ok && tc::mbar_wait(&sh.r_full[(pc + q) % NR], ((pc + q) / NR) & 1, abort_p);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
           const bool valid = TILE * j + t < L;
-          const uint8_t* page = ring + ((pc + (t >> 6)) % NR) * PSLOT;
+          const uint32_t page = ring_s + ((pc + (t >> 6)) % NR) * PSLOT;
           const int slot = t & 63;
+          const uint32_t row = page + slot * (D / 2);
+          uint32_t sc[2] = {0u, 0u};
+          if (valid) {
+            const uint4 sv = tc::lds128(page + PAGE_DATA + (slot & ~1) * 8);   // 8 scale bytes of this token
+            sc[0] = (slot & 1) ? sv.z : sv.x;
+            sc[1] = (slot & 1) ? sv.w : sv.y;
+          }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {             // channels 64*hf .. 64*hf+63
             uint32_t r[32];
             if (valid) {
-              const uint8_t* row = page + slot * (D / 2);
-              const uint4 lo = *reinterpret_cast<const uint4*>(row + 16 * ((2 * hf) ^ (slot & 3)));
-              const uint4 hi = *reinterpret_cast<const uint4*>(row + 16 * ((2 * hf + 1) ^ (slot & 3)));
-              const uint32_t sc = *reinterpret_cast<const uint32_t*>(page + PAGE_DATA + slot * 8 + 4 * hf);
+              const uint4 lo = tc::lds128(row + 16 * ((2 * hf) ^ (slot & 3)));
+              const uint4 hi = tc::lds128(row + 16 * ((2 * hf + 1) ^ (slot & 3)));
               const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+              uint32_t s4[2];
+              tc::e4m3x4_to_f16x2x2(sc[hf], s4);
 #pragma unroll
-              for (int bk = 0; bk < 4; ++bk) {
-                const uint32_t sb = (sc >> (8 * bk)) & 0xFFu;
-                const uint32_t s2 = tc::e4m3x2_to_f16x2(sb | (sb << 8));
+              for (int q = 0; q < 8; ++q) {
+                uint32_t e[4];
+                tc::e2m1x8_to_f16x2x4(w[q], e);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  r[8 * bk + i] = tc::hmul2(tc::e2m1x2_to_f16x2((w[2 * bk + (i >> 2)] >> (8 * (i & 3))) & 0xFFu), s2);
+                for (int i = 0; i < 4; ++i)
+                  r[4 * q + i] = (q & 2) ? tc::hmul2_hi(e[i], s4[q >> 2]) : tc::hmul2_lo(e[i], s4[q >> 2]);
               }
             } else {
 #pragma unroll
@@ -285,65 +327,59 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
             for (int q = 0; q < npg; ++q) tc::mbar_arrive(&sh.r_empty[(pc + q) % NR]);
           }
           pc += npg;
-          ++n;
         }
         x = tile_start[g] + j1;
         ++g;
       }
-    } else if (warp >= 8) {
+    } else if (warp >= W_EPI) {
       // ======================================================== epilogue (thread = token)
-      const int t = tid - 256;
+      // group eg takes the tiles n = eg, eg+2, ... of this CTA
+      const int t = 32 * (warp & 3) + lane;
+      const int eg = (warp - W_EPI) >> 2;
       const uint32_t lb = lane_base(warp);
       const float sc = a.tq * a.ic.ts;
+      const uint32_t w_s = tc::smem_u32(sh.w);
       int n = 0;
       bool ok = true;
       long long x = x0;
-      int g = group_of(tile_start, a.B, x);
-      bool loaded = false;
+      int g = g0;
       while (x < x1 && ok) {
         const int L = seq_tokens(a, g);
         const int nt = tile_start[g + 1] - tile_start[g];
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         if (j1 > j0) {
-          if (!loaded) {
+          // every S^T of the previous sequence has been read (so its MMAs are done): new Q, w
+          tc::named_bar(1, 256);
+          if (eg == 0) {
             load_q(a, g, sQ, sh.w, t);
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&sh.q_full);
           }
-          loaded = false;
+          tc::named_bar(1, 256);                    // sh.w of this sequence visible to both groups
         }
-        tc::named_bar(1, 128);                      // sh.w of this sequence visible to all 4 warps
-        for (int j = j0; j < j1; ++j) {
-          const int s = n & 1;
-          const bool w_ok = tc::mbar_wait(&sh.s_full[s], (n >> 1) & 1, abort_p);
-          if (tc::named_bar_or(2, 128, !w_ok)) { fail(sh, a.err); ok = false; break; }
+        for (int j = j0; j < j1; ++j, ++n) {
+          if ((n & 1) != eg) continue;
+          const int s = n % NS;
+          const uint32_t ph = (n / NS) & 1;
+          const bool w_ok = tc::mbar_wait(&sh.s_full[s], ph, abort_p);
+          if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
           tc::tc_fence_after();
-          float acc = 0.f;
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t r[32];
-            tc::tmem_ld32(tbase + lb + COL_S + 64 * s + 32 * hf, r);
-            tc::tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc = fmaf(sh.w[32 * hf + i], fmaxf(__uint_as_float(r[i]), 0.f), acc);
-          }
+          uint32_t r[64];
+          tc::tmem_ld32(tbase + lb + COL_S + 64 * s, r);
+          tc::tmem_ld32(tbase + lb + COL_S + 64 * s + 32, r + 32);
+          tc::tc_wait_ld();
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sh.s_empty[s]);
-          ++n;
-          // all S^T of this sequence read: the next sequence's queries may replace these
-          if (j == j1 - 1) {
-            // next sequence with tiles in this CTA's range (empty sequences have none)
-            int gn = g + 1;
-            while (gn < a.B && tile_start[gn + 1] == tile_start[gn]) ++gn;
-            if (gn < a.B && tile_start[gn] < x1) {
-              tc::named_bar(1, 128);                // every warp is done with sh.w
-              load_q(a, gn, sQ, sh.w, t);
-              __syncwarp();
-              if (lane == 0) tc::mbar_arrive(&sh.q_full);
-              loaded = true;
-            }
+          float acc = 0.f;
+#pragma unroll
+          for (int i4 = 0; i4 < 16; ++i4) {
+            const uint4 wv = tc::lds128(w_s + 16 * i4);
+            acc = fmaf(__uint_as_float(wv.x), fmaxf(__uint_as_float(r[4 * i4]), 0.f), acc);
+            acc = fmaf(__uint_as_float(wv.y), fmaxf(__uint_as_float(r[4 * i4 + 1]), 0.f), acc);
+            acc = fmaf(__uint_as_float(wv.z), fmaxf(__uint_as_float(r[4 * i4 + 2]), 0.f), acc);
+            acc = fmaf(__uint_as_float(wv.w), fmaxf(__uint_as_float(r[4 * i4 + 3]), 0.f), acc);
           }
           const int tok = TILE * j + t;
           if (tok < L) a.scores[(size_t)g * a.Lmax + tok] = acc * sc;
@@ -356,13 +392,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc(tbase, 256);
+  if (warp == W_MMA) tc::tmem_dealloc(tbase, 512);
 }
 
 }  // namespace tcscore
 }  // namespace pkv
 
-size_t pkv_score_tc_ws_bytes(int B) { return ((size_t)(B + 1) * 4 + 255) / 256 * 256; }
+size_t pkv_score_tc_ws_bytes(int B, int num_sms) { return ((size_t)(B + 1 + num_sms) * 4 + 255) / 256 * 256; }
 
 cudaError_t pkv_score_tc_init() {
   return cudaFuncSetAttribute(pkv::tcscore::score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -378,9 +414,9 @@ cudaError_t pkv_launch_score_tc(const uint8_t* q_idx, float tq, const float* w, 
   a.q = q_idx; a.tq = tq; a.w = w; a.ic = ic; a.page_table = page_table; a.max_pages = max_pages;
   a.seq_len = seq_len; a.B = B; a.Hi = Hi; a.Lmax = Lmax; a.scores = scores; a.err = err;
   int* tile_start = (int*)ws;
-  plan_kernel<<<1, 1024, 0, st>>>(a, tile_start);
   const long long tmax = (long long)B * ((Lmax + TILE - 1) / TILE);
   const int G = (int)(tmax < num_sms ? (tmax > 0 ? tmax : 1) : num_sms);
+  plan_kernel<<<1, 1024, 0, st>>>(a, tile_start, G);
   score_tc_kernel<<<G, NTHREADS, DYN, st>>>(a, tile_start);
   return cudaGetLastError();
 }
