@@ -147,7 +147,7 @@ size_t pkv_workspace_bytes(const pkv_ctx* c, int op, int batch, int max_len) {
     }
     case PKV_OP_SCORE_TOPK:
       return (size_t)batch * (size_t)max_len * 4 + 256 + pkv_score_tc_ws_bytes(batch, c->num_sms) +
-             pkv_topk_ws_bytes(batch, PKV_TOPK_MAX_K) + 256;
+             pkv_topk_ws_bytes(batch, PKV_TOPK_MAX_K, max_len) + 256;
   }
   return 0;
 }

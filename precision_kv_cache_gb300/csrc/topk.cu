@@ -6,7 +6,8 @@
 //   pass 3  emit keys above (b1,b2); collect keys in (b1,b2) as candidates
 //   finish  sort candidates by (key desc, position asc), emit what is still needed
 //           (if the candidate buffer overflowed: an ordered scan of the sequence)
-//   sort    the k emitted positions ascending (bitonic, one block per sequence)
+//   extract "emit" sets the position's bit in a per-sequence bitmap; the k
+//           positions are read out of it in ascending order (no sort)
 #include "pkv_common.cuh"
 #include "launch.h"
 
@@ -39,9 +40,16 @@ __global__ void __launch_bounds__(TK_THREADS) tk_pass1(const float* __restrict__
   const int L = seq_length(seq_len, b, Lmax);
   const int base = blockIdx.x * TK_THREADS * TK_ITEMS;
   const float* s = scores + (size_t)b * Lmax;
+  float v[TK_ITEMS];                      // every load in flight before any use
+#pragma unroll
   for (int i = 0; i < TK_ITEMS; ++i) {
     const int t = base + i * TK_THREADS + threadIdx.x;
-    if (t < L) atomicAdd(&h[order_key(s[t]) >> 20], 1u);
+    v[i] = t < L ? s[t] : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < TK_ITEMS; ++i) {
+    const int t = base + i * TK_THREADS + threadIdx.x;
+    if (t < L) atomicAdd(&h[order_key(v[i]) >> 20], 1u);
   }
   __syncthreads();
   uint32_t* g = hist + (size_t)b * TK_BINS;
@@ -98,14 +106,15 @@ __global__ void __launch_bounds__(1024) tk_find(const uint32_t* __restrict__ his
   }
 }
 
-__device__ __forceinline__ void emit(int32_t* out_b, int* st, int t) {
-  const int p = atomicAdd(&st[ST_OUT], 1);
-  out_b[p] = t;
+// selected position t: count it and set its bit in the sequence's bitmap
+__device__ __forceinline__ void emit(uint32_t* bm_b, int* st, int t) {
+  atomicAdd(&st[ST_OUT], 1);
+  atomicOr(&bm_b[t >> 5], 1u << (t & 31));
 }
 
 __global__ void __launch_bounds__(TK_THREADS) tk_pass2(const float* __restrict__ scores, int Lmax,
                                                        int* __restrict__ state, uint32_t* __restrict__ hist2,
-                                                       int32_t* __restrict__ out, int k) {
+                                                       uint32_t* __restrict__ bm, int W) {
   __shared__ uint32_t h[TK_BINS];
   const int b = blockIdx.y;
   int* st = state + b * ST_WORDS;
@@ -115,13 +124,20 @@ __global__ void __launch_bounds__(TK_THREADS) tk_pass2(const float* __restrict__
   __syncthreads();
   const int base = blockIdx.x * TK_THREADS * TK_ITEMS;
   const float* s = scores + (size_t)b * Lmax;
-  int32_t* ob = out + (size_t)b * k;
+  uint32_t* bmb = bm + (size_t)b * W;
+  float v[TK_ITEMS];
+#pragma unroll
+  for (int i = 0; i < TK_ITEMS; ++i) {
+    const int t = base + i * TK_THREADS + threadIdx.x;
+    v[i] = t < L ? s[t] : 0.f;
+  }
+#pragma unroll
   for (int i = 0; i < TK_ITEMS; ++i) {
     const int t = base + i * TK_THREADS + threadIdx.x;
     if (t < L) {
-      const uint32_t key = order_key(s[t]);
+      const uint32_t key = order_key(v[i]);
       const int hi = (int)(key >> 20);
-      if (hi > bin1) emit(ob, st, t);
+      if (hi > bin1) emit(bmb, st, t);
       else if (hi == bin1) atomicAdd(&h[(key >> 8) & 0xFFFu], 1u);
     }
   }
@@ -134,7 +150,7 @@ __global__ void __launch_bounds__(TK_THREADS) tk_pass2(const float* __restrict__
 
 __global__ void __launch_bounds__(TK_THREADS) tk_pass3(const float* __restrict__ scores, int Lmax,
                                                        int* __restrict__ state, unsigned long long* __restrict__ cand,
-                                                       int cap, int32_t* __restrict__ out, int k) {
+                                                       int cap, uint32_t* __restrict__ bm, int W) {
   const int b = blockIdx.y;
   int* st = state + b * ST_WORDS;
   const int bin1 = st[ST_BIN1];
@@ -143,15 +159,22 @@ __global__ void __launch_bounds__(TK_THREADS) tk_pass3(const float* __restrict__
   const int L = st[ST_L];
   const int base = blockIdx.x * TK_THREADS * TK_ITEMS;
   const float* s = scores + (size_t)b * Lmax;
-  int32_t* ob = out + (size_t)b * k;
+  uint32_t* bmb = bm + (size_t)b * W;
   unsigned long long* cb = cand + (size_t)b * cap;
+  float v[TK_ITEMS];
+#pragma unroll
+  for (int i = 0; i < TK_ITEMS; ++i) {
+    const int t = base + i * TK_THREADS + threadIdx.x;
+    v[i] = t < L ? s[t] : 0.f;
+  }
+#pragma unroll
   for (int i = 0; i < TK_ITEMS; ++i) {
     const int t = base + i * TK_THREADS + threadIdx.x;
     if (t < L) {
-      const uint32_t key = order_key(s[t]);
+      const uint32_t key = order_key(v[i]);
       if ((int)(key >> 20) != bin1) continue;
       const int mid = (int)((key >> 8) & 0xFFFu);
-      if (mid > bin2) emit(ob, st, t);
+      if (mid > bin2) emit(bmb, st, t);
       else if (mid == bin2) {
         const int c = atomicAdd(&st[ST_NCAND], 1);
         if (c < cap) cb[c] = ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
@@ -180,14 +203,14 @@ __device__ void bitonic_desc(unsigned long long* v, int n) {
 __global__ void __launch_bounds__(1024) tk_finish(const float* __restrict__ scores, int Lmax,
                                                   int* __restrict__ state,
                                                   const unsigned long long* __restrict__ cand, int cap,
-                                                  int32_t* __restrict__ out, int k) {
+                                                  uint32_t* __restrict__ bm, int W) {
   extern __shared__ unsigned long long sv[];
   const int b = blockIdx.x;
   int* st = state + b * ST_WORDS;
   const int bin1 = st[ST_BIN1];
   if (bin1 < 0) return;
   const int need = st[ST_NEED2];
-  int32_t* ob = out + (size_t)b * k;
+  uint32_t* bmb = bm + (size_t)b * W;
   if (!st[ST_OVF]) {
     const int n = min(st[ST_NCAND], cap);
     int n2 = 1;
@@ -195,11 +218,10 @@ __global__ void __launch_bounds__(1024) tk_finish(const float* __restrict__ scor
     for (int i = threadIdx.x; i < n2; i += blockDim.x) sv[i] = i < n ? cand[(size_t)b * cap + i] : 0ull;
     __syncthreads();
     bitonic_desc(sv, n2);
-    const int base = st[ST_OUT];
-    for (int i = threadIdx.x; i < need; i += blockDim.x)
-      ob[base + i] = (int)(0xFFFFFFFFu - (uint32_t)(sv[i] & 0xFFFFFFFFull));
-    __syncthreads();
-    if (threadIdx.x == 0) st[ST_OUT] = base + need;
+    for (int i = threadIdx.x; i < need; i += blockDim.x) {
+      const int t = (int)(0xFFFFFFFFu - (uint32_t)(sv[i] & 0xFFFFFFFFull));
+      atomicOr(&bmb[t >> 5], 1u << (t & 31));
+    }
     return;
   }
   // Overflow: many scores share the boundary's top 24 bits.  Ordered scan of the
@@ -228,10 +250,6 @@ __global__ void __launch_bounds__(1024) tk_finish(const float* __restrict__ scor
   }
   __syncthreads();
   const uint32_t T = (prefix << 8) | (uint32_t)sel_bin;
-  const int base = st[ST_OUT];
-  __shared__ int emitted;
-  if (threadIdx.x == 0) emitted = 0;
-  __syncthreads();
   for (int t0 = 0; t0 < L; t0 += blockDim.x) {
     const int t = t0 + threadIdx.x;
     uint32_t key = 0u;
@@ -241,7 +259,7 @@ __global__ void __launch_bounds__(1024) tk_finish(const float* __restrict__ scor
       above = ((key >> 8) == prefix) && (key > T);
       tie = (key == T);
     }
-    if (above) { const int p = atomicAdd(&emitted, 1); ob[base + p] = t; }
+    if (above) atomicOr(&bmb[t >> 5], 1u << (t & 31));
     // rank of this tie among the ties of this block, in position order
     const unsigned bal = __ballot_sync(0xffffffffu, tie);
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -250,36 +268,74 @@ __global__ void __launch_bounds__(1024) tk_finish(const float* __restrict__ scor
     int before = 0;
     for (int i = 0; i < wid; ++i) before += (int)wcnt[i];
     const int rank = taken + before + __popc(bal & ((1u << lane) - 1u));
-    if (tie && rank < sel_need) { const int p = atomicAdd(&emitted, 1); ob[base + p] = t; }
+    if (tie && rank < sel_need) atomicOr(&bmb[t >> 5], 1u << (t & 31));
     __syncthreads();
     if (threadIdx.x == 0) { int tot = 0; for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += (int)wcnt[i]; taken += tot; }
     __syncthreads();
   }
-  if (threadIdx.x == 0) st[ST_OUT] = base + emitted;
 }
 
-// sort the emitted positions ascending, pad with -1
-__global__ void __launch_bounds__(1024) tk_sort_out(int* __restrict__ state, int32_t* __restrict__ out, int k) {
-  extern __shared__ unsigned long long sv[];
+// The selected positions of sequence b, ascending, from its bitmap (one block of
+// 1024 threads per sequence: each thread counts the bits of a contiguous run of
+// words, a block scan gives its output offset); the rest of the row is -1.
+__global__ void __launch_bounds__(1024) tk_extract(const uint32_t* __restrict__ bm, int W, int32_t* __restrict__ out,
+                                                   int k) {
+  __shared__ int wsum[32];
   const int b = blockIdx.x;
-  const int n = min(state[b * ST_WORDS + ST_OUT], k);
-  int n2 = 1;
-  while (n2 < k) n2 <<= 1;
+  const uint32_t* bmb = bm + (size_t)b * W;
   int32_t* ob = out + (size_t)b * k;
-  // descending sort of (~pos) == ascending positions; padding sorts last
-  for (int i = threadIdx.x; i < n2; i += blockDim.x)
-    sv[i] = i < n ? (unsigned long long)(0xFFFFFFFFu - (uint32_t)ob[i]) : 0ull;
+  // thread i owns words [i*per, i*per + per); up to 16 of them are held in registers
+  const int per = (W + 1023) / 1024;
+  const int w0 = threadIdx.x * per, w1 = min(W, w0 + per);
+  constexpr int R = 16;
+  uint32_t x[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) x[i] = (i < per && w0 + i < w1) ? bmb[w0 + i] : 0u;
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) cnt += __popc(x[i]);
+  for (int w = w0 + R; w < w1; ++w) cnt += __popc(bmb[w]);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[wid] = incl;
   __syncthreads();
-  bitonic_desc(sv, n2);
-  for (int i = threadIdx.x; i < k; i += blockDim.x)
-    ob[i] = i < n ? (int)(0xFFFFFFFFu - (uint32_t)sv[i]) : -1;
+  int pos = incl - cnt;
+  for (int i = 0; i < wid; ++i) pos += wsum[i];
+  int total = 0;
+  for (int i = 0; i < 32; ++i) total += wsum[i];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    uint32_t y = x[i];
+    while (y) {
+      const int bit = __ffs(y) - 1;
+      if (pos < k) ob[pos] = 32 * (w0 + i) + bit;
+      ++pos;
+      y &= y - 1;
+    }
+  }
+  for (int w = w0 + R; w < w1; ++w) {
+    uint32_t y = bmb[w];
+    while (y) {
+      const int bit = __ffs(y) - 1;
+      if (pos < k) ob[pos] = 32 * w + bit;
+      ++pos;
+      y &= y - 1;
+    }
+  }
+  for (int i = min(total, k) + threadIdx.x; i < k; i += 1024) ob[i] = -1;
 }
 
 }  // namespace pkv
 
-size_t pkv_topk_ws_bytes(int B, int k) {
+size_t pkv_topk_ws_bytes(int B, int k, int Lmax) {
   (void)k;
-  return (size_t)B * (2 * pkv::TK_BINS * 4 + pkv::ST_WORDS * 4 + PKV_TOPK_CAND * 8) + 256;
+  const size_t W = ((size_t)Lmax + 31) / 32;
+  return (size_t)B * (2 * pkv::TK_BINS * 4 + pkv::ST_WORDS * 4 + W * 4 + PKV_TOPK_CAND * 8) + 512;
 }
 
 cudaError_t pkv_launch_topk(const float* scores, int Lmax, const int32_t* seq_len, int B, int k,
@@ -289,20 +345,20 @@ cudaError_t pkv_launch_topk(const float* scores, int Lmax, const int32_t* seq_le
   uint32_t* hist1 = (uint32_t*)p;  p += (size_t)B * TK_BINS * 4;
   uint32_t* hist2 = (uint32_t*)p;  p += (size_t)B * TK_BINS * 4;
   int* state = (int*)p;            p += (size_t)B * ST_WORDS * 4;
+  const int W = (Lmax + 31) / 32;
+  uint32_t* bm = (uint32_t*)p;     p += (size_t)B * W * 4;
   p = (uint8_t*)(((uintptr_t)p + 15) & ~(uintptr_t)15);
   unsigned long long* cand = (unsigned long long*)p;
-  cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)B * (2 * TK_BINS + ST_WORDS) * 4, st);
+  cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)B * (2 * TK_BINS + ST_WORDS + W) * 4, st);
   if (e != cudaSuccess) return e;
   const int chunks = (Lmax + TK_THREADS * TK_ITEMS - 1) / (TK_THREADS * TK_ITEMS);
   dim3 grid(chunks > 0 ? chunks : 1, B);
-  int n2 = 1;
-  while (n2 < k) n2 <<= 1;
   tk_pass1<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, seq_len, hist1);
   tk_find<<<B, 1024, 0, st>>>(hist1, state, seq_len, Lmax, k, 1);
-  tk_pass2<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, state, hist2, out, k);
+  tk_pass2<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, state, hist2, bm, W);
   tk_find<<<B, 1024, 0, st>>>(hist2, state, seq_len, Lmax, k, 2);
-  tk_pass3<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, state, cand, PKV_TOPK_CAND, out, k);
-  tk_finish<<<B, 1024, PKV_TOPK_CAND * 8, st>>>(scores, Lmax, state, cand, PKV_TOPK_CAND, out, k);
-  tk_sort_out<<<B, 1024, (size_t)n2 * 8, st>>>(state, out, k);
+  tk_pass3<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, state, cand, PKV_TOPK_CAND, bm, W);
+  tk_finish<<<B, 1024, PKV_TOPK_CAND * 8, st>>>(scores, Lmax, state, cand, PKV_TOPK_CAND, bm, W);
+  tk_extract<<<B, 1024, 0, st>>>(bm, W, out, k);
   return cudaGetLastError();
 }
