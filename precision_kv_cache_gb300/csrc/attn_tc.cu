@@ -32,6 +32,7 @@
 //     O and write the partial result.
 // Every wait is bounded; on a timeout the CTA sets the error word, stops all
 // roles, drains its own copies / MMAs and frees its TMEM before returning.
+#include <cstddef>
 #include "attn_tc.h"
 #include "launch.h"
 #include "tc_ptx.cuh"
@@ -94,8 +95,10 @@ struct Shared {
   alignas(16) float m[NH];     // running max per head (log2 units)
   float alpha[NH];             // rescale factor of the current tile
   float red[4][NH];            // cross-warp reductions
-  uint32_t vsc[8][64];         // per V warp: f16x2 block-scale pairs of its current chunk (2 blocks x 32)
+  alignas(16) uint32_t vsc[8][64];   // per V warp: f16x2 block-scale pairs of its current chunk (2 blocks x 32)
 };
+static_assert(offsetof(Shared, m) % 16 == 0 && offsetof(Shared, alpha) % 16 == 0 && offsetof(Shared, vsc) % 16 == 0,
+              "16-byte shared-memory vector accesses");
 
 // ---------------------------------------------------------------- schedule
 struct Sched {
