@@ -134,6 +134,15 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 (= f16) tensor peak: the measured sustained figure (a long kernel), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured (bf16 dense, sustained)"
+    except Exception:
+        return 1700.0, "fallback (bf16 dense, sustained)"
+
+
 def committed_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu capture, if taken on the current kernel source."""
     try:
@@ -330,6 +339,22 @@ def run_gpu(args, rank, world, pool):
     gbs = step_bytes / (ms_step * 1e-3) / 1e9 * world
     peak, peak_kind = measured_peak()
     achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
+    roofline = {"kernel": "attention (global + window segments)", "bound": "hbm",
+                "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "bytes_per_launch": int(attn_bytes), "launch_ms": round(kern_ms, 5),
+                "traffic": committed_traffic("attention", name)}
+    if wl.replay:
+        # bounded replay is a dense contraction: QK^T and P.V, 2 flops per multiply-add,
+        # for every (replayed row, head, entry it attends) = 4*H*d flops per (row, entry)
+        entries = sum(128 * (int(wl.prefix_len[b]) - 128) + 128 * 129 // 2 for b in range(B))
+        flops = 4.0 * H * d * entries
+        tpeak, tkind = tensor_peak()
+        tf = flops / (kern_ms * 1e-3) / 1e12
+        roofline = {"kernel": "attention (replay)", "bound": "tensor", "achieved": round(tf, 1), "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": round(tf / tpeak, 4), "peak_kind": tkind,
+                    "flops_per_launch": flops, "launch_ms": round(kern_ms, 5), "traffic": None,
+                    "hbm_gbs": round(achieved, 2)}
     launches_per_step = (n1 - n0) / args.steps
 
     # ---- end to end through the public API with host buffers
@@ -381,11 +406,7 @@ def run_gpu(args, rank, world, pool):
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2), "hbm_peak_kind": peak_kind,
         "pct_of_8TBps_nominal": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "seq_per_s": round(B * world / (ms_step * 1e-3), 1),
-        "roofline": {"kernel": "attention (global + window segments)", "bound": "hbm",
-                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "bytes_per_launch": int(attn_bytes), "launch_ms": round(kern_ms, 5),
-                     "traffic": committed_traffic("attention", name)},
+        "roofline": roofline,
         "clocks": clk, "gpu_launches": int(n1 - n0), "launches_per_step": launches_per_step,
         "setup_s": round(setup_s, 1),
     }
