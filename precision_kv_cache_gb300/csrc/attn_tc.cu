@@ -66,8 +66,8 @@ constexpr uint32_t COL_V = 160;        // V^T chunk slots: NVS x 32 columns (64 
 constexpr uint32_t COL_O = 256;        // O^T: 4 chunks x 64 columns
 static_assert(COL_K == COL_S + 64 && COL_V == COL_K + 32 * NKS && COL_O >= COL_V + 32 * NVS, "TMEM map");
 
-constexpr int NKR = 3;                 // K ring: page slots
-constexpr int NVR = 4;                 // V ring: page slots
+constexpr int NKR = 4;                 // K ring: page slots (a tile holds two for its whole duration)
+constexpr int NVR = 3;                 // V ring: page slots (released page by page)
 
 template <int D>
 struct Cfg {
