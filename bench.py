@@ -44,6 +44,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 WORKLOADS = {"c1": 1, "c2": 2, "c3": 3, "c4": 4}
+SWEEP = {f"s{L // 1024}k": L for L in W.LONG_CONTEXT}     # long-context decode sweep (--sweep)
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
@@ -67,8 +68,15 @@ _WL = {}
 
 def _wl_cache(name):
     if name not in _WL:
-        _WL[name] = W.config(WORKLOADS[name])
+        _WL[name] = W.long_context(SWEEP[name]) if name in SWEEP else W.config(WORKLOADS[name])
     return _WL[name]
+
+
+def workload_desc(name):
+    if name in SWEEP:
+        wl = _wl_cache(name)
+        return f"long-context decode sweep: batch {wl.B}, 64 heads, d=512, {SWEEP[name]} global tokens each + window"
+    return W.CONFIGS[WORKLOADS[name]]
 
 
 def tensor_scales():
@@ -400,7 +408,7 @@ def run_gpu(args, rank, world, pool):
                   else "f32 CUDA-core FMA"),
         "attention_path": {1: "cuda-core split-K", 2: "tcgen05 tensor-core"}.get(ctx.pkv_attn_path(), "none"),
         "data": "synthetic (seeded N(0,1), 2% channels x8, bf16 Q; no trained weights)",
-        "config": {"workload": W.CONFIGS[WORKLOADS[name]], "name": wl.name, "batch": B, "heads": H, "d": d,
+        "config": {"workload": workload_desc(name), "name": wl.name, "batch": B, "heads": H, "d": d,
                    "tokens_read": int(tokens), "needed_bytes_per_step": int(step_bytes),
                    "l2": "working set > 129 MB L2; no flush between steps"},
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2), "hbm_peak_kind": peak_kind,
@@ -505,7 +513,7 @@ def run_reference(args):
             "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": W.CONFIGS[WORKLOADS[name]], "name": wl.name,
+            "config": {"workload": workload_desc(name), "name": wl.name,
                        "sample": f"each step: the first <=8192 global tokens + window of one of the first {nprep} "
                                  f"sequences (dequantize + float64 decode)"},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
@@ -520,7 +528,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(SWEEP), default="c2")
+    ap.add_argument("--sweep", action="store_true",
+                    help="long-context decode sweep (32K-512K tokens, >= 1 GiB of KV per step): one line per length")
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-region", action="store_true",
@@ -547,6 +557,14 @@ def main():
             import torch.distributed as dist
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
             dist.init_process_group("nccl")
+        if args.sweep:
+            for name in sorted(SWEEP, key=SWEEP.get):
+                args.workload = name
+                res, wl = run_gpu(args, rank, world, pool)
+                if rank == 0:
+                    print(json.dumps(res), flush=True)
+                _WL.pop(name, None)
+            return
         res, wl = run_gpu(args, rank, world, pool)
     finally:
         if pool:

@@ -245,6 +245,16 @@ def config(i: int, seed: int = 0) -> Workload:
     raise ValueError(i)
 
 
+# Long-context decode sweep: the dense 64-head d=512 decode shape at one length
+# L, with the batch sized so that the NVFP4 K/V read per step is at least 1 GiB.
+LONG_CONTEXT = (32768, 65536, 131072, 262144, 524288)
+
+
+def long_context(L: int, seed: int = 0) -> Workload:
+    B = -(-(1 << 30) // (L * 576))
+    return make_dense(f"sweep_decode_{L // 1024}k", seed, B, 64, 512, [L] * B, perm_seed_key=L)
+
+
 CONFIGS = {
     0: "batch 1, 8 heads, d=128, 1024 global tokens + 128-entry FP8 window",
     1: "batch 32, 64 heads, d=512, 8192 global tokens each + window",
