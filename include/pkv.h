@@ -111,7 +111,7 @@ typedef struct {
 } pkv_window;
 
 /* Operations for pkv_workspace_bytes. */
-enum { PKV_OP_DECODE = 1, PKV_OP_SCORE_TOPK = 2, PKV_OP_REPLAY = 3, PKV_OP_DECODE_SPARSE = 4 };
+enum { PKV_OP_DECODE = 1, PKV_OP_SCORE_TOPK = 2, PKV_OP_REPLAY = 3, PKV_OP_DECODE_SPARSE = 4, PKV_OP_SCORE_CAND = 5 };
 
 /* Create a context on CUDA device `device` (made current for the call).
  * Allocates the context's 4-byte device error word.  Returns
@@ -123,6 +123,7 @@ void pkv_destroy(pkv_ctx* ctx);
  * max_len: PKV_OP_DECODE - max_pages*64 of the page table;
  * PKV_OP_REPLAY - max_pages*64 (batch = sequences, 128 queries each);
  * PKV_OP_SCORE_TOPK - max_pages*64 (the score buffer and radix-select state);
+ * PKV_OP_SCORE_CAND - n_cand, the candidates per sequence;
  * PKV_OP_DECODE_SPARSE - k, the number of selected positions per sequence
  * (decode over sel_idx: the selected tokens are first gathered into compact
  * pages inside the workspace). */
@@ -164,6 +165,22 @@ pkv_status pkv_score_topk(pkv_ctx* ctx, const uint8_t* q_idx, float tq, const fl
                           int max_pages, const int32_t* seq_len, int B, int k,
                           int32_t* out_idx, float* out_score, void* ws, size_t ws_bytes,
                           void* stream);
+
+/* The same scoring and top-k restricted to a candidate list per sequence (the
+ * fixed candidate set of "Logits MQA creux", vLLM blog "Kernels"): only the
+ * positions cand[b][0..n_cand) are scored.  cand int32 [B][n_cand], each row
+ * strictly ascending and -1 padded at the end; every listed position must have
+ * its page in page_table (else the error word is set and the position scores
+ * as a zero key).  Writes the k highest-scoring candidates' positions to
+ * out_idx int32 [B][k] in ascending order (ties: lower position first), -1
+ * padded when a row has fewer than k candidates, and the candidates' scores to
+ * out_score float32 [B][n_cand] (entry i = candidate i; unspecified after the
+ * last valid one) when not NULL.  1 <= k <= 4096, 1 <= n_cand <= 2^30.
+ * Workspace: pkv_workspace_bytes(ctx, PKV_OP_SCORE_CAND, B, n_cand). */
+pkv_status pkv_score_topk_cand(pkv_ctx* ctx, const uint8_t* q_idx, float tq, const float* w,
+                               const pkv_idx_cache* icache, const int32_t* page_table, int max_pages,
+                               const int32_t* cand, int n_cand, int B, int k, int32_t* out_idx,
+                               float* out_score, void* ws, size_t ws_bytes, void* stream);
 
 /* Decode attention (flash-decoding split along the sequence + LSE merge).
  * For sequence b, query head h (q bf16 [B][n_heads][d]):

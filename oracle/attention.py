@@ -96,6 +96,17 @@ def topk(scores, k):
     return out
 
 
+def topk_cand(cand_scores, cand, k):
+    """Top-k restricted to a candidate list ("Logits MQA creux", vLLM blog
+    "Kernels": only a fixed candidate set is scored): ``cand`` holds ascending
+    positions, ``cand_scores[i]`` the score of position cand[i].  Returns the
+    selected positions in ascending order (ties: lower position first, which is
+    the lower candidate index because the list is ascending), -1 padded."""
+    cand = np.asarray(cand, np.int64)
+    sel = topk(cand_scores, k)
+    return np.where(sel >= 0, cand[np.maximum(sel, 0)], -1)
+
+
 def topk_matches(gpu_idx, scores, k, rel=1e-5):
     """Set check of a top-k answer against float64 scores: exactly the oracle's
     set, except members whose score lies within ``rel`` * |S_k| of the k-th

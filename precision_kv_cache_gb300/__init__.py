@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, "libpkv.so")
 PAGE = 64
 WINDOW = 128
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_BAD_PAGE, ERR_TIMEOUT, ERR_WORKSPACE = range(7)
-OP_DECODE, OP_SCORE_TOPK, OP_REPLAY, OP_DECODE_SPARSE = 1, 2, 3, 4
+OP_DECODE, OP_SCORE_TOPK, OP_REPLAY, OP_DECODE_SPARSE, OP_SCORE_CAND = 1, 2, 3, 4, 5
 
 
 class PkvError(RuntimeError):
@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             "pkv_append_index": (i, [vp, vp, vp, vp, i, ctypes.POINTER(_IdxCache), vp, i, vp]),
             "pkv_quantize_fp8": (i, [vp, sz, f, vp, vp]),
             "pkv_score_topk": (i, [vp, vp, f, vp, ctypes.POINTER(_IdxCache), vp, i, vp, i, i, vp, vp, vp, sz, vp]),
+            "pkv_score_topk_cand": (i, [vp, vp, f, vp, ctypes.POINTER(_IdxCache), vp, i, vp, i, i, i, vp, vp, vp, sz,
+                                        vp]),
             "pkv_decode_attn": (i, [vp, vp, ctypes.POINTER(_KVCache), vp, i, vp, i, vp, i,
                                     ctypes.POINTER(_Window), f, vp, vp, vp, sz, vp]),
             "pkv_replay_attn": (i, [vp, vp, ctypes.POINTER(_KVCache), vp, i, vp, i, ctypes.POINTER(_Window),
@@ -213,6 +215,16 @@ class Context:
         _check(lib().pkv_score_topk(self.h, _p(q_idx), tq, _p(w), ctypes.byref(c), _p(page_table),
                                     page_table.shape[1], _p(seq_len), B, k, _p(out_idx), _p(out_score),
                                     _p(ws), ws.numel(), _stream(stream)), "pkv_score_topk")
+
+    def pkv_score_topk_cand(self, q_idx, tq, w, icache: IdxCache, page_table, cand, k, out_idx, out_score=None,
+                            ws=None, stream=None):
+        B, n = cand.shape
+        if ws is None:
+            ws = self.workspace(OP_SCORE_CAND, B, n)
+        c = icache._c()
+        _check(lib().pkv_score_topk_cand(self.h, _p(q_idx), tq, _p(w), ctypes.byref(c), _p(page_table),
+                                         page_table.shape[1], _p(cand), n, B, k, _p(out_idx), _p(out_score),
+                                         _p(ws), ws.numel(), _stream(stream)), "pkv_score_topk_cand")
 
     def pkv_decode_attn(self, q, cache: KVCache, page_table, seq_len, win: Window, scale, out, out_lse=None,
                         ws=None, sel_idx=None, stream=None):

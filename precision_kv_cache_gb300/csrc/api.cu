@@ -145,6 +145,9 @@ size_t pkv_workspace_bytes(const pkv_ctx* c, int op, int batch, int max_len) {
       const int kp = (max_len + PKV_PAGE - 1) / PKV_PAGE * PKV_PAGE;
       return pkv_gather_ws_bytes(c->cfg.d, batch, max_len) + 256 + attn_ws_bytes(c, batch, kp + PKV_WINDOW);
     }
+    case PKV_OP_SCORE_CAND:
+      return pkv_gather_index_ws_bytes(batch, max_len) + 256 + (size_t)batch * (size_t)max_len * 4 + 256 +
+             pkv_score_tc_ws_bytes(batch, c->num_sms) + pkv_topk_ws_bytes(batch, PKV_TOPK_MAX_K, max_len) + 256;
     case PKV_OP_SCORE_TOPK:
       return (size_t)batch * (size_t)max_len * 4 + 256 + pkv_score_tc_ws_bytes(batch, c->num_sms) +
              pkv_topk_ws_bytes(batch, PKV_TOPK_MAX_K, max_len) + 256;
@@ -213,6 +216,46 @@ pkv_status pkv_score_topk(pkv_ctx* c, const uint8_t* q_idx, float tq, const floa
                                       scores, Lmax, plan, c->num_sms, c->d_err, st);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return cuda_status(pkv_launch_topk(scores, Lmax, seq_len, B, k, out_idx, p, st));
+}
+
+pkv_status pkv_score_topk_cand(pkv_ctx* c, const uint8_t* q_idx, float tq, const float* w, const pkv_idx_cache* ic,
+                               const int32_t* page_table, int max_pages, const int32_t* cand, int n_cand, int B,
+                               int k, int32_t* out_idx, float* out_score, void* ws, size_t ws_bytes, void* stream) {
+  if (!c || B <= 0 || max_pages <= 0 || k < 1 || k > PKV_TOPK_MAX_K || n_cand < 1 || n_cand > (1 << 30))
+    return PKV_ERR_INVALID_ARG;
+  if (!q_idx || !w || !ic || !ic->data || !ic->scale || !page_table || !cand || !out_idx) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(ic->data) || !aligned16(ic->scale) || ic->num_pages <= 0 || !(ic->ts > 0.f) ||
+      !(tq > 0.f) || !(tq < INFINITY) || !(ic->ts < INFINITY))
+    return PKV_ERR_INVALID_ARG;
+  if ((long long)max_pages * PKV_PAGE > (1LL << 30)) return PKV_ERR_UNSUPPORTED;
+  const size_t need = pkv_workspace_bytes(c, PKV_OP_SCORE_CAND, B, n_cand);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return PKV_ERR_WORKSPACE;
+  DeviceGuard g(c->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* p = (uint8_t*)ws;
+  // candidate keys gathered into compact pages, one compact sequence per row
+  pkv_idx_cache cc;
+  int32_t *cpt = nullptr, *cnt = nullptr;
+  int npb = 0;
+  cudaError_t e = pkv_launch_gather_index(*ic, page_table, max_pages, cand, B, n_cand, p, &cc, &cpt, &cnt, &npb,
+                                          c->d_err, st);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  p += pkv_gather_index_ws_bytes(B, n_cand);
+  p = (uint8_t*)(((uintptr_t)p + 255) & ~(uintptr_t)255);
+  float* scores = out_score;
+  if (!scores) scores = (float*)p;
+  p += (size_t)B * n_cand * 4;
+  p = (uint8_t*)(((uintptr_t)p + 255) & ~(uintptr_t)255);
+  void* plan = p;
+  p += pkv_score_tc_ws_bytes(B, c->num_sms);
+  c->launches += 2 + 2 + PKV_TOPK_LAUNCHES + 1;
+  e = pkv_launch_score_tc(q_idx, tq, w, cc, cpt, npb, cnt, B, c->cfg.n_index_heads, scores, n_cand, plan,
+                          c->num_sms, c->d_err, st);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  // top-k over candidate indices (ascending candidates: lower index = lower position), then to positions
+  e = pkv_launch_topk(scores, n_cand, cnt, B, k, out_idx, p, st);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  return cuda_status(pkv_launch_map_cand(out_idx, cand, B, n_cand, k, st));
 }
 
 static pkv_status run_attention(pkv_ctx* c, pkv::AttnArgs& a, int max_entries, float* out, float* out_lse,

@@ -138,3 +138,103 @@ cudaError_t pkv_launch_gather(int d, const pkv_kv_cache& src, const int32_t* pag
   }
   return cudaGetLastError();
 }
+
+// ---------------------------------------------------------------- candidate index keys
+// Candidate-list scoring ("Logits MQA creux": score a fixed candidate set per
+// sequence): the index keys of the candidates cand[b][0..n) are gathered, in
+// order, into compact pages b*npb .. b*npb+npb-1 (npb = ceil(n/64)) of an index
+// pool with the same byte layout (128-channel K-layout: 64 code bytes per token,
+// 16-byte pieces swizzled by slot mod 4; scales [1][64][8]).  cnt[b] = number
+// of valid candidates (the list is ascending and -1 padded at the end).
+namespace pkv {
+
+__global__ void __launch_bounds__(256) gather_index_kernel(pkv_idx_cache src, const int32_t* __restrict__ page_table,
+                                                           int max_pages, const int32_t* __restrict__ cand, int n,
+                                                           int npb, pkv_idx_cache dst, int32_t* __restrict__ cnt,
+                                                           int* err) {
+  constexpr int PD = PKV_PAGE * 64, PS = PKV_PAGE * 8;    // 128-channel index keys
+  __shared__ int spage[64], sslot[64];
+  const int page = blockIdx.x, b = page / npb, jp = page % npb;
+  const int tid = threadIdx.x;
+  if (tid < 64) {
+    const int i = jp * PKV_PAGE + tid;
+    int pg = -1, sl = 0;
+    if (i < n) {
+      const int t = cand[(size_t)b * n + i];
+      if (t >= 0) {
+        const int j = t >> 6;
+        const int p = j < max_pages ? page_table[(size_t)b * max_pages + j] : -1;
+        if (p >= 0 && p < src.num_pages) { pg = p; sl = t & 63; }
+        else report(err, PKV_DEVERR_BAD_PAGE);
+      }
+    }
+    spage[tid] = pg;
+    sslot[tid] = sl;
+  }
+  if (jp == 0 && tid == 64) {
+    int lo = 0, hi = n;                       // first index holding -1
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (cand[(size_t)b * n + mid] >= 0) lo = mid + 1; else hi = mid;
+    }
+    cnt[b] = lo;
+  }
+  __syncthreads();
+  // codes: thread = (token s, 16-byte piece c)
+  {
+    const int s = tid >> 2, c = tid & 3;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (spage[s] >= 0) {
+      const int ss = sslot[s];
+      v = *reinterpret_cast<const uint4*>(src.data + (size_t)spage[s] * PD + ss * 64 + 16 * (c ^ (ss & 3)));
+    }
+    *reinterpret_cast<uint4*>(dst.data + (size_t)page * PD + s * 64 + 16 * (c ^ (s & 3))) = v;
+  }
+  // scales: one 8-byte word per token
+  if (tid < 64) {
+    uint2 v = make_uint2(0u, 0u);
+    if (spage[tid] >= 0) v = *reinterpret_cast<const uint2*>(src.scale + (size_t)spage[tid] * PS + sslot[tid] * 8);
+    *reinterpret_cast<uint2*>(dst.scale + (size_t)page * PS + tid * 8) = v;
+  }
+}
+
+// out[b][i] (a candidate index, or -1) -> the candidate's position
+__global__ void map_cand_kernel(int32_t* __restrict__ out, const int32_t* __restrict__ cand, int B, int n, int k) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * k) return;
+  const int b = i / k, c = out[i];
+  out[i] = c >= 0 ? cand[(size_t)b * n + c] : -1;
+}
+
+}  // namespace pkv
+
+size_t pkv_gather_index_ws_bytes(int B, int n) {
+  const size_t npb = (size_t)(n + PKV_PAGE - 1) / PKV_PAGE;
+  const size_t pages = (size_t)B * npb;
+  return pages * (PKV_PAGE * 64 + PKV_PAGE * 8) + pages * 4 + (size_t)B * 4 + 4 * 256;
+}
+
+cudaError_t pkv_launch_gather_index(const pkv_idx_cache& src, const int32_t* page_table, int max_pages,
+                                    const int32_t* cand, int B, int n, void* ws, pkv_idx_cache* dst,
+                                    int32_t** dst_pt, int32_t** dst_cnt, int* npb_out, int* err, cudaStream_t st) {
+  const int npb = (n + PKV_PAGE - 1) / PKV_PAGE;
+  const size_t pages = (size_t)B * npb;
+  uint8_t* p = (uint8_t*)ws;
+  auto take = [&](size_t bytes) { uint8_t* r = p; p += (bytes + 255) / 256 * 256; return r; };
+  dst->data = take(pages * PKV_PAGE * 64);
+  dst->scale = take(pages * PKV_PAGE * 8);
+  dst->num_pages = (int)pages;
+  dst->ts = src.ts;
+  *dst_pt = (int32_t*)take(pages * 4);
+  *dst_cnt = (int32_t*)take((size_t)B * 4);
+  *npb_out = npb;
+  pkv::identity_table_kernel<<<(int)((pages + 255) / 256), 256, 0, st>>>(*dst_pt, B, npb);
+  pkv::gather_index_kernel<<<(int)pages, 256, 0, st>>>(src, page_table, max_pages, cand, n, npb, *dst, *dst_cnt, err);
+  return cudaGetLastError();
+}
+
+cudaError_t pkv_launch_map_cand(int32_t* out, const int32_t* cand, int B, int n, int k, cudaStream_t st) {
+  const int tot = B * k;
+  pkv::map_cand_kernel<<<(tot + 255) / 256, 256, 0, st>>>(out, cand, B, n, k);
+  return cudaGetLastError();
+}

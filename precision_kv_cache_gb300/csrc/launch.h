@@ -39,6 +39,12 @@ cudaError_t pkv_launch_gather(int d, const pkv_kv_cache& src, const int32_t* pag
                               const int32_t* sel, int B, int k, void* ws, pkv_kv_cache* dst, int32_t** dst_pt,
                               int32_t** dst_len, int* npb_out, int* err, cudaStream_t st);
 
+size_t pkv_gather_index_ws_bytes(int B, int n);
+cudaError_t pkv_launch_gather_index(const pkv_idx_cache& src, const int32_t* page_table, int max_pages,
+                                    const int32_t* cand, int B, int n, void* ws, pkv_idx_cache* dst,
+                                    int32_t** dst_pt, int32_t** dst_cnt, int* npb_out, int* err, cudaStream_t st);
+cudaError_t pkv_launch_map_cand(int32_t* out, const int32_t* cand, int B, int n, int k, cudaStream_t st);
+
 size_t pkv_score_tc_ws_bytes(int B, int num_sms);
 cudaError_t pkv_score_tc_init();
 cudaError_t pkv_launch_score_tc(const uint8_t* q_idx, float tq, const float* w, const pkv_idx_cache& ic,

@@ -256,3 +256,24 @@ def test_cache_fill_and_dequant_match_direct_quantization():
     assert (wl.page_table[0, :2] == wl.page_table[1, :2]).all()
     assert (wl.page_table[2, :2] == wl.page_table[3, :2]).all()
     assert wl.page_table[0, 0] != wl.page_table[2, 0]
+
+
+def test_topk_cand_all_positions_is_dense_topk():
+    """Candidate list = every position: the candidate top-k is the dense top-k."""
+    rng = np.random.default_rng(7)
+    s = rng.normal(size=300)
+    s[[5, 17, 200]] = s.max() + 1.0               # planted maxima
+    assert (A.topk_cand(s, np.arange(300), 40) == A.topk(s, 40)).all()
+
+
+def test_topk_cand_brute_force_small():
+    """Tiny cases against enumeration: positions of the k best candidates, ties to the lower position."""
+    rng = np.random.default_rng(8)
+    for _ in range(200):
+        n = int(rng.integers(1, 9))
+        cand = np.sort(rng.choice(50, size=n, replace=False))
+        sc = rng.integers(0, 4, size=n).astype(np.float64)      # many ties
+        k = int(rng.integers(1, 10))
+        best = sorted(range(n), key=lambda i: (-sc[i], cand[i]))[:k]
+        want = sorted(int(cand[i]) for i in best) + [-1] * (k - min(k, n))
+        assert list(A.topk_cand(sc, cand, k)) == want
