@@ -43,7 +43,8 @@ sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
 
-WORKLOADS = {"c1": 1, "c2": 2, "c3": 3, "c4": 4}
+WORKLOADS = {"c1": 1, "c2": 2, "c3": 3, "c4": 4, "c3c": 3}
+CAND_C3C = 16384                   # c3c: the sparse workload scoring a fixed candidate set per sequence
 SWEEP = {f"s{L // 1024}k": L for L in W.LONG_CONTEXT}     # long-context decode sweep (--sweep)
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
@@ -69,6 +70,8 @@ _WL = {}
 def _wl_cache(name):
     if name not in _WL:
         _WL[name] = W.long_context(SWEEP[name]) if name in SWEEP else W.config(WORKLOADS[name])
+        if name == "c3c":
+            _WL[name].n_cand = CAND_C3C
     return _WL[name]
 
 
@@ -76,6 +79,8 @@ def workload_desc(name):
     if name in SWEEP:
         wl = _wl_cache(name)
         return f"long-context decode sweep: batch {wl.B}, 64 heads, d=512, {SWEEP[name]} global tokens each + window"
+    if name == "c3c":
+        return W.CONFIGS[3] + f", scoring only a fixed {CAND_C3C}-position candidate set per sequence"
     return W.CONFIGS[WORKLOADS[name]]
 
 
@@ -275,7 +280,11 @@ def run_gpu(args, rank, world, pool):
         P.pkv_quantize_fp8(torch.from_numpy(qf).to(dev), tq, qidx)
         wts = torch.from_numpy(wl.index_w()).to(dev)
         sel = torch.empty(B, wl.topk, dtype=torch.int32, device=dev)
-        ws_s = ctx.workspace(P.OP_SCORE_TOPK, B, pt.shape[1] * 64)
+        if wl.n_cand:
+            cand = torch.from_numpy(wl.cand_lists(wl.n_cand)).to(dev)
+            ws_s = ctx.workspace(P.OP_SCORE_CAND, B, wl.n_cand)
+        else:
+            ws_s = ctx.workspace(P.OP_SCORE_TOPK, B, pt.shape[1] * 64)
         ws = ctx.workspace(P.OP_DECODE_SPARSE, B, wl.topk)
     elif not wl.replay:
         ws = ctx.workspace(P.OP_DECODE, B, pt.shape[1] * 64)
@@ -291,7 +300,10 @@ def run_gpu(args, rank, world, pool):
         if wl.append:
             ctx.pkv_append_kv(knew, vnew, bidx, pos, cache, pt)
         if wl.topk:
-            ctx.pkv_score_topk(qidx, tq, wts, ic, pt, seq_len, wl.topk, sel, ws=ws_s)
+            if wl.n_cand:
+                ctx.pkv_score_topk_cand(qidx, tq, wts, ic, pt, cand, wl.topk, sel, ws=ws_s)
+            else:
+                ctx.pkv_score_topk(qidx, tq, wts, ic, pt, seq_len, wl.topk, sel, ws=ws_s)
         if ev is not None:
             ctx.pkv_set_profile_events(ev[0], ev[1])
         if wl.replay:
@@ -339,7 +351,10 @@ def run_gpu(args, rank, world, pool):
     if wl.topk:
         cnt = (sel >= 0).sum(1).cpu().numpy()
         attn_bytes, tokens = needed_bytes(wl, sel_counts=cnt)
-        score_bytes = sum((int(L) + 63) // 64 for L in wl.seq_len) * 64 * (64 + 8) + B * 64 * 128 + B * 64 * 4 + B * wl.topk * 4
+        if wl.n_cand:     # candidate list + the candidates' index keys
+            score_bytes = B * wl.n_cand * (4 + 64 + 8) + B * 64 * 128 + B * 64 * 4 + B * wl.topk * 4
+        else:
+            score_bytes = sum((int(L) + 63) // 64 for L in wl.seq_len) * 64 * (64 + 8) + B * 64 * 128 + B * 64 * 4 + B * wl.topk * 4
         step_bytes = attn_bytes + score_bytes
     else:
         attn_bytes, tokens = needed_bytes(wl)

@@ -27,7 +27,7 @@ D_INDEX = 128      # index-key / index-query width
 H_INDEX = 64       # index heads
 
 # tensor ids of the substreams
-T_K, T_V, T_Q, T_KW, T_VW, T_IK, T_IQ, T_W, T_KNEW, T_VNEW, T_RQ, T_OUTL = range(1, 13)
+T_K, T_V, T_Q, T_KW, T_VW, T_IK, T_IQ, T_W, T_KNEW, T_VNEW, T_RQ, T_OUTL, T_CAND = range(1, 14)
 
 
 def rng(seed: int, *key: int) -> np.random.Generator:
@@ -88,6 +88,16 @@ class Workload:
     topk: int = 0                  # >0: sparse path (index scoring + top-k)
     replay: bool = False           # bounded replay: 128 queries at [H-128, H)
     prefix_len: Optional[np.ndarray] = None   # H per sequence (replay)
+    n_cand: int = 0                # >0: candidate-list scoring of that many positions per sequence
+
+    def cand_lists(self, n: int) -> np.ndarray:
+        """int32 [B][n]: min(n, L) distinct positions per sequence, ascending, -1 padded."""
+        out = np.full((self.B, n), -1, np.int32)
+        for b in range(self.B):
+            L = int(self.seq_len[b])
+            m = min(n, L)
+            out[b, :m] = np.sort(rng(self.seed, T_CAND, b).choice(L, size=m, replace=False))
+        return out
 
     @property
     def max_pages(self) -> int:
