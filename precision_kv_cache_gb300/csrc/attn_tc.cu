@@ -942,13 +942,22 @@ __global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups
   const int n = nseg_s, c_lo = cl_s;
   for (int d4 = threadIdx.x; d4 < D / 4; d4 += blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < n; ++i) {
-      const float w = wts[i];
-      if (w == 0.f) continue;
-      const size_t r = (size_t)(c_lo + i) + g;
-      const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + (r * H + h) * D) + d4);
-      acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+    // four segments per round, loads issued before use (segments are L2 round trips)
+    for (int i0 = 0; i0 < n; i0 += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u;
+        v[u] = (i < n && wts[i] != 0.f)
+                   ? __ldg(reinterpret_cast<const float4*>(part_o + (((size_t)(c_lo + i) + g) * H + h) * D) + d4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = i0 + u < n ? wts[i0 + u] : 0.f;
+        acc.x = fmaf(w, v[u].x, acc.x); acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z); acc.w = fmaf(w, v[u].w, acc.w);
+      }
     }
     reinterpret_cast<float4*>(out + ((size_t)g * H + h) * D)[d4] = acc;
   }
