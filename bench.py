@@ -147,6 +147,23 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(values, world, device):
+    """The element-wise maximum over all ranks (the slowest rank times the job); identity at world = 1."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_gbs(step_bytes_per_rank, ms_step_max, world):
+    """Whole-job throughput: every rank processes its own copy of the workload (weak
+    scaling, no data-path collective); the job takes as long as its slowest rank."""
+    return step_bytes_per_rank * world / (ms_step_max * 1e-3) / 1e9
+
+
 def tensor_peak():
     """Dense bf16 (= f16) tensor peak: the measured sustained figure (a long kernel), else the fallback."""
     try:
@@ -340,10 +357,7 @@ def run_gpu(args, rank, world, pool):
         dist.barrier()
     ms_step = t0e.elapsed_time(t1e) / args.steps
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    if world > 1:
-        t = torch.tensor([ms_step, kern_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, kern_ms = float(t[0]), float(t[1])
+    ms_step, kern_ms = max_over_ranks([ms_step, kern_ms], world, dev)
     if ctx.pkv_get_error() != P.OK:
         raise RuntimeError("device error in the timed region")
 
@@ -359,7 +373,7 @@ def run_gpu(args, rank, world, pool):
     else:
         attn_bytes, tokens = needed_bytes(wl)
         step_bytes = attn_bytes + (B * (2 * d * 4 + 8 + kv_token_bytes(d)) if wl.append else 0)
-    gbs = step_bytes / (ms_step * 1e-3) / 1e9 * world
+    gbs = job_gbs(step_bytes, ms_step, world)
     peak, peak_kind = measured_peak()
     achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
     roofline = {"kernel": "attention (global + window segments)", "bound": "hbm",
