@@ -358,6 +358,31 @@ def run_gpu(args, rank, world, pool):
     ms_step = t0e.elapsed_time(t1e) / args.steps
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     ms_step, kern_ms = max_over_ranks([ms_step, kern_ms], world, dev)
+    ms_eager = ms_step
+    graph = getattr(args, "graph", False)
+    if graph:
+        # the whole step captured once as a CUDA graph, then replayed: same kernels, no
+        # per-launch host work (kern_ms above stays the eager per-launch measurement)
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            g.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        ms_step = max_over_ranks([g0.elapsed_time(g1) / args.steps], world, dev)[0]
     if ctx.pkv_get_error() != P.OK:
         raise RuntimeError("device error in the timed region")
 
@@ -446,6 +471,7 @@ def run_gpu(args, rank, world, pool):
         "roofline": roofline,
         "clocks": clk, "gpu_launches": int(n1 - n0), "launches_per_step": launches_per_step,
         "setup_s": round(setup_s, 1),
+        "step_mode": "cuda graph replay" if graph else "eager", "ms_per_step_eager": round(ms_eager, 4),
     }
     if e2e:
         res["e2e"] = e2e
@@ -558,6 +584,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(SWEEP), default="c2")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="time eager calls instead of the step captured as one CUDA graph (the default)")
     ap.add_argument("--sweep", action="store_true",
                     help="long-context decode sweep (32K-512K tokens, >= 1 GiB of KV per step): one line per length")
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work for cpu_baseline")
