@@ -21,6 +21,13 @@ Each function is the plain definition, with no blocking, fusion or reordering:
   ([blog] "Kernels", "Logits MQA creux": late indexer layers pick their top-k
   positions from scores).
 * ``topk``: the k highest scores, ties to the lower index, returned ascending.
+* ``rope``: the rotary position embedding that the fused decode of [blog]
+  "MegaAttention avec KV compressé NVFP4" applies to the queries before QK and,
+  inverted, to the output after the attention.  The pages name the step but
+  not its layout; the reading taken: the last ``rope_dim`` channels of a head
+  rotate, as interleaved pairs (2i, 2i+1), each pair by its own angle, given
+  by a caller table of cosines and sines (the rotary cache a serving engine
+  keeps), the other channels pass through.
 """
 from __future__ import annotations
 
@@ -58,6 +65,26 @@ def replay(q, K, V, Kw, Vw, scale, rows=None):
         O[r], L[r] = segment(q[r], np.concatenate([K, Kw[:r + 1]], 0),
                              np.concatenate([V, Vw[:r + 1]], 0), scale)
     return O, L
+
+
+def rope(x, cos, sin, rope_dim: int, inverse: bool = False):
+    """x [..., d] (float64) with pair i = channels (d - rope_dim + 2i, d - rope_dim + 2i + 1)
+    turned by the angle whose cosine and sine are cos[i], sin[i] (by minus that
+    angle when ``inverse``):  y0 = x0 cos - x1 sin,  y1 = x0 sin + x1 cos.
+    cos / sin broadcast against x[..., rope_dim // 2]."""
+    y = np.array(x, dtype=np.float64, copy=True)
+    if rope_dim == 0:
+        return y
+    d = y.shape[-1]
+    c = np.asarray(cos, np.float64)
+    s = np.asarray(sin, np.float64)
+    if inverse:
+        s = -s
+    x0 = y[..., d - rope_dim::2].copy()
+    x1 = y[..., d - rope_dim + 1::2].copy()
+    y[..., d - rope_dim::2] = x0 * c - x1 * s
+    y[..., d - rope_dim + 1::2] = x0 * s + x1 * c
+    return y
 
 
 def merge(Oa, La, Ob, Lb):

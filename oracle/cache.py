@@ -123,3 +123,36 @@ def expected_decode(wl: W.Workload, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b: int, head
     if heads is not None:
         q = q[heads]
     return A.decode(q, K, V, Kw, Vw, scale)
+
+
+def expected_decode_fused(wl: W.Workload, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b: int, table, rope_dim: int,
+                          out_scale, pos=None, sel=None, heads=None, scale=None):
+    """Fused decode of sequence b ([blog] "MegaAttention avec KV compressé NVFP4":
+    query RoPE, attention, inverse RoPE on the output and FP8 conversion in one
+    pass): q' = rope(q, pos), (O, LSE) = attention of q' over global + window
+    (all L_b tokens, or the positions ``sel`` when given), O' = rope^-1(O, pos),
+    codes = E4M3(fp32(fp32(O') / out_scale)).  ``table`` float32 [max_pos][rope_dim]:
+    cosines then sines per position.  Returns (O' float64, LSE, codes uint8)."""
+    d = wl.d
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    p = int(wl.rope_pos()[b]) if pos is None else int(pos)
+    row = np.asarray(table[p], np.float64)
+    cos, sin = row[:rope_dim // 2], row[rope_dim // 2:rope_dim]
+    L = int(wl.seq_len[b])
+    if sel is None:
+        K = dequant_seq(wl, Kp, ts_k, b, L)
+        V = dequant_seq(wl, Vp, ts_v, b, L)
+    else:
+        idx = [int(t) for t in sel if t >= 0]
+        K = dequant_tokens(wl, Kp, ts_k, b, idx)
+        V = dequant_tokens(wl, Vp, ts_v, b, idx)
+    kw, vw = window_codes(wl, tw_k, tw_v, b)
+    n = int(wl.win_len[b])
+    Kw = F.fp8_dequantize(kw[:n], tw_k)
+    Vw = F.fp8_dequantize(vw[:n], tw_v)
+    q = F.bf16_to_f64(wl.q_bits_seq(b))
+    if heads is not None:
+        q = q[heads]
+    O, lse = A.decode(A.rope(q, cos, sin, rope_dim), K, V, Kw, Vw, scale)
+    Or = A.rope(O, cos, sin, rope_dim, inverse=True)
+    return Or, lse, F.fp8_quantize(Or, out_scale)

@@ -1,0 +1,167 @@
+"""Pins of the oracle's rotary embedding and fused decode (query RoPE, attention,
+inverse RoPE on the output, FP8 output; vLLM blog, "MegaAttention avec KV
+compressé NVFP4").
+
+The rotation is checked against basis vectors turned by a quarter turn,
+against complex multiplication by e^{i theta} (a second formulation), for
+inversion, length preservation and the relative-position property of angles
+linear in the position; the fused decode against the plain decode with an
+identity table and against a second route that turns the keys the other way
+instead of the query.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import attention as A
+from oracle import cache as C
+from oracle import formats as F
+
+
+def _complex_rotate(x, theta, rope_dim, sign=1.0):
+    """Second formulation: pair (x0, x1) as x0 + i x1, multiplied by e^{i sign theta}."""
+    x = np.array(x, np.float64)
+    d = x.shape[-1]
+    z = x[..., d - rope_dim::2] + 1j * x[..., d - rope_dim + 1::2]
+    z = z * np.exp(1j * sign * np.asarray(theta))
+    y = x.copy()
+    y[..., d - rope_dim::2] = z.real
+    y[..., d - rope_dim + 1::2] = z.imag
+    return y
+
+
+@pytest.mark.parametrize("d,rd", [(16, 8), (128, 64), (64, 64)])
+def test_quarter_turn_moves_basis_vectors(d, rd):
+    # cos = 0, sin = 1: e_{2i} -> e_{2i+1}, e_{2i+1} -> -e_{2i} inside the rotated part
+    cos, sin = np.zeros(rd // 2), np.ones(rd // 2)
+    for i in range(rd // 2):
+        c0 = d - rd + 2 * i
+        e = np.zeros(d); e[c0] = 1.0
+        y = A.rope(e, cos, sin, rd)
+        want = np.zeros(d); want[c0 + 1] = 1.0
+        assert np.array_equal(y, want)
+        e = np.zeros(d); e[c0 + 1] = 1.0
+        y = A.rope(e, cos, sin, rd)
+        want = np.zeros(d); want[c0] = -1.0
+        assert np.array_equal(y, want)
+        # the inverse turns the other way
+        y = A.rope(e, cos, sin, rd, inverse=True)
+        want = np.zeros(d); want[c0] = 1.0
+        assert np.array_equal(y, want)
+
+
+def test_channels_outside_the_rotated_part_pass_through():
+    r = np.random.default_rng(1)
+    x = r.standard_normal((3, 5, 96))
+    th = r.random(16) * 6.28
+    y = A.rope(x, np.cos(th), np.sin(th), 32)
+    assert np.array_equal(y[..., :64], x[..., :64])
+    assert np.array_equal(A.rope(x, [], [], 0), x)
+
+
+@pytest.mark.parametrize("inverse", [False, True])
+def test_matches_complex_multiplication(inverse):
+    r = np.random.default_rng(2)
+    x = r.standard_normal((7, 128))
+    th = r.random(32) * 2 * np.pi
+    y = A.rope(x, np.cos(th), np.sin(th), 64, inverse=inverse)
+    z = _complex_rotate(x, th, 64, sign=-1.0 if inverse else 1.0)
+    np.testing.assert_allclose(y, z, rtol=0, atol=1e-13)
+
+
+def test_inverse_undoes_and_lengths_are_kept():
+    r = np.random.default_rng(3)
+    x = r.standard_normal((4, 256))
+    th = r.random(32) * 2 * np.pi
+    c, s = np.cos(th), np.sin(th)
+    y = A.rope(x, c, s, 64)
+    np.testing.assert_allclose(A.rope(y, c, s, 64, inverse=True), x, rtol=0, atol=1e-13)
+    # every pair keeps its length
+    p0 = x[:, 192::2] ** 2 + x[:, 193::2] ** 2
+    p1 = y[:, 192::2] ** 2 + y[:, 193::2] ** 2
+    np.testing.assert_allclose(p1, p0, rtol=1e-13)
+
+
+def test_relative_position_property():
+    # angles linear in the position (theta_i(m) = m f_i): <R(m) q, R(n) k> = <R(m - n) q, k>
+    r = np.random.default_rng(4)
+    f = 10000.0 ** (-np.arange(32) / 32.0)
+    q, k = r.standard_normal(128), r.standard_normal(128)
+    rot = lambda x, m: A.rope(x, np.cos(m * f), np.sin(m * f), 64)
+    for m, n in [(5, 3), (100, 7), (1000, 999), (17, 40)]:
+        assert abs(rot(q, m) @ rot(k, n) - rot(q, m - n) @ k) < 1e-9
+
+
+def _small_workload():
+    wl = W.make_dense("fused_small", 3, 2, 4, 128, [300, 77])
+    ts, tw = C.tensor_scales(wl)
+    Kp, Vp = C.fill_pages(wl, ts, ts)
+    return wl, Kp, Vp, ts, ts, tw, tw
+
+
+def test_fused_with_identity_table_is_the_plain_decode():
+    wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v = _small_workload()
+    table = np.concatenate([np.ones((400, 32)), np.zeros((400, 32))], 1).astype(np.float32)
+    for b in range(wl.B):
+        O, L = C.expected_decode(wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b)
+        Of, Lf, codes = C.expected_decode_fused(wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b, table, 64, W.OUT_SCALE)
+        assert np.array_equal(Of, O) and np.array_equal(Lf, L)
+        assert np.array_equal(codes, F.fp8_quantize(O, W.OUT_SCALE))
+
+
+def test_fused_equals_keys_turned_the_other_way():
+    # <R q, k> = <q, R^-1 k>: attend with the unrotated query over inversely turned
+    # keys (complex formulation), then turn the output back
+    wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v = _small_workload()
+    table = W.rope_table(wl.seed, 400, 64)
+    for b in range(wl.B):
+        pos = int(wl.rope_pos()[b])
+        th = np.arctan2(table[pos, 32:].astype(np.float64), table[pos, :32].astype(np.float64))
+        rad = np.hypot(table[pos, 32:].astype(np.float64), table[pos, :32].astype(np.float64))
+        L = int(wl.seq_len[b])
+        K = C.dequant_seq(wl, Kp, ts_k, b, L)
+        V = C.dequant_seq(wl, Vp, ts_v, b, L)
+        kw, vw = C.window_codes(wl, tw_k, tw_v, b)
+        Kw, Vw = F.fp8_dequantize(kw, tw_k), F.fp8_dequantize(vw, tw_v)
+        Kall = np.concatenate([K, Kw], 0)
+        Vall = np.concatenate([V, Vw], 0)
+        q = F.bf16_to_f64(wl.q_bits_seq(b))
+        # scale the rotated query part by the table's radius (fp32 cos^2 + sin^2 != 1 exactly)
+        qs = q.copy()
+        qs[:, 64::2] *= rad
+        qs[:, 65::2] *= rad
+        Kinv = _complex_rotate(Kall, th, 64, sign=-1.0)
+        z = (qs @ Kinv.T) / np.sqrt(128)
+        m = z.max(1, keepdims=True)
+        p = np.exp(z - m)
+        O = (p @ Vall) / p.sum(1, keepdims=True)
+        lse = (m + np.log(p.sum(1, keepdims=True)))[:, 0]
+        O = _complex_rotate(O, th, 64, sign=-1.0)
+        O[:, 64::2] *= rad
+        O[:, 65::2] *= rad
+        Of, Lf, codes = C.expected_decode_fused(wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b, table, 64, W.OUT_SCALE)
+        np.testing.assert_allclose(Of, O, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(Lf, lse, rtol=1e-12)
+
+
+def test_fused_codes_are_the_fp8_encoding_of_the_output():
+    wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v = _small_workload()
+    table = W.rope_table(wl.seed, 400, 64)
+    Of, _, codes = C.expected_decode_fused(wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v, 0, table, 64, W.OUT_SCALE)
+    assert codes.dtype == np.uint8 and codes.shape == Of.shape
+    # decoded codes within half an E4M3 step of the scaled output (no saturation here)
+    x = Of / W.OUT_SCALE
+    assert np.abs(x).max() < 448
+    dec = F.fp8_dequantize(codes, W.OUT_SCALE) / W.OUT_SCALE
+    step = np.where(np.abs(x) < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -6))) - 3))
+    assert np.all(np.abs(dec - x) <= step / 2 + 1e-12)
+
+
+def test_fused_sparse_selection_matches_dense_on_all_positions():
+    wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v = _small_workload()
+    table = W.rope_table(wl.seed, 400, 64)
+    b = 1
+    sel = np.arange(int(wl.seq_len[b]))
+    a = C.expected_decode_fused(wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b, table, 64, W.OUT_SCALE)
+    s = C.expected_decode_fused(wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b, table, 64, W.OUT_SCALE, sel=sel)
+    assert all(np.array_equal(x, y) for x, y in zip(s, a))

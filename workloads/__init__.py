@@ -27,7 +27,11 @@ D_INDEX = 128      # index-key / index-query width
 H_INDEX = 64       # index heads
 
 # tensor ids of the substreams
-T_K, T_V, T_Q, T_KW, T_VW, T_IK, T_IQ, T_W, T_KNEW, T_VNEW, T_RQ, T_OUTL, T_CAND = range(1, 14)
+T_K, T_V, T_Q, T_KW, T_VW, T_IK, T_IQ, T_W, T_KNEW, T_VNEW, T_RQ, T_OUTL, T_CAND, T_ROPE = range(1, 15)
+
+ROPE_DIM = 64      # channels of each head a fused decode rotates (the last ROPE_DIM of d)
+OUT_SCALE = 1.0 / 64.0   # FP8 output scale of a fused decode: O/OUT_SCALE in E4M3's normal range
+                         # for softmax averages of N(0,1) rows; |O| > 7 saturates at 448
 
 
 def rng(seed: int, *key: int) -> np.random.Generator:
@@ -89,6 +93,10 @@ class Workload:
     replay: bool = False           # bounded replay: 128 queries at [H-128, H)
     prefix_len: Optional[np.ndarray] = None   # H per sequence (replay)
     n_cand: int = 0                # >0: candidate-list scoring of that many positions per sequence
+
+    def rope_pos(self) -> np.ndarray:
+        """int32 [B]: position of each sequence's query token (its newest, seq_len - 1)."""
+        return np.maximum(self.seq_len.astype(np.int64) - 1, 0).astype(np.int32)
 
     def cand_lists(self, n: int) -> np.ndarray:
         """int32 [B][n]: min(n, L) distinct positions per sequence, ascending, -1 padded."""
@@ -161,6 +169,15 @@ class Workload:
         """(b, t0, t1) token ranges a cache fill writes, shared pages once."""
         return [(b, int(self.fill_start[b]), int(self.fill_end[b])) for b in range(self.B)
                 if self.fill_end[b] > self.fill_start[b]]
+
+
+def rope_table(seed: int, max_pos: int, rope_dim: int = ROPE_DIM) -> np.ndarray:
+    """float32 [max_pos][rope_dim] rotary table in the layout a serving engine
+    keeps: per position, the cosines of its rope_dim/2 pair angles, then their
+    sines.  The angles are drawn uniformly on [0, 2 pi) (seeded), so the table
+    exercises arbitrary rotations; the attention path takes any table."""
+    th = rng(seed, T_ROPE, max_pos, rope_dim).random((max_pos, rope_dim // 2)) * (2.0 * np.pi)
+    return np.concatenate([np.cos(th), np.sin(th)], axis=1).astype(np.float32)
 
 
 def _pages_for(lengths: np.ndarray) -> np.ndarray:
