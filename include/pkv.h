@@ -196,6 +196,38 @@ pkv_status pkv_decode_attn(pkv_ctx* ctx, const void* q_bf16, const pkv_kv_cache*
                            float softmax_scale, float* out, float* out_lse, void* ws,
                            size_t ws_bytes, void* stream);
 
+/* Rotary and FP8-output parameters of the fused decode below. */
+typedef struct {
+  const int32_t* pos;     /* device [B]: position of each sequence's query token (a row of cos_sin) */
+  const float* cos_sin;   /* device [max_pos][rope_dim], 16-byte aligned: per position the cosines of
+                             the rope_dim/2 pair angles, then their sines (a serving engine's rotary cache) */
+  int max_pos;            /* rows of cos_sin, >= 1 */
+  int rope_dim;           /* rotated channels, the last rope_dim of d: a multiple of 8 in [8, d] */
+  float out_scale;        /* FP8 output scale: finite, > 0 */
+} pkv_rope_fp8;
+
+/* Fused decode ("MegaAttention avec KV compressé NVFP4", vLLM blog "Kernels":
+ * query RoPE, attention, inverse RoPE on the output and FP8 conversion in one
+ * pass, writing the buffer the output projection reads).  With c_i, s_i the
+ * entries i and rope_dim/2 + i of row pos[b] of cos_sin, and pair i the
+ * channels (d - rope_dim + 2i, d - rope_dim + 2i + 1) of a head:
+ *   q' = q with each pair (x0, x1) -> (x0 c_i - x1 s_i, x0 s_i + x1 c_i);
+ *   (O, LSE) = pkv_decode_attn of q' (same entries, sel_idx, window, scale);
+ *   O' = O with each pair (y0, y1) -> (y0 c_i + y1 s_i, -y0 s_i + y1 c_i);
+ *   out_fp8 uint8 [B][H][d] = E4M3(fp32(O' / out_scale)) (nearest, ties to
+ *   even, saturating at 448, sign kept);
+ *   out float32 [B][H][d] = O' and out_lse float32 [B][H] when not NULL.
+ * Channels outside the rotated part pass through.  q' enters the tensor-core
+ * contraction rounded to f16.  A position outside [0, max_pos) sets the error
+ * word (PKV_ERR_BAD_PAGE: an index out of range) and that row is not rotated.
+ * Workspace as pkv_decode_attn.  PKV_ERR_UNSUPPORTED unless the tensor-core
+ * kernel takes the shape (n_heads <= 64; tw_v / ts_v within [2^-7, 2^7]). */
+pkv_status pkv_decode_attn_fused(pkv_ctx* ctx, const void* q_bf16, const pkv_kv_cache* cache,
+                                 const int32_t* page_table, int max_pages, const int32_t* seq_len,
+                                 int B, const int32_t* sel_idx, int k, const pkv_window* win,
+                                 float softmax_scale, const pkv_rope_fp8* fz, uint8_t* out_fp8,
+                                 float* out, float* out_lse, void* ws, size_t ws_bytes, void* stream);
+
 /* Bounded replay ("SWA bounded replay", "Côté encodeur"): for sequence b with
  * prefix length H_b = prefix_len[b] >= 128 and s_b = H_b - 128, query r
  * (q bf16 [B][128][n_heads][d], position s_b + r) attends the global tokens

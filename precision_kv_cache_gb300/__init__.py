@@ -53,6 +53,11 @@ class _Window(ctypes.Structure):
                 ("tw_v", ctypes.c_float), ("win_len", ctypes.c_void_p)]
 
 
+class _RopeFp8(ctypes.Structure):
+    _fields_ = [("pos", ctypes.c_void_p), ("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int),
+                ("rope_dim", ctypes.c_int), ("out_scale", ctypes.c_float)]
+
+
 _lib = None
 
 
@@ -76,6 +81,9 @@ def lib() -> ctypes.CDLL:
                                         vp]),
             "pkv_decode_attn": (i, [vp, vp, ctypes.POINTER(_KVCache), vp, i, vp, i, vp, i,
                                     ctypes.POINTER(_Window), f, vp, vp, vp, sz, vp]),
+            "pkv_decode_attn_fused": (i, [vp, vp, ctypes.POINTER(_KVCache), vp, i, vp, i, vp, i,
+                                          ctypes.POINTER(_Window), f, ctypes.POINTER(_RopeFp8), vp, vp, vp, vp, sz,
+                                          vp]),
             "pkv_replay_attn": (i, [vp, vp, ctypes.POINTER(_KVCache), vp, i, vp, i, ctypes.POINTER(_Window),
                                     f, vp, vp, vp, sz, vp]),
             "pkv_merge": (i, [vp, vp, vp, vp, vp, vp, i, i, vp]),
@@ -238,6 +246,23 @@ class Context:
         _check(lib().pkv_decode_attn(self.h, _p(q), ctypes.byref(c), _p(page_table), page_table.shape[1],
                                      _p(seq_len), B, _p(sel_idx), k, ctypes.byref(w), scale, _p(out),
                                      _p(out_lse), _p(ws), ws.numel(), _stream(stream)), "pkv_decode_attn")
+
+    def pkv_decode_attn_fused(self, q, cache: KVCache, page_table, seq_len, win: Window, scale, pos, cos_sin,
+                              rope_dim, out_scale, out_fp8, out=None, out_lse=None, ws=None, sel_idx=None,
+                              stream=None):
+        """Decode with query RoPE, inverse RoPE on O and E4M3 output (cos_sin float32 [max_pos][rope_dim])."""
+        B = seq_len.shape[0]
+        k = sel_idx.shape[1] if sel_idx is not None else 0
+        if ws is None:
+            ws = (self.workspace(OP_DECODE_SPARSE, B, k) if sel_idx is not None
+                  else self.workspace(OP_DECODE, B, page_table.shape[1] * PAGE))
+        c = cache._c()
+        w = win._c()
+        fz = _RopeFp8(pos.data_ptr(), cos_sin.data_ptr(), cos_sin.shape[0], rope_dim, out_scale)
+        _check(lib().pkv_decode_attn_fused(self.h, _p(q), ctypes.byref(c), _p(page_table), page_table.shape[1],
+                                           _p(seq_len), B, _p(sel_idx), k, ctypes.byref(w), scale, ctypes.byref(fz),
+                                           _p(out_fp8), _p(out), _p(out_lse), _p(ws), ws.numel(), _stream(stream)),
+               "pkv_decode_attn_fused")
 
     def pkv_decode_attn_noalloc(self, q, cache: KVCache, page_table, seq_len, win: Window, scale, out,
                                 out_lse=None, sel_idx=None, stream=None):

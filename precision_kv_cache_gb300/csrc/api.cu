@@ -344,6 +344,70 @@ pkv_status pkv_decode_attn(pkv_ctx* c, const void* q, const pkv_kv_cache* cache,
   return run_attention(c, a, max_entries, out, out_lse, ws, ws_bytes, (cudaStream_t)stream);
 }
 
+pkv_status pkv_decode_attn_fused(pkv_ctx* c, const void* q, const pkv_kv_cache* cache, const int32_t* page_table,
+                                 int max_pages, const int32_t* seq_len, int B, const int32_t* sel_idx, int k,
+                                 const pkv_window* win, float softmax_scale, const pkv_rope_fp8* fz,
+                                 uint8_t* out_fp8, float* out, float* out_lse, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (!c || B <= 0 || max_pages <= 0 || !q || !page_table || !seq_len || !fz || !out_fp8 || !aligned16(q) ||
+      !aligned16(out_fp8) || (out && !aligned16(out)))
+    return PKV_ERR_INVALID_ARG;
+  if (!fz->pos || !fz->cos_sin || !aligned16(fz->cos_sin) || fz->max_pos < 1 || fz->rope_dim < 8 ||
+      fz->rope_dim > c->cfg.d || fz->rope_dim % 8 != 0 || !(fz->out_scale > 0.f) || !(fz->out_scale < INFINITY))
+    return PKV_ERR_INVALID_ARG;
+  if ((long long)fz->max_pos * fz->rope_dim > (1LL << 40)) return PKV_ERR_INVALID_ARG;
+  if (!valid_cache(c, cache) || !valid_window(win)) return PKV_ERR_INVALID_ARG;
+  if (sel_idx && (k < 1 || k > PKV_TOPK_MAX_K)) return PKV_ERR_INVALID_ARG;
+  if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
+    return PKV_ERR_INVALID_ARG;
+  if ((long long)max_pages * PKV_PAGE > (1LL << 30)) return PKV_ERR_UNSUPPORTED;
+  pkv::AttnArgs a{};
+  a.q = (const uint16_t*)q;
+  a.cache = *cache;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.lens = seq_len;
+  a.wk = win->k;
+  a.wv = win->v;
+  a.tw_k = win->tw_k;
+  a.tw_v = win->tw_v;
+  a.win_len = win->win_len;
+  a.scale = softmax_scale;
+  a.H = c->cfg.n_heads;
+  a.D = c->cfg.d;
+  a.n_groups = B;
+  a.replay = 0;
+  a.err = c->d_err;
+  a.rope_pos = fz->pos;
+  a.cos_sin = fz->cos_sin;
+  a.max_pos = fz->max_pos;
+  a.rope_dim = fz->rope_dim;
+  a.out_scale = fz->out_scale;
+  a.out_fp8 = out_fp8;
+  // the fusion lives in the tensor-core kernel's Q load and merge epilogue
+  if (!pkv_attn_tc_supported(a, c->cfg.d)) return PKV_ERR_UNSUPPORTED;
+  DeviceGuard g(c->device);
+  if (sel_idx) {
+    const size_t need = pkv_workspace_bytes(c, PKV_OP_DECODE_SPARSE, B, k);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return PKV_ERR_WORKSPACE;
+    const size_t gbytes = (pkv_gather_ws_bytes(c->cfg.d, B, k) + 255) / 256 * 256;
+    pkv_kv_cache compact{};
+    int32_t *cpt = nullptr, *clen = nullptr;
+    int npb = 0;
+    c->launches += 2;
+    cudaError_t e = pkv_launch_gather(c->cfg.d, *cache, page_table, max_pages, sel_idx, B, k, ws, &compact, &cpt,
+                                      &clen, &npb, c->d_err, (cudaStream_t)stream);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    a.cache = compact;
+    a.page_table = cpt;
+    a.max_pages = npb;
+    a.lens = clen;
+    return run_attention(c, a, npb * PKV_PAGE + PKV_WINDOW, out, out_lse, (uint8_t*)ws + gbytes, ws_bytes - gbytes,
+                         (cudaStream_t)stream);
+  }
+  return run_attention(c, a, max_pages * PKV_PAGE + PKV_WINDOW, out, out_lse, ws, ws_bytes, (cudaStream_t)stream);
+}
+
 pkv_status pkv_replay_attn(pkv_ctx* c, const void* q, const pkv_kv_cache* cache, const int32_t* page_table,
                            int max_pages, const int32_t* prefix_len, int B, const pkv_window* cw,
                            float softmax_scale, float* out, float* out_lse, void* ws, size_t ws_bytes,

@@ -28,6 +28,13 @@ struct AttnArgs {
   float* part_o;              // [n_groups][n_split][H][D]
   float* part_lse;            // [n_groups][n_split][H]
   int* err;
+  // fused decode (tensor-core path only): query rotation before QK, inverse
+  // rotation of O and its FP8 encoding in the merge; rope_dim 0 = none
+  const int32_t* rope_pos;    // [n_groups] row of cos_sin of each query row
+  const float* cos_sin;       // [max_pos][rope_dim]: cosines, then sines
+  int max_pos, rope_dim;
+  float out_scale;
+  uint8_t* out_fp8;           // [n_groups][H][D] or NULL
 };
 
 // Which sequence a query row belongs to and how many global / window entries it sees.

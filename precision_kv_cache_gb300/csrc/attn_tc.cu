@@ -30,6 +30,11 @@
 //   * warps 16-23 run the online softmax on S (FP32, exp2, lazy max update
 //     with threshold 2^8), write P (f16, shared memory) and finally normalize
 //     O and write the partial result.
+//   * fused decode ("MegaAttention avec KV compressé NVFP4": query RoPE,
+//     attention, inverse RoPE on the output, FP8 output in one pass): the Q
+//     load turns the rotary pairs of each query before its f16 rounding, and
+//     the merge turns the final O back and encodes it as E4M3 - no extra
+//     kernel and no extra pass over O.
 // Every wait is bounded; on a timeout the CTA sets the error word, stops all
 // roles, drains its own copies / MMAs and frees its TMEM before returning.
 #include <cstddef>
@@ -216,13 +221,31 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
 
 // Q of query row g -> shared memory: f16 (from bf16; exact for |q| in [2^-14, 65504]),
 // K-major with the 128-byte swizzle, heads >= H zero.  Called by the 256 softmax threads.
+// Fused decode: the pairs (2i, 2i+1) of the last rope_dim channels are first turned
+// by the row's rotary angles (FP32, then rounded to f16).
 template <int D>
 __device__ __noinline__ void load_q(const AttnArgs& a, int g, uint8_t* sQ, int st) {
   constexpr int NV = NH * D / 8 / 256;                // 16-byte vectors per thread
   constexpr int NB = 4;                               // loads in flight per thread
   static_assert(NV % NB == 0, "Q vectors per thread");
+  static_assert(256 % (D / 8) == 0, "a thread sees the same 8 channels in every vector");
   const uint16_t* qg = a.q + (size_t)g * a.H * D;
   const uint32_t sq = tc::smem_u32(sQ);
+  // rotary factors of this thread's 4 channel pairs (if they lie in the rotated part)
+  bool rot = false;
+  float4 cr = make_float4(1.f, 1.f, 1.f, 1.f), sr = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.rope_dim > 0 && 8 * (st % (D / 8)) >= D - a.rope_dim) {
+    const int p = a.rope_pos[g];
+    if (p >= 0 && p < a.max_pos) {
+      const int i0 = 4 * (st % (D / 8)) - (D - a.rope_dim) / 2;
+      const float* row = a.cos_sin + (size_t)p * a.rope_dim;
+      cr = __ldg(reinterpret_cast<const float4*>(row + i0));
+      sr = __ldg(reinterpret_cast<const float4*>(row + a.rope_dim / 2 + i0));
+      rot = true;
+    } else {
+      report(a.err, PKV_DEVERR_BAD_PAGE);
+    }
+  }
 #pragma unroll 1
   for (int b0 = 0; b0 < NV; b0 += NB) {
     uint4 in[NB];
@@ -238,9 +261,18 @@ __device__ __noinline__ void load_q(const AttnArgs& a, int g, uint8_t* sQ, int s
       const int h = v / (D / 8), c8 = v % (D / 8);
       const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
       uint32_t r[4];
+      if (rot) {
+        const float c[4] = {cr.x, cr.y, cr.z, cr.w}, sn[4] = {sr.x, sr.y, sr.z, sr.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        r[i] = f32_to_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+        for (int i = 0; i < 4; ++i) {
+          const float x0 = __uint_as_float(w[i] << 16), x1 = __uint_as_float(w[i] & 0xFFFF0000u);
+          r[i] = f32_to_f16x2(x0 * c[i] - x1 * sn[i], x0 * sn[i] + x1 * c[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          r[i] = f32_to_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+      }
       const int atom = c8 >> 3, ch = c8 & 7;
       tc::sts128(sq + atom * (NH * 128) + h * 128 + 16 * (ch ^ (h & 7)), make_uint4(r[0], r[1], r[2], r[3]));
     }
@@ -896,14 +928,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   if (warp == W_MMA) tc::tmem_dealloc(tbase, 512);
 }
 
+// Output side of a fused decode, applied by the merge to the final O.
+struct Epilogue {
+  const int32_t* rope_pos;    // NULL: no rotation
+  const float* cos_sin;
+  int max_pos, rope_dim;
+  float out_scale;
+  uint8_t* out_fp8;           // NULL: no FP8 output
+  int* err;
+};
+
 // Merge the segment partials of each query row: rows cta+g for every CTA whose
 // (non-empty) tile range meets g's tiles.  One block of D/4 threads per (g, h):
 // warp 0 computes the LSE weights once, every thread combines one float4.
+// Fused decode: the merged O is turned back by the row's rotary angles and
+// encoded as E4M3 of O / out_scale.
 __global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups, int G, int H, int D,
                                 const float* __restrict__ part_o, const float* __restrict__ part_lse,
-                                float* __restrict__ out, float* __restrict__ out_lse) {
+                                float* __restrict__ out, float* __restrict__ out_lse, Epilogue ep) {
   __shared__ float wts[1024];
-  __shared__ int nseg_s, cl_s;
+  __shared__ int nseg_s, cl_s, pos_s;
   __shared__ float lse_s;
   const int g = blockIdx.x / H, h = blockIdx.x % H;
   const long long T = tile_start[n_groups];
@@ -934,6 +978,15 @@ __global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups
       nseg_s = n;
       cl_s = c_lo;
       lse_s = m == -INFINITY ? -INFINITY : m + logf(sum);
+      int p = -1;
+      if (ep.rope_pos) {
+        p = ep.rope_pos[g];
+        if (p < 0 || p >= ep.max_pos) {
+          if (h == 0) report(ep.err, PKV_DEVERR_BAD_PAGE);
+          p = -1;
+        }
+      }
+      pos_s = p;
     }
     const float inv = sum > 0.f ? 1.f / sum : 0.f;
     for (int i = threadIdx.x; i < n; i += 32) wts[i] *= inv;
@@ -959,7 +1012,25 @@ __global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups
         acc.z = fmaf(w, v[u].z, acc.z); acc.w = fmaf(w, v[u].w, acc.w);
       }
     }
-    reinterpret_cast<float4*>(out + ((size_t)g * H + h) * D)[d4] = acc;
+    if (pos_s >= 0 && 4 * d4 >= D - ep.rope_dim) {
+      // pairs i0, i0+1 of the rotated part: turn back by the row's angles
+      const int i0 = 2 * d4 - (D - ep.rope_dim) / 2;
+      const float* row = ep.cos_sin + (size_t)pos_s * ep.rope_dim;
+      const float2 c = __ldg(reinterpret_cast<const float2*>(row + i0));
+      const float2 sn = __ldg(reinterpret_cast<const float2*>(row + ep.rope_dim / 2 + i0));
+      const float4 o = acc;
+      acc.x = o.x * c.x + o.y * sn.x;
+      acc.y = o.y * c.x - o.x * sn.x;
+      acc.z = o.z * c.y + o.w * sn.y;
+      acc.w = o.w * c.y - o.z * sn.y;
+    }
+    if (out) reinterpret_cast<float4*>(out + ((size_t)g * H + h) * D)[d4] = acc;
+    if (ep.out_fp8) {
+      const float sc = ep.out_scale;
+      const uint32_t code = e4m3_code(__fdiv_rn(acc.x, sc)) | (e4m3_code(__fdiv_rn(acc.y, sc)) << 8) |
+                            (e4m3_code(__fdiv_rn(acc.z, sc)) << 16) | (e4m3_code(__fdiv_rn(acc.w, sc)) << 24);
+      reinterpret_cast<uint32_t*>(ep.out_fp8 + ((size_t)g * H + h) * D)[d4] = code;
+    }
   }
   if (threadIdx.x == 0 && out_lse) out_lse[(size_t)g * H + h] = lse_s;
 }
@@ -1030,8 +1101,18 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   e = cudaGetLastError();
   if (e0 && e1) cudaEventRecord(e1, st);
   if (e != cudaSuccess) return e;
+  Epilogue ep{};
+  if (a.rope_dim > 0) {
+    ep.rope_pos = a.rope_pos;
+    ep.cos_sin = a.cos_sin;
+    ep.max_pos = a.max_pos;
+    ep.rope_dim = a.rope_dim;
+  }
+  ep.out_scale = a.out_scale;
+  ep.out_fp8 = a.out_fp8;
+  ep.err = a.err;
   merge_tc_kernel<<<a.n_groups * a.H, a.D / 4, 0, st>>>(tile_start, a.n_groups, G, a.H, a.D, part_o, part_lse,
-                                                        out, out_lse);
+                                                        out, out_lse, ep);
   *n_launches = 3;
   return cudaGetLastError();
 }

@@ -63,3 +63,25 @@ def q_tensor(bits):
 def i32(a):
     import torch
     return torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).to(torch_dev())
+
+
+def assert_fp8_codes(gc, Or, out_scale, what, atol=ATOL, rtol=RTOL):
+    """E4M3 codes the GPU encoded from its own FP32 output, against the oracle's
+    float64 output Or.  The GPU's value lies within the attention tolerance of
+    Or and E4M3 rounding is monotone, so each code must decode between the
+    oracle's encodings of Or - tol and Or + tol: it equals the oracle's code
+    wherever no rounding midpoint lies within the tolerance."""
+    Or = np.asarray(Or, np.float64)
+    tol = atol + rtol * np.abs(Or)
+    lo = F.fp8_dequantize(F.fp8_quantize(Or - tol, out_scale), out_scale)
+    hi = F.fp8_dequantize(F.fp8_quantize(Or + tol, out_scale), out_scale)
+    g = F.fp8_dequantize(np.asarray(gc, np.uint8), out_scale)
+    bad = ~((g >= lo) & (g <= hi))
+    if bad.any():
+        i = np.unravel_index(np.argmax(bad), g.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {g.size} FP8 codes outside [{lo[i]}, {hi[i]}] at {i}: "
+                             f"gpu={g[i]} oracle value={Or[i]}")
+    # where the interval holds one value, the code is the oracle's exactly
+    one = lo == hi
+    rc = F.fp8_quantize(Or, out_scale)
+    assert np.array_equal(g[one], F.fp8_dequantize(rc, out_scale)[one]), what

@@ -70,6 +70,33 @@ def test_fullsize_dense_decode_8k(pool):
         assert_close(gl[b], L, f"c1 LSE seq {b}")
 
 
+def test_fullsize_fused_dense_decode_8k(pool):
+    """Fused decode (query RoPE, inverse RoPE on O, FP8 output) at the 8K dense decode size."""
+    import torch
+    from helpers import assert_fp8_codes
+    wl, ctx, cache, pt, win, ts, tw = _setup("c1", pool)
+    dev = torch_dev()
+    q = torch.from_numpy(wl.q_bits().view(np.int16)).to(dev).view(torch.bfloat16)
+    pos = wl.rope_pos()
+    table = W.rope_table(wl.seed, int(pos.max()) + 1, W.ROPE_DIM)
+    out = torch.empty(wl.B, wl.H, wl.d, device=dev)
+    lse = torch.empty(wl.B, wl.H, device=dev)
+    o8 = torch.empty(wl.B, wl.H, wl.d, dtype=torch.uint8, device=dev)
+    scale = 1 / math.sqrt(wl.d)
+    ctx.pkv_decode_attn_fused(q, cache, pt, torch.from_numpy(wl.seq_len).to(dev), win, scale, i32(pos),
+                              torch.from_numpy(table).to(dev), W.ROPE_DIM, W.OUT_SCALE, o8, out, lse)
+    torch.cuda.synchronize()
+    assert ctx.pkv_get_error() == 0 and ctx.pkv_attn_path() == 2
+    go, gl, g8 = out.cpu().numpy(), lse.cpu().numpy(), o8.cpu().numpy()
+    for b in (0, 31):
+        Kp, Vp = _oracle_seq(wl, b, int(wl.seq_len[b]), ts)
+        Or, L, _ = C.expected_decode_fused(wl, Kp, Vp, ts, ts, tw, tw, b, table, W.ROPE_DIM, W.OUT_SCALE,
+                                           scale=scale)
+        assert_close(go[b], Or, f"c1 fused O' seq {b}")
+        assert_close(gl[b], L, f"c1 fused LSE seq {b}")
+        assert_fp8_codes(g8[b], Or, W.OUT_SCALE, f"c1 fused FP8 seq {b}")
+
+
 def test_fullsize_ragged_paged_decode_with_append(pool):
     import torch
     wl, ctx, cache, pt, win, ts, tw = _setup("c2", pool)
