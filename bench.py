@@ -2,7 +2,7 @@
 """Benchmark of the NVFP4-KV decode-attention path on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c1|c2|c3|c4]
+                    [--workload c1|c2|c3|c4|c3c|c1f|c3f]
 
 A step is one pass of the decode path over one batch held in HBM.  Default
 workload (c2): 64 sequences of 16K-32K tokens (uniform), 64 query heads sharing
@@ -11,7 +11,9 @@ their first 4096 tokens, an FP8 window of 128 entries per sequence; the step
 appends one NVFP4 token per sequence and then runs decode attention (split-K
 over the global pages, window segment, LSE merge).  Other workloads: c1 (dense
 8K decode, B=32), c3 (index scoring + top-2048 + sparse decode, B=4 at 512K),
-c4 (bounded replay of 128 tokens, B=16, H in [32K,128K]).
+c4 (bounded replay of 128 tokens, B=16, H in [32K,128K]); c3c (c3 scoring a
+fixed 16K candidate set per sequence); c1f / c3f (c1 / c3 with the decode as
+one fused call: query RoPE, attention, inverse RoPE on O, E4M3 output).
 
 Metric: decode-attention KV GB/s = needed bytes / step time, where needed bytes
 count the NVFP4 K/V bytes (codes + scales) of every distinct token the step
@@ -43,8 +45,9 @@ sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
 
-WORKLOADS = {"c1": 1, "c2": 2, "c3": 3, "c4": 4, "c3c": 3}
+WORKLOADS = {"c1": 1, "c2": 2, "c3": 3, "c4": 4, "c3c": 3, "c1f": 1, "c3f": 3}
 CAND_C3C = 16384                   # c3c: the sparse workload scoring a fixed candidate set per sequence
+FUSED = ("c1f", "c3f")             # the decode as one fused call: query RoPE, attention, inverse RoPE, FP8 O
 SWEEP = {f"s{L // 1024}k": L for L in W.LONG_CONTEXT}     # long-context decode sweep (--sweep)
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
@@ -72,6 +75,8 @@ def _wl_cache(name):
         _WL[name] = W.long_context(SWEEP[name]) if name in SWEEP else W.config(WORKLOADS[name])
         if name == "c3c":
             _WL[name].n_cand = CAND_C3C
+        if name in FUSED:
+            _WL[name].name += "_fused"
     return _WL[name]
 
 
@@ -81,6 +86,9 @@ def workload_desc(name):
         return f"long-context decode sweep: batch {wl.B}, 64 heads, d=512, {SWEEP[name]} global tokens each + window"
     if name == "c3c":
         return W.CONFIGS[3] + f", scoring only a fixed {CAND_C3C}-position candidate set per sequence"
+    if name in FUSED:
+        return (W.CONFIGS[WORKLOADS[name]] + f"; fused decode: query RoPE on the last {W.ROPE_DIM} channels, "
+                "inverse RoPE on O, E4M3 output")
     return W.CONFIGS[WORKLOADS[name]]
 
 
@@ -191,7 +199,7 @@ def kv_token_bytes(d):
     return 2 * (d // 2 + d // 16)          # K and V: codes + E4M3 scales
 
 
-def needed_bytes(wl, sel_counts=None):
+def needed_bytes(wl, sel_counts=None, fused=False):
     """Algorithmic bytes of one decode-attention launch over ``wl`` (see module doc)."""
     d, H, B = wl.d, wl.H, wl.B
     if sel_counts is not None:
@@ -219,6 +227,8 @@ def needed_bytes(wl, sel_counts=None):
     win = B * 128 * d * 2
     q = rows * H * d * 2
     o = rows * H * (d + 1) * 4
+    if fused:     # E4M3 O + LSE, plus each row's position and cos/sin row
+        o = rows * H * d + rows * H * 4 + rows * (4 + W.ROPE_DIM * 4)
     return tokens * kv_token_bytes(d) + pt + win + q + o, tokens
 
 
@@ -305,6 +315,11 @@ def run_gpu(args, rank, world, pool):
         ws = ctx.workspace(P.OP_DECODE_SPARSE, B, wl.topk)
     elif not wl.replay:
         ws = ctx.workspace(P.OP_DECODE, B, pt.shape[1] * 64)
+    fused = name in FUSED
+    if fused:
+        rpos = torch.from_numpy(wl.rope_pos()).to(dev)
+        table = torch.from_numpy(W.rope_table(wl.seed, int(wl.rope_pos().max()) + 1, W.ROPE_DIM)).to(dev)
+        out8 = torch.empty(B, H, d, dtype=torch.uint8, device=dev)
     if wl.append:
         knew = torch.from_numpy(wl.new_rows(W.T_KNEW)).to(dev)
         vnew = torch.from_numpy(wl.new_rows(W.T_VNEW)).to(dev)
@@ -325,6 +340,9 @@ def run_gpu(args, rank, world, pool):
             ctx.pkv_set_profile_events(ev[0], ev[1])
         if wl.replay:
             ctx.pkv_replay_attn(q, cache, pt, plen, win, scale, out, lse, ws=ws)
+        elif fused:
+            ctx.pkv_decode_attn_fused(q, cache, pt, seq_len, win, scale, rpos, table, W.ROPE_DIM, W.OUT_SCALE, out8,
+                                      None, lse, ws=ws, sel_idx=sel)
         else:
             ctx.pkv_decode_attn(q, cache, pt, seq_len, win, scale, out, lse, ws=ws, sel_idx=sel)
 
@@ -389,14 +407,14 @@ def run_gpu(args, rank, world, pool):
     # ---- accounting
     if wl.topk:
         cnt = (sel >= 0).sum(1).cpu().numpy()
-        attn_bytes, tokens = needed_bytes(wl, sel_counts=cnt)
+        attn_bytes, tokens = needed_bytes(wl, sel_counts=cnt, fused=fused)
         if wl.n_cand:     # candidate list + the candidates' index keys
             score_bytes = B * wl.n_cand * (4 + 64 + 8) + B * 64 * 128 + B * 64 * 4 + B * wl.topk * 4
         else:
             score_bytes = sum((int(L) + 63) // 64 for L in wl.seq_len) * 64 * (64 + 8) + B * 64 * 128 + B * 64 * 4 + B * wl.topk * 4
         step_bytes = attn_bytes + score_bytes
     else:
-        attn_bytes, tokens = needed_bytes(wl)
+        attn_bytes, tokens = needed_bytes(wl, fused=fused)
         step_bytes = attn_bytes + (B * (2 * d * 4 + 8 + kv_token_bytes(d)) if wl.append else 0)
     gbs = job_gbs(step_bytes, ms_step, world)
     peak, peak_kind = measured_peak()
@@ -423,7 +441,8 @@ def run_gpu(args, rank, world, pool):
     e2e = None
     if not wl.topk:
         qh = torch.from_numpy(q_host.view(np.int16)).pin_memory()
-        oh = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        o_dev = out8 if fused else out
+        oh = torch.empty(o_dev.shape, dtype=o_dev.dtype).pin_memory()
         lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
         kh = vh = None
         if wl.append:
@@ -437,7 +456,7 @@ def run_gpu(args, rank, world, pool):
                 knew.copy_(kh, non_blocking=True)
                 vnew.copy_(vh, non_blocking=True)
             step()
-            oh.copy_(out, non_blocking=True)
+            oh.copy_(o_dev, non_blocking=True)
             lh.copy_(lse, non_blocking=True)
         for _ in range(2):
             e2e_step()
@@ -450,7 +469,7 @@ def run_gpu(args, rank, world, pool):
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(b2) / n_e2e
         bi = qh.numel() * 2 + (kh.numel() * 4 * 2 if wl.append else 0)
-        bo = oh.numel() * 4 + lh.numel() * 4
+        bo = oh.numel() * oh.element_size() + lh.numel() * 4
         e2e = {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
 
@@ -482,6 +501,24 @@ TC_DTYPE = "fp16 tensor-core MMA, fp32 accumulate"
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
+_TABLE = {}
+
+
+def _oracle_decode(name, wl, b, q, K, V, Kw, Vw, scale):
+    """The oracle's decode of one sequence; for a fused workload with the query
+    rotated, the output turned back and encoded as E4M3."""
+    from oracle import attention as A
+    from oracle import formats as F
+    if name not in FUSED:
+        return A.decode(q, K, V, Kw, Vw, scale)
+    if name not in _TABLE:
+        _TABLE[name] = W.rope_table(wl.seed, int(wl.rope_pos().max()) + 1, W.ROPE_DIM)
+    row = _TABLE[name][int(wl.rope_pos()[b])].astype(np.float64)
+    c, sn = row[:W.ROPE_DIM // 2], row[W.ROPE_DIM // 2:]
+    O, lse = A.decode(A.rope(q, c, sn, W.ROPE_DIM), K, V, Kw, Vw, scale)
+    return F.fp8_quantize(A.rope(O, c, sn, W.ROPE_DIM, inverse=True), W.OUT_SCALE), lse
+
+
 def oracle_sample(name, budget_s=15.0, max_seqs=None):
     """Time the float64 oracle's decode step on a bounded sample of the workload:
     sequences in order until ~budget_s seconds of timed CPU work."""
@@ -493,6 +530,8 @@ def oracle_sample(name, budget_s=15.0, max_seqs=None):
     ts, tw = np.float32(ts), np.float32(tw)
     spent, nbytes, seqs = 0.0, 0, 0
     scale = 1.0 / math.sqrt(wl.d)
+    if name in FUSED and name not in _TABLE:
+        _TABLE[name] = W.rope_table(wl.seed, int(wl.rope_pos().max()) + 1, W.ROPE_DIM)
     order = range(wl.B) if max_seqs is None else range(min(wl.B, max_seqs))
     for b in order:
         if wl.replay:
@@ -511,7 +550,7 @@ def oracle_sample(name, budget_s=15.0, max_seqs=None):
             A.replay(q, K, V, Kw, Vw, scale, rows=[0, 127])
             rows = 2
         else:
-            A.decode(F.bf16_to_f64(wl.q_bits_seq(b)), K, V, Kw, Vw, scale)
+            _oracle_decode(name, wl, b, F.bf16_to_f64(wl.q_bits_seq(b)), K, V, Kw, Vw, scale)
             rows = 1
         spent += time.perf_counter() - t0
         nbytes += L * kv_token_bytes(wl.d) + 128 * wl.d * 2 + rows * wl.H * wl.d * (2 + 4)
@@ -537,6 +576,8 @@ def run_reference(args):
     scale = 1.0 / math.sqrt(wl.d)
     prepared = []
     nprep = min(wl.B, 4)
+    if name in FUSED and name not in _TABLE:
+        _TABLE[name] = W.rope_table(wl.seed, int(wl.rope_pos().max()) + 1, W.ROPE_DIM)
     for b in range(nprep):
         L = int(wl.prefix_len[b]) - 128 if wl.replay else int(wl.seq_len[b])
         pages = {int(wl.page_table[b, j]) for j in range((L + 63) // 64)}
@@ -552,7 +593,7 @@ def run_reference(args):
         if wl.replay:
             A.replay(F.bf16_to_f64(wl.replay_q_bits(b)), K, V, Kw, Vw, scale, rows=[0])
             return L * kv_token_bytes(wl.d) + 128 * wl.d * 2 + wl.H * wl.d * 6
-        A.decode(F.bf16_to_f64(wl.q_bits_seq(b)), K, V, Kw, Vw, scale)
+        _oracle_decode(name, wl, b, F.bf16_to_f64(wl.q_bits_seq(b)), K, V, Kw, Vw, scale)
         return L * kv_token_bytes(wl.d) + 128 * wl.d * 2 + wl.H * wl.d * 6
 
     for i in range(args.warmup):
