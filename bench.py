@@ -49,6 +49,7 @@ WORKLOADS = {"c1": 1, "c2": 2, "c3": 3, "c4": 4, "c3c": 3, "c1f": 1, "c3f": 3}
 CAND_C3C = 16384                   # c3c: the sparse workload scoring a fixed candidate set per sequence
 FUSED = ("c1f", "c3f")             # the decode as one fused call: query RoPE, attention, inverse RoPE, FP8 O
 SWEEP = {f"s{L // 1024}k": L for L in W.LONG_CONTEXT}     # long-context decode sweep (--sweep)
+SCORE_SWEEP = {f"x{L // 1024}k": L for L in W.LONG_CONTEXT}   # index-scoring sweep (--score-sweep)
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
@@ -72,7 +73,12 @@ _WL = {}
 
 def _wl_cache(name):
     if name not in _WL:
-        _WL[name] = W.long_context(SWEEP[name]) if name in SWEEP else W.config(WORKLOADS[name])
+        if name in SCORE_SWEEP:     # the sparse shape (4 sequences, top-2048) at length L
+            L = SCORE_SWEEP[name]
+            _WL[name] = W.make_dense(f"sweep_scoring_{L // 1024}k", 0, 4, 64, 512, [L] * 4, perm_seed_key=L + 1)
+            _WL[name].topk = 2048
+        else:
+            _WL[name] = W.long_context(SWEEP[name]) if name in SWEEP else W.config(WORKLOADS[name])
         if name == "c3c":
             _WL[name].n_cand = CAND_C3C
         if name in FUSED:
@@ -251,6 +257,30 @@ def fill_cache(ctx, P, torch, wl, name, ts_k, ts_v, pool):
     return cache, pt
 
 
+def fill_index(ctx, P, torch, wl, name, ts, pool, pt):
+    """NVFP4 index keys of every page through the product append (each page written via its owner)."""
+    dev = torch.device(f"cuda:{ctx.device}")
+    ic = P.IdxCache.empty(wl.num_pages, ts, device=dev)
+    pages = list(range(wl.num_pages))
+    chunks = [(name, pages[i:i + 512]) for i in range(0, len(pages), 512)]
+    it = pool.map(_gen_index, chunks) if pool else map(_gen_index, chunks)
+    owner = {int(wl.page_table[b, j]): (b, j) for b in range(wl.B) for j in range(wl.page_table.shape[1])
+             if wl.page_table[b, j] >= 0}
+    for (pg, rows) in it:
+        bs = np.repeat([owner[p][0] for p in pg], 64).astype(np.int32)
+        ps = np.concatenate([64 * owner[p][1] + np.arange(64) for p in pg]).astype(np.int32)
+        ctx.pkv_append_index(torch.from_numpy(rows.reshape(-1, 128)).to(dev), torch.from_numpy(bs).to(dev),
+                             torch.from_numpy(ps).to(dev), ic, pt)
+    torch.cuda.synchronize()
+    return ic
+
+
+def score_kernel_bytes(wl, positions, pages):
+    """Algorithmic bytes of one index-scoring launch: 72 B of NVFP4 key + 4 B of score per
+    position, the page-table entries, the FP8 queries and the head weights."""
+    return positions * (64 + 8 + 4) + pages * 4 + wl.B * 64 * 128 + wl.B * 64 * 4
+
+
 def window_codes_gpu(P, torch, wl, tw, dev, rows_fn):
     x = torch.from_numpy(np.stack([rows_fn(b) for b in range(wl.B)])).to(dev)
     out = torch.empty(x.shape, dtype=torch.uint8, device=dev)
@@ -290,17 +320,7 @@ def run_gpu(args, rank, world, pool):
     q = torch.from_numpy(q_host.view(np.int16)).to(dev).view(torch.bfloat16)
     sel = None
     if wl.topk:
-        ic = P.IdxCache.empty(wl.num_pages, ts, device=dev)
-        pages = list(range(wl.num_pages))
-        chunks = [(name, pages[i:i + 512]) for i in range(0, len(pages), 512)]
-        it = pool.map(_gen_index, chunks) if pool else map(_gen_index, chunks)
-        # the dense page table maps (b, j) -> page; invert to write each page through its owner
-        owner = {int(wl.page_table[b, j]): (b, j) for b in range(B) for j in range(wl.page_table.shape[1])}
-        for (pg, rows) in it:
-            bs = np.repeat([owner[p][0] for p in pg], 64).astype(np.int32)
-            ps = np.concatenate([64 * owner[p][1] + np.arange(64) for p in pg]).astype(np.int32)
-            ctx.pkv_append_index(torch.from_numpy(rows.reshape(-1, 128)).to(dev), torch.from_numpy(bs).to(dev),
-                                 torch.from_numpy(ps).to(dev), ic, pt)
+        ic = fill_index(ctx, P, torch, wl, name, ts, pool, pt)
         qf = wl.index_q()
         tq = float(np.float32(np.float32(np.abs(qf).max()) / np.float32(448.0)))
         qidx = torch.empty(qf.shape, dtype=torch.uint8, device=dev)
@@ -331,13 +351,14 @@ def run_gpu(args, rank, world, pool):
     def step(ev=None):
         if wl.append:
             ctx.pkv_append_kv(knew, vnew, bidx, pos, cache, pt)
+        if ev is not None:
+            # the dominant kernel: index scoring on the sparse workloads, attention otherwise
+            ctx.pkv_set_profile_events(ev[0], ev[1])
         if wl.topk:
             if wl.n_cand:
                 ctx.pkv_score_topk_cand(qidx, tq, wts, ic, pt, cand, wl.topk, sel, ws=ws_s)
             else:
                 ctx.pkv_score_topk(qidx, tq, wts, ic, pt, seq_len, wl.topk, sel, ws=ws_s)
-        if ev is not None:
-            ctx.pkv_set_profile_events(ev[0], ev[1])
         if wl.replay:
             ctx.pkv_replay_attn(q, cache, pt, plen, win, scale, out, lse, ws=ws)
         elif fused:
@@ -424,6 +445,18 @@ def run_gpu(args, rank, world, pool):
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "bytes_per_launch": int(attn_bytes), "launch_ms": round(kern_ms, 5),
                 "traffic": committed_traffic("attention", name)}
+    if wl.topk:
+        if wl.n_cand:
+            positions, pages = B * wl.n_cand, B * ((wl.n_cand + 63) // 64)
+        else:
+            pages = sum((int(L) + 63) // 64 for L in wl.seq_len)
+            positions = int(np.sum(wl.seq_len))
+        sbytes = score_kernel_bytes(wl, positions, pages)
+        sach = sbytes / (kern_ms * 1e-3) / 1e9
+        roofline = {"kernel": "index scoring (score_tc_kernel)", "bound": "hbm", "achieved": round(sach, 2),
+                    "peak": peak, "unit": "GB/s", "frac": round(sach / peak, 4), "peak_kind": peak_kind,
+                    "bytes_per_launch": int(sbytes), "launch_ms": round(kern_ms, 5),
+                    "traffic": committed_traffic("score", name)}
     if wl.replay:
         # bounded replay is a dense contraction: QK^T and P.V, 2 flops per multiply-add,
         # for every (replayed row, head, entry it attends) = 4*H*d flops per (row, entry)
@@ -498,6 +531,97 @@ def run_gpu(args, rank, world, pool):
 
 
 TC_DTYPE = "fp16 tensor-core MMA, fp32 accumulate"
+
+
+def run_score_sweep(args, name, pool):
+    """Index scoring + top-2048 of the sparse shape (4 sequences) at one length, the L2
+    flushed (256 MB written) before every step, so the index keys come from HBM: one
+    line with the scoring kernel's roofline."""
+    import torch
+    import precision_kv_cache_gb300 as P
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    wl = _wl_cache(name)
+    ts, _ = tensor_scales()
+    ctx = P.Context(wl.d, wl.H, device=0)
+    pt = torch.from_numpy(wl.page_table).to(dev)
+    ic = fill_index(ctx, P, torch, wl, name, ts, pool, pt)
+    qf = wl.index_q()
+    tq = float(np.float32(np.float32(np.abs(qf).max()) / np.float32(448.0)))
+    qidx = torch.empty(qf.shape, dtype=torch.uint8, device=dev)
+    P.pkv_quantize_fp8(torch.from_numpy(qf).to(dev), tq, qidx)
+    wts = torch.from_numpy(wl.index_w()).to(dev)
+    seq_len = torch.from_numpy(wl.seq_len).to(dev)
+    sel = torch.empty(wl.B, wl.topk, dtype=torch.int32, device=dev)
+    ws = ctx.workspace(P.OP_SCORE_TOPK, wl.B, pt.shape[1] * 64)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)      # 256 MB > 129 MB of L2
+
+    def call():
+        ctx.pkv_score_topk(qidx, tq, wts, ic, pt, seq_len, wl.topk, sel, ws=ws)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    if ctx.pkv_get_error() != P.OK:
+        raise RuntimeError("device error during warm-up")
+    # the call captured once as a CUDA graph (events around the scoring kernel inside it);
+    # each step: flush the L2, then replay
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_call = ctx.pkv_launch_count()
+    call()
+    n_call = ctx.pkv_launch_count() - n_call
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(g):
+        ctx.pkv_set_profile_events(k0, k1)
+        call()
+    for _ in range(3):
+        flush.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    call_t, kern_t = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        a0.record()
+        g.replay()
+        a1.record()
+        torch.cuda.synchronize()
+        call_t.append(a0.elapsed_time(a1))
+        kern_t.append(k0.elapsed_time(k1))
+    clk = clocks.stop()
+    if ctx.pkv_get_error() != P.OK:
+        raise RuntimeError("device error in the timed region")
+    n0, n1 = 0, n_call * args.steps
+    call_ms = statistics.mean(call_t)
+    kern_ms = statistics.mean(kern_t)
+    pages = sum((int(L) + 63) // 64 for L in wl.seq_len)
+    positions = int(np.sum(wl.seq_len))
+    sbytes = score_kernel_bytes(wl, positions, pages)
+    needed = positions * (64 + 8) + pages * 4 + wl.B * 64 * (128 + 4) + wl.B * wl.topk * 4
+    peak, peak_kind = measured_peak()
+    ach = sbytes / (kern_ms * 1e-3) / 1e9
+    return {"metric": "index scoring + top-k GB/s (needed bytes / call time)",
+            "value": round(needed / (call_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(call_ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 tensor-core MMA (f32 accumulate)",
+            "data": "synthetic (seeded N(0,1) index keys with 2% channels x8, FP8 queries, U(0,1) weights)",
+            "config": {"workload": f"index scoring sweep: batch {wl.B}, 64 FP8 index heads x 128, NVFP4 keys, "
+                                   f"{SCORE_SWEEP[name]} positions each, top-{wl.topk}",
+                       "name": wl.name, "batch": wl.B, "positions": positions, "needed_bytes_per_step": int(needed),
+                       "l2": "flushed before every step (256 MB written, outside the timed events)"},
+            "roofline": {"kernel": "index scoring (score_tc_kernel)", "bound": "hbm", "achieved": round(ach, 2),
+                         "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4), "peak_kind": peak_kind,
+                         "bytes_per_launch": int(sbytes), "launch_ms": round(kern_ms, 5), "traffic": None},
+            "clocks": clk, "gpu_launches": int(n1 - n0), "launches_per_step": (n1 - n0) / args.steps,
+            "plan_topk_ms": round(call_ms - kern_ms, 4), "step_mode": "cuda graph replay, L2 flushed between replays"}
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
@@ -627,6 +751,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(SWEEP), default="c2")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time eager calls instead of the step captured as one CUDA graph (the default)")
+    ap.add_argument("--score-sweep", action="store_true",
+                    help="index-scoring sweep (4 sequences of 32K-512K positions, L2 flushed per step): one line per length")
     ap.add_argument("--sweep", action="store_true",
                     help="long-context decode sweep (32K-512K tokens, >= 1 GiB of KV per step): one line per length")
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work for cpu_baseline")
@@ -655,6 +781,12 @@ def main():
             import torch.distributed as dist
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
             dist.init_process_group("nccl")
+        if args.score_sweep:
+            if rank == 0:
+                for name in sorted(SCORE_SWEEP, key=SCORE_SWEEP.get):
+                    print(json.dumps(run_score_sweep(args, name, pool)), flush=True)
+                    _WL.pop(name, None)
+            return
         if args.sweep:
             for name in sorted(SWEEP, key=SWEEP.get):
                 args.workload = name

@@ -274,8 +274,10 @@ pkv_status pkv_decode_attn_noalloc(pkv_ctx* ctx, const void* q_bf16, const pkv_k
 
 /* Measurement aids (no counterpart in the pages; used by the benchmark).
  * pkv_set_profile_events: when both are non-NULL cudaEvent_t handles, the next
- * attention call (decode or replay) records `start` on its stream right before
- * its main attention kernel and `stop` right after it, then forgets them.
+ * attention call (decode or replay) or scoring call (pkv_score_topk,
+ * pkv_score_topk_cand) records `start` on its stream right before its main
+ * kernel (attention, or index scoring) and `stop` right after it, then forgets
+ * them.
  * pkv_launch_count: number of kernels this context has launched so far.
  * pkv_attn_path: kernel family of the last attention call: 1 = CUDA-core
  * split-K path, 2 = tensor-core (tcgen05) path, 0 = none yet. */

@@ -17,7 +17,7 @@ struct pkv_ctx {
   int device;
   int num_sms;
   int* d_err;
-  cudaEvent_t prof_start = nullptr;   // one-shot events around the next attention kernel
+  cudaEvent_t prof_start = nullptr;   // one-shot events around the next attention or scoring kernel
   cudaEvent_t prof_stop = nullptr;
   long long launches = 0;
   int last_path = 0;                  // 1 = CUDA-core attention, 2 = tensor-core attention
@@ -212,8 +212,10 @@ pkv_status pkv_score_topk(pkv_ctx* c, const uint8_t* q_idx, float tq, const floa
   void* plan = p;
   p += pkv_score_tc_ws_bytes(B, c->num_sms);
   c->launches += 2 + PKV_TOPK_LAUNCHES;
+  cudaEvent_t e0 = c->prof_start, e1 = c->prof_stop;
+  c->prof_start = c->prof_stop = nullptr;
   cudaError_t e = pkv_launch_score_tc(q_idx, tq, w, *ic, page_table, max_pages, seq_len, B, c->cfg.n_index_heads,
-                                      scores, Lmax, plan, c->num_sms, c->d_err, st);
+                                      scores, Lmax, plan, c->num_sms, c->d_err, st, e0, e1);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return cuda_status(pkv_launch_topk(scores, Lmax, seq_len, B, k, out_idx, p, st));
 }
@@ -249,8 +251,10 @@ pkv_status pkv_score_topk_cand(pkv_ctx* c, const uint8_t* q_idx, float tq, const
   void* plan = p;
   p += pkv_score_tc_ws_bytes(B, c->num_sms);
   c->launches += 2 + 2 + PKV_TOPK_LAUNCHES + 1;
+  cudaEvent_t e0 = c->prof_start, e1 = c->prof_stop;
+  c->prof_start = c->prof_stop = nullptr;
   e = pkv_launch_score_tc(q_idx, tq, w, cc, cpt, npb, cnt, B, c->cfg.n_index_heads, scores, n_cand, plan,
-                          c->num_sms, c->d_err, st);
+                          c->num_sms, c->d_err, st, e0, e1);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   // top-k over candidate indices (ascending candidates: lower index = lower position), then to positions
   e = pkv_launch_topk(scores, n_cand, cnt, B, k, out_idx, p, st);

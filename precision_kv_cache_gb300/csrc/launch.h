@@ -47,6 +47,8 @@ cudaError_t pkv_launch_map_cand(int32_t* out, const int32_t* cand, int B, int n,
 
 size_t pkv_score_tc_ws_bytes(int B, int num_sms);
 cudaError_t pkv_score_tc_init();
+// prof_start/prof_stop (may be null): events recorded around the scoring kernel
 cudaError_t pkv_launch_score_tc(const uint8_t* q_idx, float tq, const float* w, const pkv_idx_cache& ic,
                                 const int32_t* page_table, int max_pages, const int32_t* seq_len, int B, int Hi,
-                                float* scores, int Lmax, void* ws, int num_sms, int* err, cudaStream_t st);
+                                float* scores, int Lmax, void* ws, int num_sms, int* err, cudaStream_t st,
+                                cudaEvent_t prof_start = nullptr, cudaEvent_t prof_stop = nullptr);

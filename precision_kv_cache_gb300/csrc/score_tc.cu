@@ -408,7 +408,8 @@ cudaError_t pkv_score_tc_init() {
 // scores[b][t] for t < seq_len[b]; ws holds the tile plan ([B+1] ints)
 cudaError_t pkv_launch_score_tc(const uint8_t* q_idx, float tq, const float* w, const pkv_idx_cache& ic,
                                 const int32_t* page_table, int max_pages, const int32_t* seq_len, int B, int Hi,
-                                float* scores, int Lmax, void* ws, int num_sms, int* err, cudaStream_t st) {
+                                float* scores, int Lmax, void* ws, int num_sms, int* err, cudaStream_t st,
+                                cudaEvent_t prof_start, cudaEvent_t prof_stop) {
   using namespace pkv::tcscore;
   Args a;
   a.q = q_idx; a.tq = tq; a.w = w; a.ic = ic; a.page_table = page_table; a.max_pages = max_pages;
@@ -417,6 +418,9 @@ cudaError_t pkv_launch_score_tc(const uint8_t* q_idx, float tq, const float* w, 
   const long long tmax = (long long)B * ((Lmax + TILE - 1) / TILE);
   const int G = (int)(tmax < num_sms ? (tmax > 0 ? tmax : 1) : num_sms);
   plan_kernel<<<1, 1024, 0, st>>>(a, tile_start, G);
+  if (prof_start && prof_stop) cudaEventRecord(prof_start, st);
   score_tc_kernel<<<G, NTHREADS, DYN, st>>>(a, tile_start);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (prof_start && prof_stop) cudaEventRecord(prof_stop, st);
+  return e;
 }
