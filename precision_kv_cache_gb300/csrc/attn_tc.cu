@@ -5,8 +5,9 @@
 // token), all H <= 64 query heads attend the same K/V (MQA over one shared
 // latent - vLLM blog "Performances agentiques"): the global tokens of the
 // sequence, stored in NVFP4 64-token pages ("MegaAttention avec KV compressé
-// NVFP4"), then the FP8 window entries ([news] "Les particularités du modèle
-// lui-même"; replay: causal, clipped at s = H-128, "SWA bounded replay").
+// NVFP4"), then the FP8 window entries (cocoloop summary of the same blog,
+// "Les particularités du modèle lui-même"; replay: causal, clipped at
+// s = H-128, "SWA bounded replay").
 // Output: a normalized partial (O, LSE) per (CTA, query row) segment, merged
 // by merge_tc_kernel ("flash-decoding": split along the sequence + LSE merge).
 //
@@ -16,15 +17,15 @@
 //     range per CTA (balanced to one tile).
 //   * warps 24 (K) and 26 (V) stream the raw pages of each tile (codes +
 //     scales) into two shared-memory page rings with 1-D bulk copies (TMA).
-//   * warps 0-7 (thread = token; two warps per TMEM lane quarter, each one
-//     half of the channels) dequantize K to f16 (exact: E2M1 x E4M3 has <= 6
-//     significant bits) into TMEM, 64 channels at a time: the A operand of
-//     S^T = K Q^T  (M = 128 tokens, N = 64 heads, K = d).
-//   * warps 8-15 (thread = channel; two warps per lane quarter, each one half
-//     of the tokens) dequantize V^T to f16 into TMEM, 128 channels x 64
-//     tokens at a time: the A operand of O^T = V^T P (M = 128 channels,
-//     N = 64 heads, K = tokens).  Each warp converts the E4M3 block scales it
-//     needs once (one per lane) and shares them through shared memory.
+//   * warps 0-7 (thread = token) dequantize K to f16 (exact: E2M1 x E4M3 has
+//     <= 6 significant bits) into TMEM, 64 channels at a time: the A operand
+//     of S^T = K Q^T  (M = 128 tokens, N = 64 heads, K = d).  Two groups of
+//     four warps (one per TMEM lane quarter) take alternate chunks.
+//   * warps 8-15 (thread = channel) dequantize V^T to f16 into TMEM, 128
+//     channels x 64 tokens at a time: the A operand of O^T = V^T P (M = 128
+//     channels, N = 64 heads, K = tokens); two groups of four warps take
+//     alternate chunks.  Each warp converts the E4M3 block scales of its
+//     chunk once (two per lane) and shares them through shared memory.
 //   * warp 25 issues the QK MMAs, warp 27 the PV MMAs (Q and P are the
 //     shared-memory B operands).
 //   * warps 16-23 run the online softmax on S (FP32, exp2, lazy max update
