@@ -187,15 +187,25 @@ def tensor_peak():
         return 1700.0, "fallback (bf16 dense, sustained)"
 
 
+def code_sha(path: str) -> str:
+    """Hash of a C/CUDA source without its comments and blank lines (a capture stays
+    valid across comment edits, not across code edits)."""
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    code = "\n".join(ln for ln in lines if ln.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
 def committed_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu capture, if taken on the current kernel source."""
+    """DRAM bytes per launch from a committed ncu capture, if taken on the current kernel code."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         e = d[kernel][workload]
         src = os.path.join(ROOT, "precision_kv_cache_gb300", "csrc", e["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return float(e["dram_bytes_per_launch"]) if sha == e["source_sha"] else None
+        return float(e["dram_bytes_per_launch"]) if code_sha(src) == e["code_sha"] else None
     except Exception:
         return None
 
@@ -565,12 +575,21 @@ def run_score_sweep(args, name, pool):
     torch.cuda.synchronize()
     if ctx.pkv_get_error() != P.OK:
         raise RuntimeError("device error during warm-up")
-    # the call captured once as a CUDA graph (events around the scoring kernel inside it);
-    # each step: flush the L2, then replay
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    # the scoring kernel alone: eager calls, the library's events around that kernel
+    n0 = ctx.pkv_launch_count()
+    kern_t = []
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_call = ctx.pkv_launch_count()
-    call()
-    n_call = ctx.pkv_launch_count() - n_call
+    for _ in range(args.steps):
+        flush.zero_()
+        ctx.pkv_set_profile_events(k0, k1)
+        call()
+        torch.cuda.synchronize()
+        kern_t.append(k0.elapsed_time(k1))
+    n_call = (ctx.pkv_launch_count() - n0) // args.steps
+    # the whole call (scoring + top-k) captured once as a CUDA graph; each step flushes
+    # the L2, then replays it between two events
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -578,16 +597,13 @@ def run_score_sweep(args, name, pool):
         call()
     torch.cuda.current_stream().wait_stream(side)
     with torch.cuda.graph(g):
-        ctx.pkv_set_profile_events(k0, k1)
         call()
     for _ in range(3):
         flush.zero_()
         g.replay()
     torch.cuda.synchronize()
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev.index)
-    clocks.start()
-    call_t, kern_t = [], []
+    call_t = []
     for _ in range(args.steps):
         flush.zero_()
         a0.record()
@@ -595,7 +611,6 @@ def run_score_sweep(args, name, pool):
         a1.record()
         torch.cuda.synchronize()
         call_t.append(a0.elapsed_time(a1))
-        kern_t.append(k0.elapsed_time(k1))
     clk = clocks.stop()
     if ctx.pkv_get_error() != P.OK:
         raise RuntimeError("device error in the timed region")
@@ -621,7 +636,7 @@ def run_score_sweep(args, name, pool):
                          "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4), "peak_kind": peak_kind,
                          "bytes_per_launch": int(sbytes), "launch_ms": round(kern_ms, 5), "traffic": None},
             "clocks": clk, "gpu_launches": int(n1 - n0), "launches_per_step": (n1 - n0) / args.steps,
-            "plan_topk_ms": round(call_ms - kern_ms, 4), "step_mode": "cuda graph replay, L2 flushed between replays"}
+            "plan_topk_ms": round(call_ms - kern_ms, 4), "step_mode": "call: cuda graph replay; scoring kernel: eager calls; L2 flushed before each"}
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
