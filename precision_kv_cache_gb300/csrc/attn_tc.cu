@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       // (the last use of each slot; earlier uses were waited for by the consumers)
       if (lane == 0)
         for (int k = (pi > nslot ? pi - nslot : 0); k < pi; ++k)
-          tc::mbar_wait(&fullb[k % nslot], (k / nslot) & 1, abort_p, 1LL << 31);
+          if (!tc::mbar_drain(&fullb[k % nslot], (k / nslot) & 1)) report(a.err, PKV_DEVERR_TIMEOUT);
     }
     // ======================================================== MMA issuers
     // One warp issues S^T = K Q^T (per 64-channel K chunk: 4 MMAs), another
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       // drain outstanding MMAs before TMEM is freed
       if (tc::elect_one()) tc::mma_commit(&sh.drain);
       __syncwarp();
-      tc::mbar_wait(&sh.drain, 0, abort_p, 1LL << 31);
+      if (!tc::mbar_drain(&sh.drain, 0) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     }
     else if (warp == W_MMA2) {
       const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       if (!ok && lane == 0) fail(sh, a.err);
       if (tc::elect_one()) tc::mma_commit(&sh.drain2);
       __syncwarp();
-      tc::mbar_wait(&sh.drain2, 0, abort_p, 1LL << 31);
+      if (!tc::mbar_drain(&sh.drain2, 0) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     }
     // ======================================================== K dequantizer (thread = token)
     // Two groups of four warps (one warp per TMEM lane quarter); group kg

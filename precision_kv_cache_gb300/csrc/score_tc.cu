@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
       }
       if (lane == 0)
         for (int k = (pi > NR ? pi - NR : 0); k < pi; ++k)
-          tc::mbar_wait(&sh.r_full[k % NR], (k / NR) & 1, abort_p, 1LL << 31);
+          if (!tc::mbar_drain(&sh.r_full[k % NR], (k / NR) & 1)) report(a.err, PKV_DEVERR_TIMEOUT);
     } else if (warp == W_MMA) {
       // ======================================================== MMA issuer (whole warp, one elected lane issues)
       const uint32_t idq = tc::idesc_f16(128, NH, false, false);
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
       if (!ok && lane == 0) fail(sh, a.err);
       if (tc::elect_one()) tc::mma_commit(&sh.drain);
       __syncwarp();
-      tc::mbar_wait(&sh.drain, 0, abort_p, 1LL << 31);
+      if (!tc::mbar_drain(&sh.drain, 0) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     } else if (warp >= W_DEQ && warp < W_EPI) {
       // ======================================================== key dequantizer (thread = token)
       // group kg takes the tiles n = kg, kg+2, ... of this CTA (n counted from x0)

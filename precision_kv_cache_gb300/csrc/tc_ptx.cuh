@@ -103,6 +103,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// The same wait without the abort test, bounded by `limit` cycles only: the
+// drains before a CTA exits (copies and MMAs it issued must have landed even
+// when another role gave up, or the CTA would leave them in flight).
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, long long limit = (1LL << 31)) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (clock64() - t0 > limit) return false;
+  }
+}
+
 // ---------------------------------------------------------------- bulk copy
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size multiple of 16),
 // completion reported as transaction bytes on `bar`.
