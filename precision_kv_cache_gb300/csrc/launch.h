@@ -24,9 +24,6 @@ cudaError_t pkv_launch_merge_splits(const float* part_o, const float* part_lse, 
                                     int H, int D, float* out, float* out_lse, cudaStream_t st);
 cudaError_t pkv_launch_merge2(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
                               float* o, float* lse, int rows, int dv, cudaStream_t st);
-cudaError_t pkv_launch_score_simple(const uint8_t* q_idx, float tq, const float* w, const pkv_idx_cache& ic,
-                                    const int32_t* page_table, int max_pages, const int32_t* seq_len, int B,
-                                    int Hi, float* scores, int Lmax, int* err, cudaStream_t st);
 size_t pkv_topk_ws_bytes(int B, int k, int Lmax);
 cudaError_t pkv_launch_topk(const float* scores, int Lmax, const int32_t* seq_len, int B, int k,
                             int32_t* out, void* ws, cudaStream_t st);
