@@ -540,9 +540,6 @@ def run_gpu(args, rank, world, pool):
     return res, wl
 
 
-TC_DTYPE = "fp16 tensor-core MMA, fp32 accumulate"
-
-
 def run_score_sweep(args, name, pool):
     """Index scoring + top-2048 of the sparse shape (4 sequences) at one length, the L2
     flushed (256 MB written) before every step, so the index keys come from HBM: one

@@ -43,10 +43,6 @@ def tensor_scales(wl: W.Workload, sample_pages: int = 64):
     return ts, tw
 
 
-def quantize_rows_nvfp4(rows, ts):
-    return F.nvfp4_quantize(rows, ts)
-
-
 def fill_pages(wl: W.Workload, ts_k, ts_v, pages=None):
     """Quantize and store the filled tokens of ``wl`` into fresh K and V pools.
     ``pages``: optional set of physical pages to fill (others stay zero)."""

@@ -62,10 +62,6 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return r.astype(np.uint16)
 
 
-def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
-    return (b.astype(np.uint32) << 16).view(np.float32)
-
-
 @dataclasses.dataclass
 class Workload:
     """One decode-attention workload: shapes, page tables and the page keys.
