@@ -7,6 +7,22 @@ whose device pointers are passed through unchanged; torch is used for device
 memory and streams only.  If the shared library has not been built
 (``python -m precision_kv_cache_gb300.build`` or ``__graft_entry__.build()``)
 importing the kernels raises - there is no CPU fallback.
+
+A decode step (d = 512, 64 query heads; every tensor on the context's GPU):
+
+    import precision_kv_cache_gb300 as P
+    ctx = P.Context(512, 64)
+    cache = P.KVCache.empty(num_pages, 512, ts_k, ts_v)     # paged NVFP4 K/V pools
+    win = P.Window(k_fp8, v_fp8, tw_k, tw_v)                # E4M3 window, [B][128][512]
+    ctx.pkv_append_kv(k_new, v_new, seq_idx, pos, cache, page_table)
+    ctx.pkv_decode_attn(q_bf16, cache, page_table, seq_len, win, 512 ** -0.5, out, lse)
+    assert ctx.pkv_get_error() == P.OK                      # synchronizes the stream
+
+A sparse step selects positions with ``pkv_score_topk`` (all positions) or
+``pkv_score_topk_cand`` (a candidate list) and passes them as ``sel_idx``;
+``pkv_decode_attn_fused`` adds query RoPE, inverse RoPE on the output and an
+E4M3 output; ``pkv_replay_attn`` re-runs the last 128 positions after a
+prefix hit.  Workspaces are sized by ``Context.workspace`` (or passed in).
 """
 from __future__ import annotations
 
