@@ -71,3 +71,17 @@ def test_reference_arm_prints_the_contract_line():
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["metric"] == "decode-attention KV GB/s (needed bytes / step time)"
+
+
+def test_every_bench_workload_builds_and_is_described():
+    names = sorted(bench.WORKLOADS) + sorted(bench.SWEEP) + sorted(bench.SCORE_SWEEP)
+    for name in names:
+        wl = bench._wl_cache(name)
+        assert wl.B >= 1 and wl.page_table.shape[0] == wl.B, name
+        assert (wl.page_table[wl.page_table >= 0] < wl.num_pages).all(), name
+        desc = bench.workload_desc(name) if name not in bench.SCORE_SWEEP else wl.name
+        assert isinstance(desc, str) and desc, name
+        total, tokens = bench.needed_bytes(wl, fused=name in bench.FUSED)
+        assert total > 0 and tokens >= 0, name
+        bench._WL.pop(name, None)
+    assert set(bench.FUSED) <= set(bench.WORKLOADS)
