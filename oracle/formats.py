@@ -144,17 +144,13 @@ def fp8_dequantize(codes, tw) -> np.ndarray:
     return E4M3[np.asarray(codes)] * np.float64(F32(tw))
 
 
-def tensor_scale_nvfp4(x) -> np.float32:
-    """FP32 tensor scale of an NVFP4 cache, fixed at fill: fp32(amax / (6 * 448))."""
-    return F32(F32(np.abs(np.asarray(x, F32)).max()) / F32(2688.0))
-
-
 def tensor_scale_fp8(x) -> np.float32:
     """FP32 tensor scale of an FP8 tensor: fp32(amax / 448)."""
     return F32(F32(np.abs(np.asarray(x, F32)).max()) / F32(448.0))
 
 
 def bf16_to_f64(bits) -> np.ndarray:
-    """bf16 bit patterns (uint16) -> float64 values (exact)."""
+    """bf16 bit patterns (uint16) -> float64 values (exact): a bf16 value is the
+    float32 whose upper 16 bits are the pattern and whose lower 16 bits are 0."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)

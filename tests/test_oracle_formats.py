@@ -138,3 +138,81 @@ def test_rejects_nonfinite():
         F.e4m3_encode(np.float32(np.inf))
     with pytest.raises(ValueError):
         F.nvfp4_quantize(np.zeros(16, np.float32), np.float32(0.0))
+
+
+# ---------------------------------------------------------------- bf16 queries
+def _bf16_by_definition(b: int) -> float:
+    """bf16 bit pattern -> value from the format's fields: sign bit 15, exponent
+    bits 14..7 (bias 127), mantissa bits 6..0 (7 bits, implicit leading 1 for
+    normal numbers); exponent 0 = subnormal (2^-126 * m/128), 255 = inf / NaN."""
+    s = -1.0 if b & 0x8000 else 1.0
+    e = (b >> 7) & 0xFF
+    m = b & 0x7F
+    if e == 0xFF:
+        return s * math.inf if m == 0 else math.nan
+    if e == 0:
+        return s * math.ldexp(m, -126 - 7)
+    return s * math.ldexp(128 + m, e - 127 - 7)
+
+
+def test_bf16_to_f64_hand_worked_patterns():
+    cases = {0x3F80: 1.0, 0xC000: -2.0, 0x3FC0: 1.5, 0xBF00: -0.5, 0x4049: 3.140625,
+             0x0080: 2.0 ** -126,                       # smallest normal
+             0x0001: 2.0 ** -133,                       # smallest subnormal
+             0x7F7F: (2.0 - 2.0 ** -7) * 2.0 ** 127,    # largest finite
+             0x7F80: math.inf, 0xFF80: -math.inf, 0x0000: 0.0}
+    got = F.bf16_to_f64(np.array(list(cases), np.uint16))
+    for (b, v), g in zip(cases.items(), got):
+        assert g == v, hex(b)
+    neg0 = F.bf16_to_f64(np.array([0x8000], np.uint16))[0]
+    assert neg0 == 0.0 and math.copysign(1.0, neg0) == -1.0
+    assert math.isnan(F.bf16_to_f64(np.array([0x7FC0], np.uint16))[0])
+
+
+def test_bf16_to_f64_every_pattern_by_field_decomposition():
+    got = F.bf16_to_f64(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+    ref = np.array([_bf16_by_definition(b) for b in range(65536)])
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all()
+    assert (got[~nan] == ref[~nan]).all()
+    assert (np.signbit(got[~nan]) == np.signbit(ref[~nan])).all()
+
+
+def test_bf16_to_f64_matches_ml_dtypes():
+    ml = pytest.importorskip("ml_dtypes")
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = b.view(ml.bfloat16).astype(np.float64)
+    got = F.bf16_to_f64(b)
+    fin = np.isfinite(ref)
+    assert (np.isfinite(got) == fin).all()
+    assert (got[fin] == ref[fin]).all()
+
+
+# ---------------------------------------------------------------- FP8 tensor scale
+def _f32_nearest(fr) -> np.float32:
+    """The float32 nearest to the rational fr (ties to the even significand),
+    found by comparing exact rationals against the neighbouring float32 values."""
+    from fractions import Fraction
+    c = np.float32(float(fr))
+    best = None
+    for v in (np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))):
+        d = abs(Fraction(float(v)) - fr)
+        if best is None or d < best[0] or (d == best[0] and (int(np.float32(v).view(np.uint32)) & 1) == 0):
+            best = (d, v)
+    return np.float32(best[1])
+
+
+def test_tensor_scale_fp8_worked_and_rounded():
+    from fractions import Fraction
+    assert F.tensor_scale_fp8(np.array([448.0, -3.0], np.float32)) == np.float32(1.0)
+    assert F.tensor_scale_fp8(np.array([-896.0, 5.0], np.float32)) == np.float32(2.0)
+    # amax is taken over magnitudes, then divided by 448 with one float32 rounding
+    for xs in ([-48.0, 3.0, 0.5], [100.0, -7.25], [1e-3, -2.5e-3], [3.0e4, 1.0]):
+        x = np.array(xs, np.float32)
+        amax = max(abs(Fraction(float(v))) for v in x)
+        assert F.tensor_scale_fp8(x) == _f32_nearest(amax / 448), xs
+    # every value of the tensor then encodes without saturation
+    g = np.random.default_rng(5)
+    x = (g.standard_normal(4096) * 7).astype(np.float32)
+    tw = F.tensor_scale_fp8(x)
+    assert np.abs(F.fp8_dequantize(F.fp8_quantize(x, tw), tw)).max() <= 448 * float(tw)
