@@ -520,9 +520,8 @@ def run_gpu(args, rank, world, pool):
         "metric": "decode-attention KV GB/s (needed bytes / step time)",
         "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("f16 tensor-core MMA (f32 accumulate, f32 softmax)" if ctx.pkv_attn_path() == 2
-                  else "f32 CUDA-core FMA"),
-        "attention_path": {1: "cuda-core split-K", 2: "tcgen05 tensor-core"}.get(ctx.pkv_attn_path(), "none"),
+        "dtype": "nvf4 block-scaled QK^T (5 FP4 query terms), e4m3 window QK^T, f16 PV; f32 accumulate and softmax",
+        "attention_path": {2: "tcgen05 tensor-core"}.get(ctx.pkv_attn_path(), "none"),
         "data": "synthetic (seeded N(0,1), 2% channels x8, bf16 Q; no trained weights)",
         "config": {"workload": workload_desc(name), "name": wl.name, "batch": B, "heads": H, "d": d,
                    "tokens_read": int(tokens), "needed_bytes_per_step": int(step_bytes),

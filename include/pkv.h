@@ -37,11 +37,16 @@
  *     caller through (ws, ws_bytes); pkv_workspace_bytes() gives the size.
  *
  * Cache byte layout (one 64-token page; d = head dim: 128, 256 or 512):
- *   K-layout (K, index keys):
- *     data  [64][d/2]: channel pair (2j,2j+1) of token t at byte
- *           t*(d/2) + 16*((j/16) ^ (t & s)) + j%16, s = min(8, d/32)-1,
- *           channel 2j in the low nibble;
+ *   K-layout (K): a token's d/2 code bytes in column blocks of R = min(128, d/2)
+ *     bytes, stored [d/(2R)][64 tokens][R] (the K-major operand layout, with
+ *     the 128- or 64-byte swizzle, of a block-scaled FP4 tensor-core
+ *     contraction: pages are read as stored).  Channel pair (2j, 2j+1) of
+ *     token t, q = j/16, w = t%8 (R = 128) or (t/2)%4 (R = 64), is at byte
+ *     (q/(R/16))*64*R + t*R + 16*((q%(R/16)) ^ w) + j%16, channel 2j in the
+ *     low nibble;
  *     scale [d/128][64][8]: block j of token t at ((j/8)*64 + t)*8 + j%8.
+ *   Index-key layout (index keys, d_index = 128): data [64][64]: channel pair j
+ *     of token t at t*64 + 16*((j/16) ^ (t & 3)) + j%16; scales as K.
  *   V-layout (V):
  *     data  [8][d][4]: channel c of token t is nibble t%8 of the little-endian
  *           32-bit word (t/8)*d + c;
@@ -93,7 +98,7 @@ typedef struct {
   float ts_v;
 } pkv_kv_cache;
 
-/* Paged NVFP4 index keys (d_index channels, K-layout). */
+/* Paged NVFP4 index keys (d_index channels, index-key layout). */
 typedef struct {
   uint8_t* data;      /* [num_pages][64*d_index/2] */
   uint8_t* scale;     /* [num_pages][64*d_index/16] */
@@ -142,7 +147,7 @@ pkv_status pkv_append_kv(pkv_ctx* ctx, const float* k_new, const float* v_new,
                          const pkv_kv_cache* cache, const int32_t* page_table,
                          int max_pages, void* stream);
 
-/* Same quantize + append for index keys (float32 [n][d_index], K-layout). */
+/* Same quantize + append for index keys (float32 [n][d_index], index-key layout). */
 pkv_status pkv_append_index(pkv_ctx* ctx, const float* k_idx_new, const int32_t* seq_idx,
                             const int32_t* pos, int n, const pkv_idx_cache* icache,
                             const int32_t* page_table, int max_pages, void* stream);
@@ -189,7 +194,14 @@ pkv_status pkv_score_topk_cand(pkv_ctx* ctx, const uint8_t* q_idx, float tq, con
  *             window entries [0, win_len[b]);
  *   z = softmax_scale * q.k_hat, O = softmax(z) . v_hat, LSE = ln sum exp z,
  *   k_hat/v_hat the exact dequantized values.  Writes out float32 [B][H][d]
- *   and out_lse float32 [B][H] (may be NULL). */
+ *   and out_lse float32 [B][H] (may be NULL).
+ * The contraction with the NVFP4 keys runs on block-scaled FP4 tensor cores:
+ * q enters it as four FP4 terms per head, sigma_h * sum_t c_t 8^-t with c_t
+ * E2M1 codes and sigma_h = max_i |q_h,i| / 4 (error at most sigma_h * 8^-3 / 2
+ * per channel); the contraction with the FP8 window keys takes q as two E4M3
+ * terms scaled by a power of two per head (exact for a bf16 q).
+ * PKV_ERR_UNSUPPORTED when win->tw_v / cache->ts_v lies outside [2^-7, 2^7]
+ * (the window's V scale is folded into the f16 softmax weights). */
 pkv_status pkv_decode_attn(pkv_ctx* ctx, const void* q_bf16, const pkv_kv_cache* cache,
                            const int32_t* page_table, int max_pages, const int32_t* seq_len,
                            int B, const int32_t* sel_idx, int k, const pkv_window* win,
@@ -217,8 +229,10 @@ typedef struct {
  *   out_fp8 uint8 [B][H][d] = E4M3(fp32(O' / out_scale)) (nearest, ties to
  *   even, saturating at 448, sign kept);
  *   out float32 [B][H][d] = O' and out_lse float32 [B][H] when not NULL.
- * Channels outside the rotated part pass through.  q' enters the tensor-core
- * contraction rounded to f16.  A position outside [0, max_pos) sets the error
+ * Channels outside the rotated part pass through.  q' (rotated in FP32) enters
+ * the contractions as the terms of pkv_decode_attn (four FP4 terms; two E4M3
+ * terms for the window, about bf16 precision for a rotated q').  A position
+ * outside [0, max_pos) sets the error
  * word (PKV_ERR_BAD_PAGE: an index out of range) and that row is not rotated.
  * Workspace as pkv_decode_attn.  PKV_ERR_UNSUPPORTED unless the tensor-core
  * kernel takes the shape (n_heads <= 64; tw_v / ts_v within [2^-7, 2^7]). */
@@ -233,7 +247,8 @@ pkv_status pkv_decode_attn_fused(pkv_ctx* ctx, const void* q_bf16, const pkv_kv_
  * (q bf16 [B][128][n_heads][d], position s_b + r) attends the global tokens
  * [0, s_b) and the chunk-window entries [0, r] (chunk_win->k/v [B][128][d]:
  * FP8 K/V of positions s_b..H_b-1; win_len ignored).
- * Writes out float32 [B][128][H][d], out_lse float32 [B][128][H] (may be NULL). */
+ * Writes out float32 [B][128][H][d], out_lse float32 [B][128][H] (may be NULL).
+ * Query terms and PKV_ERR_UNSUPPORTED as pkv_decode_attn. */
 pkv_status pkv_replay_attn(pkv_ctx* ctx, const void* q_bf16, const pkv_kv_cache* cache,
                            const int32_t* page_table, int max_pages, const int32_t* prefix_len,
                            int B, const pkv_window* chunk_win, float softmax_scale,
@@ -279,11 +294,23 @@ pkv_status pkv_decode_attn_noalloc(pkv_ctx* ctx, const void* q_bf16, const pkv_k
  * kernel (attention, or index scoring) and `stop` right after it, then forgets
  * them.
  * pkv_launch_count: number of kernels this context has launched so far.
- * pkv_attn_path: kernel family of the last attention call: 1 = CUDA-core
- * split-K path, 2 = tensor-core (tcgen05) path, 0 = none yet. */
+ * pkv_attn_path: 2 once an attention call has launched the tensor-core
+ * (tcgen05) kernels on this context, 0 before (there is no other path). */
 pkv_status pkv_set_profile_events(pkv_ctx* ctx, void* start, void* stop);
 long long pkv_launch_count(const pkv_ctx* ctx);
 int pkv_attn_path(const pkv_ctx* ctx);
+
+/* Testing aid for the failure path (no counterpart in the pages).  Every wait
+ * of the attention kernel on another of its roles (a copy landing, an MMA
+ * completing, a buffer freed) gives up after wait_limit_cycles SM cycles
+ * (default 2^31, about a second): the kernel then records PKV_ERR_TIMEOUT in
+ * the error word, stops its roles, waits (bounded the same way) for the copies
+ * and MMAs it has in flight, frees its tensor memory and returns.  skip_copy
+ * >= 0 makes CTA 0 of the next attention calls leave out its K-tile copy
+ * number skip_copy (counted from 0 in the CTA's issue order), so that the wait
+ * for it runs out; -1 restores normal operation.  PKV_ERR_INVALID_ARG for a
+ * limit below 1000 cycles or skip_copy < -1. */
+pkv_status pkv_set_test_hooks(pkv_ctx* ctx, long long wait_limit_cycles, int skip_copy);
 
 #ifdef __cplusplus
 }

@@ -87,6 +87,28 @@ def rope(x, cos, sin, rope_dim: int, inverse: bool = False):
     return y
 
 
+def rope_query_bf16(q, cos, sin, rope_dim: int):
+    """The rotated query of a fused decode as the contraction receives it: the
+    rotation of ``rope`` computed in float32, each product and the difference /
+    sum rounded separately (y0 = fp32(fp32(x0 c) - fp32(x1 s)), y1 =
+    fp32(fp32(x0 s) + fp32(x1 c)), c and s the table's float32 values), then
+    rounded to bf16 (nearest, ties to even): the rotated query is a bf16 tensor
+    like the query itself.  q [..., d] holds float32-exact values; returns
+    float64."""
+    F32 = np.float32
+    y = np.array(q, dtype=F32, copy=True)
+    if rope_dim:
+        d = y.shape[-1]
+        c = np.asarray(cos, F32)
+        s = np.asarray(sin, F32)
+        x0 = y[..., d - rope_dim::2].copy()
+        x1 = y[..., d - rope_dim + 1::2].copy()
+        y[..., d - rope_dim::2] = (x0 * c).astype(F32) - (x1 * s).astype(F32)
+        y[..., d - rope_dim + 1::2] = (x0 * s).astype(F32) + (x1 * c).astype(F32)
+    from . import formats
+    return formats.f32_to_bf16(y)
+
+
 def merge(Oa, La, Ob, Lb):
     """LSE merge: lse = ln(e^La + e^Lb), O = e^(La-lse) Oa + e^(Lb-lse) Ob.
     A part with LSE = -inf has weight 0; both empty gives O = 0, LSE = -inf."""

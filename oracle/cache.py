@@ -20,17 +20,21 @@ class Pools:
 
     def __init__(self, num_pages: int, d: int, kind: str):
         self.d = d
-        self.kind = kind  # "k" (K-layout) or "v" (V-layout)
+        self.kind = kind  # "k" (K-layout), "v" (V-layout) or "i" (index-key layout, d = 128)
+        assert kind in ("k", "v", "i") and (kind != "i" or d == 128)
         self.data = np.zeros((num_pages, LY.k_data_bytes(d)), np.uint8)
         self.scale = np.zeros((num_pages, LY.k_scale_bytes(d)), np.uint8)
 
     def store(self, page, slots, codes, scales):
-        f = LY.store_k_page if self.kind == "k" else LY.store_v_page
-        f(self.data, self.scale, page, slots, codes, scales)
+        if self.kind == "v":
+            LY.store_v_page(self.data, self.scale, page, slots, codes, scales)
+        else:
+            LY.store_k_page(self.data, self.scale, page, slots, codes, scales, index_keys=self.kind == "i")
 
     def load(self, page):
-        f = LY.load_k_page if self.kind == "k" else LY.load_v_page
-        return f(self.data, self.scale, page, self.d)
+        if self.kind == "v":
+            return LY.load_v_page(self.data, self.scale, page, self.d)
+        return LY.load_k_page(self.data, self.scale, page, self.d, index_keys=self.kind == "i")
 
 
 def tensor_scales(wl: W.Workload, sample_pages: int = 64):
@@ -125,7 +129,8 @@ def expected_decode_fused(wl: W.Workload, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b: int
                           out_scale, pos=None, sel=None, heads=None, scale=None):
     """Fused decode of sequence b ([blog] "MegaAttention avec KV compressé NVFP4":
     query RoPE, attention, inverse RoPE on the output and FP8 conversion in one
-    pass): q' = rope(q, pos), (O, LSE) = attention of q' over global + window
+    pass): q' = rope(q, pos) in float32 rounded to bf16 (``rope_query_bf16``),
+    (O, LSE) = attention of q' over global + window
     (all L_b tokens, or the positions ``sel`` when given), O' = rope^-1(O, pos),
     codes = E4M3(fp32(fp32(O') / out_scale)).  ``table`` float32 [max_pos][rope_dim]:
     cosines then sines per position.  Returns (O' float64, LSE, codes uint8)."""
@@ -149,6 +154,7 @@ def expected_decode_fused(wl: W.Workload, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b: int
     q = F.bf16_to_f64(wl.q_bits_seq(b))
     if heads is not None:
         q = q[heads]
-    O, lse = A.decode(A.rope(q, cos, sin, rope_dim), K, V, Kw, Vw, scale)
+    O, lse = A.decode(A.rope_query_bf16(q, table[p][:rope_dim // 2], table[p][rope_dim // 2:rope_dim], rope_dim),
+                      K, V, Kw, Vw, scale)
     Or = A.rope(O, cos, sin, rope_dim, inverse=True)
     return Or, lse, F.fp8_quantize(Or, out_scale)

@@ -154,3 +154,12 @@ def bf16_to_f64(bits) -> np.ndarray:
     float32 whose upper 16 bits are the pattern and whose lower 16 bits are 0."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+def f32_to_bf16(x) -> np.ndarray:
+    """float32 -> nearest bf16 value (ties to the even significand), returned as
+    float64: keep the upper 16 bits of the float32 pattern after adding half of
+    the dropped range (0x7FFF) plus the lowest kept bit (finite inputs)."""
+    u = np.ascontiguousarray(np.asarray(x, dtype=F32)).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)

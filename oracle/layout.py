@@ -5,12 +5,20 @@ The pages fix only that the global KV is stored in FP4 and paged ([blog]
 this library's definition, chosen so that a 64-token page is a few contiguous
 runs of bytes.  Written out here address by address:
 
-K-layout (K and the 128-wide index keys), d channels, s = min(8, d/32) - 1:
-  data  [64 tokens][d/2 bytes]: channel pair (2j, 2j+1) of token t sits in
-        byte   t*(d/2) + 16*((j div 16) XOR (t AND s)) + (j mod 16),
-        channel 2j in the low nibble, 2j+1 in the high nibble.
+K-layout (the K cache), d channels: a token's d/2 code bytes are cut into
+  column blocks of R = min(128, d/2) bytes, stored [d/(2R) blocks][64 tokens][R
+  bytes]; inside a block the 16-byte chunk c of token t is stored at chunk
+  position c XOR w(t), w(t) = t mod 8 when R = 128 and (t div 2) mod 4 when
+  R = 64 (the K-major operand layouts with the 128- and 64-byte swizzle of a
+  block-scaled FP4 tensor-core contraction, so that a page is read as is):
+  data  channel pair (2j, 2j+1) of token t sits in byte
+        (q div (R/16))*64*R + t*R + 16*((q mod (R/16)) XOR w(t)) + (j mod 16),
+        q = j div 16, channel 2j in the low nibble, 2j+1 in the high nibble.
   scale [d/128 groups][64 tokens][8 bytes]: the scale of block j (channels
         16j..16j+15) of token t sits in byte ((j div 8)*64 + t)*8 + (j mod 8).
+Index-key layout (the 128-wide index keys): data [64 tokens][64 bytes], channel
+  pair j of token t in byte t*64 + 16*((j div 16) XOR (t AND 3)) + (j mod 16);
+  scales as the K-layout.
 V-layout (V), d channels:
   data  [8 octets][d channels][4 bytes]: channel ch of token t is nibble
         (t mod 8) of the little-endian 32-bit word ((t div 8)*d + ch), i.e.
@@ -38,8 +46,14 @@ v_scale_bytes = k_scale_bytes
 
 
 def _k_data_addr(t: int, j: int, d: int) -> int:
-    s = min(8, d // 32) - 1
-    return t * (d // 2) + 16 * ((j // 16) ^ (t & s)) + (j % 16)
+    R = min(128, d // 2)
+    w = t % 8 if R == 128 else (t // 2) % 4
+    q = j // 16
+    return (q // (R // 16)) * PAGE * R + t * R + 16 * ((q % (R // 16)) ^ w) + (j % 16)
+
+
+def _i_data_addr(t: int, j: int) -> int:
+    return t * 64 + 16 * ((j // 16) ^ (t & 3)) + (j % 16)
 
 
 def _k_scale_addr(t: int, j: int) -> int:
@@ -54,19 +68,24 @@ def _v_scale_addr(t: int, j: int) -> int:
     return j * PAGE + t
 
 
-def store_k_token(data_pool, scale_pool, page, t, codes, scales):
-    """Write one token's NVFP4 codes [d] (0..15) and scale bytes [d/16] into page ``page``, slot ``t``."""
+def _data_addr(t: int, j: int, d: int, index_keys: bool) -> int:
+    return _i_data_addr(t, j) if index_keys else _k_data_addr(t, j, d)
+
+
+def store_k_token(data_pool, scale_pool, page, t, codes, scales, index_keys=False):
+    """Write one token's NVFP4 codes [d] (0..15) and scale bytes [d/16] into page
+    ``page``, slot ``t`` (K-layout, or the index-key layout when ``index_keys``)."""
     d = len(codes)
     for j in range(d // 2):
-        data_pool[page, _k_data_addr(t, j, d)] = (int(codes[2 * j]) & 0xF) | ((int(codes[2 * j + 1]) & 0xF) << 4)
+        data_pool[page, _data_addr(t, j, d, index_keys)] = (int(codes[2 * j]) & 0xF) | ((int(codes[2 * j + 1]) & 0xF) << 4)
     for j in range(d // 16):
         scale_pool[page, _k_scale_addr(t, j)] = scales[j]
 
 
-def load_k_token(data_pool, scale_pool, page, t, d):
+def load_k_token(data_pool, scale_pool, page, t, d, index_keys=False):
     codes = np.empty(d, np.uint8)
     for j in range(d // 2):
-        b = int(data_pool[page, _k_data_addr(t, j, d)])
+        b = int(data_pool[page, _data_addr(t, j, d, index_keys)])
         codes[2 * j] = b & 0xF
         codes[2 * j + 1] = b >> 4
     scales = np.array([scale_pool[page, _k_scale_addr(t, j)] for j in range(d // 16)], np.uint8)
@@ -97,11 +116,20 @@ def load_v_token(data_pool, scale_pool, page, t, d):
 # ---- vectorized forms of the same formulas (used on whole pages) -------------
 
 def k_data_index(d: int) -> np.ndarray:
-    """[64][d/2] byte address of channel pair j of token t (formula above)."""
+    """[64][d/2] byte address of channel pair j of token t (K-layout formula above)."""
     t = np.arange(PAGE)[:, None]
     j = np.arange(d // 2)[None, :]
-    s = min(8, d // 32) - 1
-    return t * (d // 2) + 16 * ((j // 16) ^ (t & s)) + (j % 16)
+    R = min(128, d // 2)
+    w = t % 8 if R == 128 else (t // 2) % 4
+    q = j // 16
+    return (q // (R // 16)) * PAGE * R + t * R + 16 * ((q % (R // 16)) ^ w) + (j % 16)
+
+
+def i_data_index() -> np.ndarray:
+    """[64][64] byte address of channel pair j of token t of a 128-wide index key."""
+    t = np.arange(PAGE)[:, None]
+    j = np.arange(64)[None, :]
+    return t * 64 + 16 * ((j // 16) ^ (t & 3)) + (j % 16)
 
 
 def k_scale_index(d: int) -> np.ndarray:
@@ -123,18 +151,20 @@ def v_scale_index(d: int) -> np.ndarray:
     return j * PAGE + t
 
 
-def store_k_page(data_pool, scale_pool, page, slots, codes, scales):
-    """Write tokens at ``slots`` of page ``page``: codes [n][d], scales [n][d/16]."""
+def store_k_page(data_pool, scale_pool, page, slots, codes, scales, index_keys=False):
+    """Write tokens at ``slots`` of page ``page``: codes [n][d], scales [n][d/16]
+    (K-layout, or the index-key layout when ``index_keys``)."""
     d = codes.shape[1]
     slots = np.asarray(slots)
     packed = (codes[:, 0::2] & 0xF) | ((codes[:, 1::2] & 0xF) << 4)
-    data_pool[page, k_data_index(d)[slots]] = packed.astype(np.uint8)
+    idx = i_data_index() if index_keys else k_data_index(d)
+    data_pool[page, idx[slots]] = packed.astype(np.uint8)
     scale_pool[page, k_scale_index(d)[slots]] = scales
 
 
-def load_k_page(data_pool, scale_pool, page, d):
+def load_k_page(data_pool, scale_pool, page, d, index_keys=False):
     """codes [64][d], scales [64][d/16] of a whole page."""
-    b = data_pool[page][k_data_index(d)]
+    b = data_pool[page][i_data_index() if index_keys else k_data_index(d)]
     codes = np.empty((PAGE, d), np.uint8)
     codes[:, 0::2] = b & 0xF
     codes[:, 1::2] = b >> 4

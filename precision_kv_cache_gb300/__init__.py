@@ -108,6 +108,7 @@ def lib() -> ctypes.CDLL:
             "pkv_set_profile_events": (i, [vp, vp, vp]),
             "pkv_decode_attn_noalloc": (i, [vp, vp, ctypes.POINTER(_KVCache), vp, i, vp, i, vp, i,
                                             ctypes.POINTER(_Window), f, vp, vp, vp]),
+            "pkv_set_test_hooks": (i, [vp, ctypes.c_longlong, i]),
             "pkv_launch_count": (ctypes.c_longlong, [vp]),
             "pkv_attn_path": (i, [vp]),
         }
@@ -313,11 +314,15 @@ class Context:
         _check(lib().pkv_set_profile_events(self.h, ctypes.c_void_p(start.cuda_event),
                                             ctypes.c_void_p(stop.cuda_event)), "pkv_set_profile_events")
 
+    def pkv_set_test_hooks(self, wait_limit_cycles: int = 1 << 31, skip_copy: int = -1):
+        """Testing aid: bounded-wait limit (SM cycles) and a K-tile copy CTA 0 leaves out (-1 = none)."""
+        _check(lib().pkv_set_test_hooks(self.h, wait_limit_cycles, skip_copy), "pkv_set_test_hooks")
+
     def pkv_launch_count(self) -> int:
         return int(lib().pkv_launch_count(self.h))
 
     def pkv_attn_path(self) -> int:
-        """1 = CUDA-core attention path, 2 = tensor-core path (last attention call)."""
+        """2 once an attention call has launched the tensor-core kernels, 0 before."""
         return int(lib().pkv_attn_path(self.h))
 
     def workspace(self, op: int, batch: int, max_len: int) -> torch.Tensor:

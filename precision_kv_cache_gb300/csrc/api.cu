@@ -20,7 +20,9 @@ struct pkv_ctx {
   cudaEvent_t prof_start = nullptr;   // one-shot events around the next attention or scoring kernel
   cudaEvent_t prof_stop = nullptr;
   long long launches = 0;
-  int last_path = 0;                  // 1 = CUDA-core attention, 2 = tensor-core attention
+  int last_path = 0;                  // 2 = tensor-core attention ran (0 = no attention call yet)
+  long long wait_limit = 1LL << 31;   // cycles a device-side bounded wait may take
+  int hook_skip_copy = -1;            // testing aid: K-tile copy left out by the attention kernel
 };
 
 namespace {
@@ -58,28 +60,8 @@ bool valid_window(const pkv_window* w) {
   return (w->tw_k > 0.f && w->tw_k < INFINITY && w->tw_v > 0.f && w->tw_v < INFINITY);
 }
 
-// Split policy of the CUDA-core attention path: enough (split, head group,
-// query row) units to give every SM several blocks, splits of >= 256 entries.
-void choose_split(const pkv_ctx* c, int n_groups, int max_entries, int* n_split, int* chunk) {
-  const int hg = (c->cfg.n_heads + 7) / 8;
-  const long long units = (long long)n_groups * hg;
-  const long long target = 4LL * c->num_sms;
-  int ns = (int)std::max<long long>(1, (target + units - 1) / units);
-  const int max_ns = std::max(1, (max_entries + 255) / 256);
-  ns = std::min(ns, max_ns);
-  int ch = (max_entries + ns - 1) / ns;
-  ch = std::max(64, (ch + 63) / 64 * 64);
-  *chunk = ch;
-  *n_split = std::max(1, (max_entries + ch - 1) / ch);
-}
-
 size_t attn_ws_bytes(const pkv_ctx* c, int n_groups, int max_entries) {
-  int ns, ch;
-  choose_split(c, n_groups, max_entries, &ns, &ch);
-  const size_t H = c->cfg.n_heads, D = c->cfg.d;
-  size_t simple = (size_t)n_groups * ns * H * (D + 1) * 4 + 256;
-  size_t tc = pkv_attn_tc_ws_bytes(c->num_sms, c->cfg.n_heads, c->cfg.d, n_groups, max_entries);
-  return std::max(simple, tc);
+  return pkv_attn_tc_ws_bytes(c->num_sms, c->cfg.n_heads, c->cfg.d, n_groups, max_entries);
 }
 
 }  // namespace
@@ -264,31 +246,19 @@ pkv_status pkv_score_topk_cand(pkv_ctx* c, const uint8_t* q_idx, float tq, const
 
 static pkv_status run_attention(pkv_ctx* c, pkv::AttnArgs& a, int max_entries, float* out, float* out_lse,
                                 void* ws, size_t ws_bytes, cudaStream_t st) {
+  // one kernel family: shapes outside it are refused, never sent elsewhere
+  if (!pkv_attn_tc_supported(a, c->cfg.d)) return PKV_ERR_UNSUPPORTED;
   const size_t need = attn_ws_bytes(c, a.n_groups, max_entries);
   if (!ws || ws_bytes < need || !aligned16(ws)) return PKV_ERR_WORKSPACE;
-  // the tensor-core kernel takes the dense cases it supports
+  a.wait_limit = c->wait_limit;
+  a.hook_skip_copy = c->hook_skip_copy;
   cudaEvent_t e0 = c->prof_start, e1 = c->prof_stop;
   c->prof_start = c->prof_stop = nullptr;
-  if (pkv_attn_tc_supported(a, c->cfg.d)) {
-    int nl = 0;
-    cudaError_t e = pkv_launch_attn_tc(a, c->num_sms, max_entries, out, out_lse, ws, st, e0, e1, &nl);
-    c->launches += nl;
-    c->last_path = 2;
-    return cuda_status(e);
-  }
-  int ns, ch;
-  choose_split(c, a.n_groups, max_entries, &ns, &ch);
-  a.n_split = ns;
-  a.chunk = ch;
-  a.part_o = (float*)ws;
-  a.part_lse = (float*)((uint8_t*)ws + (size_t)a.n_groups * ns * a.H * a.D * 4);
-  c->last_path = 1;
-  if (e0 && e1) cudaEventRecord(e0, st);
-  cudaError_t e = pkv_launch_attn_simple(c->cfg.d, a, st);
-  if (e0 && e1) cudaEventRecord(e1, st);
-  c->launches += 2;
-  if (e != cudaSuccess) return PKV_ERR_CUDA;
-  return cuda_status(pkv_launch_merge_splits(a.part_o, a.part_lse, ns, a.n_groups, a.H, a.D, out, out_lse, st));
+  int nl = 0;
+  cudaError_t e = pkv_launch_attn_tc(a, c->num_sms, max_entries, out, out_lse, ws, st, e0, e1, &nl);
+  c->launches += nl;
+  c->last_path = 2;
+  return cuda_status(e);
 }
 
 pkv_status pkv_decode_attn(pkv_ctx* c, const void* q, const pkv_kv_cache* cache, const int32_t* page_table,
@@ -322,6 +292,11 @@ pkv_status pkv_decode_attn(pkv_ctx* c, const void* q, const pkv_kv_cache* cache,
   a.n_groups = B;
   a.replay = 0;
   a.err = c->d_err;
+  {
+    pkv::AttnArgs chk = a;
+    chk.sel = nullptr;
+    if (!pkv_attn_tc_supported(chk, c->cfg.d)) return PKV_ERR_UNSUPPORTED;
+  }
   if (sel_idx) {
     // the selected tokens are gathered into compact pages, then attended as a dense segment
     const size_t need = pkv_workspace_bytes(c, PKV_OP_DECODE_SPARSE, B, k);
@@ -466,6 +441,13 @@ pkv_status pkv_get_error(pkv_ctx* c, void* stream) {
   if (cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
   if (h & PKV_DEVERR_TIMEOUT) return PKV_ERR_TIMEOUT;
   if (h & PKV_DEVERR_BAD_PAGE) return PKV_ERR_BAD_PAGE;
+  return PKV_OK;
+}
+
+pkv_status pkv_set_test_hooks(pkv_ctx* c, long long wait_limit_cycles, int skip_copy) {
+  if (!c || wait_limit_cycles < 1000 || skip_copy < -1) return PKV_ERR_INVALID_ARG;
+  c->wait_limit = wait_limit_cycles;
+  c->hook_skip_copy = skip_copy;
   return PKV_OK;
 }
 

@@ -12,7 +12,8 @@
 namespace pkv {
 
 // One warp per (entry, tensor): lane handles 16-channel blocks lane, lane+32, ...
-template <int D, bool V_LAYOUT>
+// LAYOUT: 0 = K cache (KLayout), 1 = V cache (VLayout), 2 = index keys (IdxLayout).
+template <int D, int LAYOUT>
 __device__ __forceinline__ void quantize_store_token(const float* __restrict__ x, float ts,
                                                      uint8_t* __restrict__ data,
                                                      uint8_t* __restrict__ scale, int t, int lane) {
@@ -38,14 +39,15 @@ __device__ __forceinline__ void quantize_store_token(const float* __restrict__ x
 #pragma unroll
       for (int e = 0; e < 16; ++e) code[e] = e2m1_code(__fdiv_rn(v[e], den));
     }
-    if (!V_LAYOUT) {
+    if (LAYOUT != 1) {
       uint32_t lo = 0u, hi = 0u;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         lo |= (code[2 * q] | (code[2 * q + 1] << 4)) << (8 * q);
         hi |= (code[8 + 2 * q] | (code[8 + 2 * q + 1] << 4)) << (8 * q);
       }
-      *reinterpret_cast<uint2*>(data + KLayout<D>::data(t, 8 * j)) = make_uint2(lo, hi);
+      const int off = LAYOUT == 2 ? IdxLayout::data(t, 8 * j) : KLayout<D>::data(t, 8 * j);
+      *reinterpret_cast<uint2*>(data + off) = make_uint2(lo, hi);
       scale[KLayout<D>::scale(t, j)] = (uint8_t)S;
     } else {
       uint32_t* w = reinterpret_cast<uint32_t*>(data);
@@ -88,10 +90,10 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
   if (!locate(seq_idx, pos, i, page_table, max_pages, cache.num_pages, err, &page, &slot)) return;
   const size_t pd = (size_t)page * (PKV_PAGE * D / 2), ps = (size_t)page * (PKV_PAGE * D / 16);
   if ((warp & 1) == 0)
-    quantize_store_token<D, false>(k_new + (size_t)i * D, cache.ts_k, cache.k_data + pd,
+    quantize_store_token<D, 0>(k_new + (size_t)i * D, cache.ts_k, cache.k_data + pd,
                                    cache.k_scale + ps, slot, lane);
   else
-    quantize_store_token<D, true>(v_new + (size_t)i * D, cache.ts_v, cache.v_data + pd,
+    quantize_store_token<D, 1>(v_new + (size_t)i * D, cache.ts_v, cache.v_data + pd,
                                   cache.v_scale + ps, slot, lane);
 }
 
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(256) append_index_kernel(
   if (i >= n) return;
   int page, slot;
   if (!locate(seq_idx, pos, i, page_table, max_pages, ic.num_pages, err, &page, &slot)) return;
-  quantize_store_token<D, false>(x + (size_t)i * D, ic.ts, ic.data + (size_t)page * (PKV_PAGE * D / 2),
+  quantize_store_token<D, 2>(x + (size_t)i * D, ic.ts, ic.data + (size_t)page * (PKV_PAGE * D / 2),
                                  ic.scale + (size_t)page * (PKV_PAGE * D / 16), slot, lane);
 }
 

@@ -1,6 +1,5 @@
 // Arguments of one attention launch over (global NVFP4 segment, FP8 window
-// segment) for a set of query rows, shared by the CUDA-core and tensor-core
-// attention kernels.
+// segment) for a set of query rows.
 #pragma once
 #include "pkv_common.cuh"
 
@@ -23,12 +22,10 @@ struct AttnArgs {
   int D;
   int n_groups;               // query rows: B (decode) or B*128 (replay)
   int replay;
-  int n_split;
-  int chunk;                  // entries per split
-  float* part_o;              // [n_groups][n_split][H][D]
-  float* part_lse;            // [n_groups][n_split][H]
   int* err;
-  // fused decode (tensor-core path only): query rotation before QK, inverse
+  long long wait_limit;       // cycles a bounded wait may take before the kernel gives up
+  int hook_skip_copy;         // testing aid: the K-tile copy with this index (CTA 0) is never issued; -1 = none
+  // fused decode: query rotation before QK, inverse
   // rotation of O and its FP8 encoding in the merge; rope_dim 0 = none
   const int32_t* rope_pos;    // [n_groups] row of cos_sin of each query row
   const float* cos_sin;       // [max_pos][rope_dim]: cosines, then sines

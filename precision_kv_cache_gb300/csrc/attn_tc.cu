@@ -1,5 +1,5 @@
 // Tensor-core decode / replay attention over the paged NVFP4 global KV and the
-// FP8 window, for sm_103a (tcgen05 MMA with TMEM operands and accumulators).
+// FP8 window, for sm_103a (tcgen05 MMA, block-scaled FP4 for QK^T, TMEM).
 //
 // What it computes: for every query row g (a decode sequence, or one replayed
 // token), all H <= 64 query heads attend the same K/V (MQA over one shared
@@ -11,34 +11,39 @@
 // Output: a normalized partial (O, LSE) per (CTA, query row) segment, merged
 // by merge_tc_kernel ("flash-decoding": split along the sequence + LSE merge).
 //
-// Design (one persistent CTA per SM, 896 threads, warp-specialized):
+// Design (one persistent CTA per SM, 768 threads, warp-specialized):
 //   * work = 128-token tiles; each query row has ceil(L/128) NVFP4 tiles plus
 //     one window tile; the concatenated tile list is cut into one contiguous
 //     range per CTA (balanced to one tile).
-//   * warps 24 (K) and 26 (V) stream the raw pages of each tile (codes +
-//     scales) into two shared-memory page rings with 1-D bulk copies (TMA).
-//   * warps 0-7 (thread = token) dequantize K to f16 (exact: E2M1 x E4M3 has
-//     <= 6 significant bits) into TMEM, 64 channels at a time: the A operand
-//     of S^T = K Q^T  (M = 128 tokens, N = 64 heads, K = d).  Two groups of
-//     four warps (one per TMEM lane quarter) take alternate chunks.
-//   * warps 8-15 (thread = channel) dequantize V^T to f16 into TMEM, 128
-//     channels x 64 tokens at a time: the A operand of O^T = V^T P (M = 128
-//     channels, N = 64 heads, K = tokens); two groups of four warps take
-//     alternate chunks.  Each warp converts the E4M3 block scales of its
-//     chunk once (two per lane) and shares them through shared memory.
-//   * warp 25 issues the QK MMAs, warp 27 the PV MMAs (Q and P are the
-//     shared-memory B operands).
-//   * warps 16-23 run the online softmax on S (FP32, exp2, lazy max update
-//     with threshold 2^8), write P (f16, shared memory) and finally normalize
-//     O and write the partial result.
+//   * S^T = K Q^T (M = 128 tokens, N = 64 heads) runs on the block-scaled FP4
+//     tensor-core contraction: A = the two K pages of a tile as stored (E2M1
+//     codes, K-major with the 128/64-byte swizzle), their E4M3 block scales in
+//     TMEM (written by warps 0-3, thread = tile row), B = the query written as a
+//     sum of NQT FP4 terms, q ~ sigma_h * sum_t c_t 8^-t (c_t E2M1 codes, one
+//     factor sigma_h per head applied to the logits; the term weights 8^-t are
+//     the constant B block scales).  No K dequantization.
+//   * the window tile's S^T runs on the FP8 contraction: A = the window K codes
+//     (E4M3, copied by TMA with the 128-byte swizzle), B = the query as two E4M3
+//     terms with a power-of-two factor per head (exact for a bf16 query).
+//   * warp 22 streams V pages into a shared-memory ring; warps 4-11 dequantize
+//     V^T to f16 into TMEM (thread = channel, 128 channels x 64 tokens at a
+//     time: the A operand of O^T = V^T P, M = 128 channels, N = 64 heads); warp
+//     23 issues the PV MMAs (P f16 in shared memory, B operand).
+//   * warps 12-19 run the online softmax on S (FP32, exp2, lazy max update with
+//     threshold 2^8), write P (f16), normalize O and write the partial result;
+//     at a row's start (and before its window tile) they also write the
+//     query's FP4 (or E4M3) terms into shared memory.
 //   * fused decode ("MegaAttention avec KV compressé NVFP4": query RoPE,
-//     attention, inverse RoPE on the output, FP8 output in one pass): the Q
-//     load turns the rotary pairs of each query before its f16 rounding, and
-//     the merge turns the final O back and encodes it as E4M3 - no extra
-//     kernel and no extra pass over O.
+//     attention, inverse RoPE on the output, FP8 output in one pass): the query
+//     is turned before it is split into terms, and the merge turns the final O
+//     back and encodes it as E4M3 - no extra kernel and no extra pass over O.
 // Every wait is bounded; on a timeout the CTA sets the error word, stops all
 // roles, drains its own copies / MMAs and frees its TMEM before returning.
 #include <cstddef>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "attn_tc.h"
 #include "launch.h"
 #include "tc_ptx.cuh"
@@ -48,71 +53,81 @@ namespace tcattn {
 
 constexpr int TILE = 128;
 constexpr int NH = 64;                 // MMA N: query heads (zero-padded)
-constexpr int NTHREADS = 896;       // 28 warps
+constexpr int NQT = 5;                 // FP4 terms of the query
+constexpr int NTHREADS = 768;          // 24 warps
 // warp roles
-constexpr int W_KDEQ = 0;              // 8 warps: K dequantizers
-constexpr int W_VDEQ = 8;              // 8 warps: V dequantizers
-constexpr int W_SMAX = 16;             // 8 warps: softmax + epilogue
-constexpr int W_KPROD = 24;            // K page producer
-constexpr int W_MMA = 25;              // QK MMA issuer, TMEM owner
-constexpr int W_VPROD = 26;            // V page producer
-constexpr int W_MMA2 = 27;             // PV MMA issuer
-constexpr uint32_t NDEQ = 8;           // arrivals per K (V) page release: one per dequant warp
-constexpr uint32_t NGRP = 4;           // arrivals per K (V) chunk: one per warp of a group
+constexpr int W_SF = 0;                // 4 warps: K block scales -> TMEM
+constexpr int W_VDEQ = 4;              // 8 warps: V dequantizers
+constexpr int W_SMAX = 12;             // 8 warps: softmax + epilogue + query terms
+constexpr int W_KPROD = 20;            // K tile producer
+constexpr int W_QK = 21;               // QK MMA issuer, TMEM owner
+constexpr int W_VPROD = 22;            // V page producer
+constexpr int W_PV = 23;               // PV MMA issuer
+constexpr uint32_t NDEQ = 8;           // arrivals per V page release: one per dequant warp
+constexpr uint32_t NGRP = 4;           // arrivals per V chunk: one per warp of a group
 constexpr float TAU = 8.f;             // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
 // TMEM columns (512 allocated)
-constexpr int NKS = 3;                 // K chunk slots
 constexpr int NVS = 3;                 // V chunk slots
-constexpr uint32_t COL_S = 0;          // S^T tile: 64 columns (fp32); the softmax copies it out at once
-constexpr uint32_t COL_K = 64;         // K chunk slots: NKS x 32 columns (64 channels, f16 pairs)
+constexpr uint32_t COL_S = 0;          // S^T tile: 64 columns (fp32)
+constexpr uint32_t COL_SFA = 64;       // K block scales: 2 buffers x 32 columns (4 per 64-channel K step)
+constexpr uint32_t COL_SFB = 128;      // query term weights: 4 columns per term
 constexpr uint32_t COL_V = 160;        // V^T chunk slots: NVS x 32 columns (64 tokens, f16 pairs)
 constexpr uint32_t COL_O = 256;        // O^T: 4 chunks x 64 columns
-static_assert(COL_K == COL_S + 64 && COL_V == COL_K + 32 * NKS && COL_O >= COL_V + 32 * NVS, "TMEM map");
+static_assert(COL_SFA + 64 <= COL_SFB && COL_SFB + 32 <= COL_V && COL_V + 32 * NVS <= COL_O, "TMEM map");
 
-constexpr int NKR = 4;                 // K ring: page slots (a tile holds two for its whole duration)
+constexpr int NKS = 2;                 // K tile slots (two pages each, or window chunks)
 constexpr int NVR = 3;                 // V ring: page slots (released page by page)
+constexpr int WCHUNK = 128 * 128;      // window K chunk: 128 entries x 128 channels of E4M3
 
 template <int D>
 struct Cfg {
+  static constexpr int RB = D / 2 < 128 ? D / 2 : 128;       // K code bytes of a row per column block
+  static constexpr int NCB = D / 2 / RB;                     // column blocks of a K row
+  static constexpr int KS = D / 64;                          // K steps of the FP4 contraction
   static constexpr int PAGE_DATA = PKV_PAGE * D / 2;
   static constexpr int PAGE_SCALE = PKV_PAGE * D / 16;
-  static constexpr int PSLOT = PAGE_DATA + PAGE_SCALE;            // one page of K (or V): codes + scales
-  static constexpr int Q_BYTES = NH * D * 2;
+  static constexpr int PSLOT = PAGE_DATA + PAGE_SCALE;       // one V page: codes + scales
+  static constexpr int QT_BYTES = NH * D / 2;                // one FP4 query term [NCB][64][RB]
+  static constexpr int QW_BYTES = NH * D;                    // one E4M3 query term [D/128][64][128]
+  static constexpr int Q_BYTES = NQT * QT_BYTES > 2 * QW_BYTES ? NQT * QT_BYTES : 2 * QW_BYTES;
   static constexpr int P_BYTES = TILE * NH * 2;
-  static constexpr int NKCH = D / 64;                             // K chunks of 64 channels
-  static constexpr int NVCH = D / 128;                            // V chunks of 128 channels
+  static constexpr int KSLOT = TILE * D / 2 > WCHUNK ? TILE * D / 2 : WCHUNK;
+  static constexpr int NWC = D / 128;                        // window K chunks
+  static constexpr int CPS = KSLOT / WCHUNK;                 // window chunks per K slot
+  static constexpr int NWS = (NWC + CPS - 1) / CPS;          // K slots one window tile uses
+  static constexpr int NVCH = D / 128;                       // V chunks of 128 channels
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_P = OFF_Q + Q_BYTES;                   // 2 P buffers
-  static constexpr int OFF_K = OFF_P + 2 * P_BYTES;               // K ring
-  static constexpr int OFF_V = OFF_K + NKR * PSLOT;               // V ring
-  static constexpr int DYN = OFF_V + NVR * PSLOT + 1024;          // + alignment slack
-  static_assert(OFF_K % 1024 == 0, "operand tiles stay 1024-aligned");
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;              // P (one buffer)
+  static constexpr int OFF_K = OFF_P + P_BYTES;              // K tile slots
+  static constexpr int OFF_V = OFF_K + NKS * KSLOT;          // V ring
+  static constexpr int DYN = OFF_V + NVR * PSLOT + 1024;     // + alignment slack
+  static_assert(QT_BYTES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_K % 1024 == 0 && KSLOT % 1024 == 0 &&
+                OFF_V % 16 == 0, "operand tiles stay 1024-aligned");
+  static_assert(KS * 4 <= 32, "K scales of a tile fit one 32-column buffer");
 };
 
 struct Shared {
-  uint64_t kr_full[NKR], kr_empty[NKR], vr_full[NVR], vr_empty[NVR];
-  uint64_t kfull[NKS], kempty[NKS], vfull[NVS], vempty[NVS];
-  uint64_t s_full, s_empty, p_full[2], p_empty[2], q_full, o_empty, drain, drain2;
+  uint64_t kr_full[NKS], kr_empty[NKS], vr_full[NVR], vr_empty[NVR];
+  uint64_t sfa_full[2], sfa_empty[2];
+  uint64_t vfull[NVS], vempty[NVS];
+  uint64_t s_full, s_empty, p_full, p_empty, q_full, o_empty, drain, drain2;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float m[NH];     // running max per head (log2 units)
-  float alpha[NH];             // rescale factor of the current tile
+  alignas(16) float alpha[NH];
+  alignas(16) float zsg[NH];   // logit factor per head of the global tiles (log2 units)
+  alignas(16) float zsw[NH];   // logit factor per head of the window tile (log2 units)
   float red[4][NH];            // cross-warp reductions
   alignas(16) uint32_t vsc[8][64];   // per V warp: f16x2 block-scale pairs of its current chunk (2 blocks x 32)
 };
-static_assert(offsetof(Shared, m) % 16 == 0 && offsetof(Shared, alpha) % 16 == 0 && offsetof(Shared, vsc) % 16 == 0,
+static_assert(offsetof(Shared, m) % 16 == 0 && offsetof(Shared, alpha) % 16 == 0 && offsetof(Shared, zsg) % 16 == 0 &&
+                  offsetof(Shared, zsw) % 16 == 0 && offsetof(Shared, vsc) % 16 == 0,
               "16-byte shared-memory vector accesses");
 
 // ---------------------------------------------------------------- schedule
-struct Sched {
-  const int* tile_start;       // [n_groups + 1]
-  int n_groups, G;
-  long long T;
-};
-
 __device__ __forceinline__ long long cta_start(long long T, int G, int c) { return (T * c) / G; }
 
 // first group whose tiles reach past x
@@ -187,13 +202,11 @@ __device__ __forceinline__ void fail(Shared& sh, int* err) {
   report(err, PKV_DEVERR_TIMEOUT);
 }
 
-
 __device__ __forceinline__ uint32_t f32_to_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-
 
 // 2^x, one approximate-unit instruction (relative error ~2^-22; 2^-inf = 0)
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -204,7 +217,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 // Sum of v[i] over the 32 lanes of the warp, by reduce-scatter: lane l returns
 // the total of entry (l >> 1) & 15 (the two lanes of a pair hold the same sum).
-__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
+__device__ __forceinline__ float warp_sum16(const float* v, int lane) {
   float a[8], b[4], c[2];
   const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4, u1 = lane & 2;
 #pragma unroll
@@ -220,70 +233,182 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
   return d + __shfl_xor_sync(0xffffffffu, d, 1);
 }
 
-// Q of query row g -> shared memory: f16 (from bf16; exact for |q| in [2^-14, 65504]),
-// K-major with the 128-byte swizzle, heads >= H zero.  Called by the 256 softmax threads.
-// Fused decode: the pairs (2i, 2i+1) of the last rope_dim channels are first turned
-// by the row's rotary angles (FP32, then rounded to f16).
+// TMEM store of the 4*KS scale columns of a K tile (32 lanes of one quarter)
+template <int KS>
+__device__ __forceinline__ void st_sfa(uint32_t taddr, const uint32_t* r) {
+  if constexpr (KS == 8) tc::tmem_st32(taddr, r);
+  else if constexpr (KS == 4) tc::tmem_st16(taddr, r);
+  else tc::tmem_st8(taddr, r);
+}
+
+// E4M3 code of 8 * 8^-t: the B-side block scale of query term t
+__host__ __device__ constexpr uint32_t term_scale_code(int t) {
+  return t == 0 ? 0x50u : t == 1 ? 0x38u : t == 2 ? 0x20u : t == 3 ? 0x08u : 0x01u;   // 8, 1, 1/8, 1/64, 1/512
+}
+static_assert(NQT <= 5 && 4 * NQT <= 32, "term_scale_code covers five terms; one 32-column store writes them");
+
+// channels c .. c+7 of query head h of row g as float (bf16 -> f32, exact); in the
+// rotated part of a fused decode, turned by the row's angles in FP32 (every
+// product, difference and sum rounded separately: no fused multiply-add) and
+// rounded back to bf16 (nearest, ties to even) - the rotated query is a bf16
+// tensor like the query itself
 template <int D>
-__device__ __noinline__ void load_q(const AttnArgs& a, int g, uint8_t* sQ, int st) {
-  constexpr int NV = NH * D / 8 / 256;                // 16-byte vectors per thread
-  constexpr int NB = 4;                               // loads in flight per thread
-  static_assert(NV % NB == 0, "Q vectors per thread");
-  static_assert(256 % (D / 8) == 0, "a thread sees the same 8 channels in every vector");
-  const uint16_t* qg = a.q + (size_t)g * a.H * D;
-  const uint32_t sq = tc::smem_u32(sQ);
-  // rotary factors of this thread's 4 channel pairs (if they lie in the rotated part)
-  bool rot = false;
-  float4 cr = make_float4(1.f, 1.f, 1.f, 1.f), sr = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (a.rope_dim > 0 && 8 * (st % (D / 8)) >= D - a.rope_dim) {
-    const int p = a.rope_pos[g];
-    if (p >= 0 && p < a.max_pos) {
-      const int i0 = 4 * (st % (D / 8)) - (D - a.rope_dim) / 2;
-      const float* row = a.cos_sin + (size_t)p * a.rope_dim;
-      cr = __ldg(reinterpret_cast<const float4*>(row + i0));
-      sr = __ldg(reinterpret_cast<const float4*>(row + a.rope_dim / 2 + i0));
-      rot = true;
-    } else {
-      report(a.err, PKV_DEVERR_BAD_PAGE);
+__device__ __forceinline__ void load_q8(const AttnArgs& a, const uint16_t* qh, int c, int pos, float* x) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + c));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+  if (pos >= 0 && c >= D - a.rope_dim) {
+    const int i0 = (c - (D - a.rope_dim)) / 2;
+    const float* row = a.cos_sin + (size_t)pos * a.rope_dim;
+    const float4 cr = __ldg(reinterpret_cast<const float4*>(row + i0));
+    const float4 sr = __ldg(reinterpret_cast<const float4*>(row + a.rope_dim / 2 + i0));
+    const float cc[4] = {cr.x, cr.y, cr.z, cr.w}, ss[4] = {sr.x, sr.y, sr.z, sr.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float x0 = x[2 * i], x1 = x[2 * i + 1];
+      const float y0 = __fsub_rn(__fmul_rn(x0, cc[i]), __fmul_rn(x1, ss[i]));
+      const float y1 = __fadd_rn(__fmul_rn(x0, ss[i]), __fmul_rn(x1, cc[i]));
+      x[2 * i] = __bfloat162float(__float2bfloat16_rn(y0));
+      x[2 * i + 1] = __bfloat162float(__float2bfloat16_rn(y1));
     }
   }
-#pragma unroll 1
-  for (int b0 = 0; b0 < NV; b0 += NB) {
-    uint4 in[NB];
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-      const int v = st + 256 * (b0 + k);
-      const int h = v / (D / 8), c8 = v % (D / 8);    // 8 channels per vector
-      in[k] = h < a.H ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)h * D + 8 * c8)) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Write the query of row g into shared memory as the B operand of S^T = K Q^T,
+// called by the 256 softmax threads; thread st takes head st/4, channels
+// (st%4)*D/4 .. +D/4.  Heads >= H are zero.
+//   fp4 form (global tiles): per head, x = q * 4/amax_h in [-4, 4];
+//     c_0 = E2M1(x), c_t = E2M1(8 (r_{t-1} ...)): x ~ sum_t c_t 8^-t, the codes
+//     stored as NQT K-major FP4 terms [NCB][64 heads][RB] (swizzle as the K
+//     pages); the B block scales 8^(1-t) are constants in TMEM, so the
+//     contraction gives 8x and the logit factor is scale * ts_k * amax_h / 32.
+//   e4m3 form (window tile): x = q * 2^-k_h (k_h: the least power of two with
+//     |x| <= 448), t1 = E4M3(x), t2 = E4M3(x - t1) (exact for a bf16 q), two
+//     K-major E4M3 terms [D/128][64 heads][128] (128-byte swizzle); the logit
+//     factor is scale * tw_k * 2^k_h.
+// Writes the per-head logit factors (log2 units) to zs[h].
+template <int D>
+__device__ __noinline__ void write_q(const AttnArgs& a, int g, bool e4m3_form, uint8_t* sQ, float* zs, int st) {
+  using C = Cfg<D>;
+  using KL = KLayout<D>;
+  constexpr int CPT = D / 4;                 // channels per thread
+  const int h = st >> 2, part = st & 3;
+  const int c0 = part * CPT;
+  const bool live = h < a.H;
+  const uint16_t* qh = a.q + ((size_t)g * a.H + (live ? h : 0)) * D;
+  int pos = -1;
+  if (a.rope_dim > 0) {
+    pos = a.rope_pos[g];
+    if (pos < 0 || pos >= a.max_pos) {
+      if (st == 0) report(a.err, PKV_DEVERR_BAD_PAGE);
+      pos = -1;
     }
+  }
+  float amax = 0.f;
+  if (live) {
+#pragma unroll 1
+    for (int c = c0; c < c0 + CPT; c += 8) {
+      float x[8];
+      load_q8<D>(a, qh, c, pos, x);
 #pragma unroll
-    for (int k = 0; k < NB; ++k) {
-      const int v = st + 256 * (b0 + k);
-      const int h = v / (D / 8), c8 = v % (D / 8);
-      const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
-      uint32_t r[4];
-      if (rot) {
-        const float c[4] = {cr.x, cr.y, cr.z, cr.w}, sn[4] = {sr.x, sr.y, sr.z, sr.w};
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    }
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const uint32_t sq = tc::smem_u32(sQ);
+  if (!e4m3_form) {
+    const float inv = amax > 0.f ? 4.f / amax : 0.f;
+    if (part == 0) zs[h] = amax > 0.f ? a.scale * a.cache.ts_k * LOG2E / (8.f * inv) : 0.f;
+#pragma unroll 1
+    for (int c = c0; c < c0 + CPT; c += 32) {          // one 16-byte chunk of each term
+      uint32_t w[NQT][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float x0 = __uint_as_float(w[i] << 16), x1 = __uint_as_float(w[i] & 0xFFFF0000u);
-          r[i] = f32_to_f16x2(x0 * c[i] - x1 * sn[i], x0 * sn[i] + x1 * c[i]);
+      for (int v = 0; v < 4; ++v) {
+        float x[8];
+        if (live) {
+          load_q8<D>(a, qh, c + 8 * v, pos, x);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] *= inv;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = 0.f;
         }
-      } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          r[i] = f32_to_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+        for (int t = 0; t < NQT; ++t) {
+          uint32_t word = 0u;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t b = tc::f32x2_to_e2m1x2(x[2 * i], x[2 * i + 1]);
+            word |= b << (8 * i);
+            if (t + 1 < NQT) {
+              const uint32_t v2 = tc::e2m1x2_to_f16x2(b);
+              x[2 * i] = 8.f * (x[2 * i] - tc::f16_lo_to_f32(v2));
+              x[2 * i + 1] = 8.f * (x[2 * i + 1] - tc::f16_hi_to_f32(v2));
+            }
+          }
+          w[t][v] = word;
+        }
       }
-      const int atom = c8 >> 3, ch = c8 & 7;
-      tc::sts128(sq + atom * (NH * 128) + h * 128 + 16 * (ch ^ (h & 7)), make_uint4(r[0], r[1], r[2], r[3]));
+      const int off = KL::chunk(h, c / 32);            // head row h of a term, as token row h of a page
+#pragma unroll
+      for (int t = 0; t < NQT; ++t)
+        tc::sts128(sq + t * C::QT_BYTES + off, make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]));
+    }
+  } else {
+    int k = 0;
+    if (amax > 0.f) {
+      const uint32_t u = __float_as_uint(amax / 448.f);
+      k = (int)((u >> 23) & 0xFFu) - 127 + ((u & 0x7FFFFFu) ? 1 : 0);
+      k = k < -126 ? -126 : (k > 126 ? 126 : k);
+    }
+    const float down = __uint_as_float((uint32_t)(127 - k) << 23);   // 2^-k
+    const float up = __uint_as_float((uint32_t)(127 + k) << 23);     // 2^k
+    if (part == 0) zs[h] = amax > 0.f ? a.scale * a.tw_k * up * LOG2E : 0.f;
+#pragma unroll 1
+    for (int c = c0; c < c0 + CPT; c += 16) {          // 16 channels = one 16-byte chunk of each term
+      uint32_t w1[4], w2[4];
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        float x[8];
+        if (live) {
+          load_q8<D>(a, qh, c + 8 * v, pos, x);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] *= down;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+          const uint32_t b0 = tc::f32x2_to_e4m3x2(x[2 * i], x[2 * i + 1]);
+          const uint32_t b1 = tc::f32x2_to_e4m3x2(x[2 * i + 2], x[2 * i + 3]);
+          const uint32_t v0 = tc::e4m3x2_to_f16x2(b0), v1 = tc::e4m3x2_to_f16x2(b1);
+          const uint32_t r0 = tc::f32x2_to_e4m3x2(x[2 * i] - tc::f16_lo_to_f32(v0), x[2 * i + 1] - tc::f16_hi_to_f32(v0));
+          const uint32_t r1 = tc::f32x2_to_e4m3x2(x[2 * i + 2] - tc::f16_lo_to_f32(v1),
+                                                  x[2 * i + 3] - tc::f16_hi_to_f32(v1));
+          w1[2 * v + i / 2] = b0 | (b1 << 16);
+          w2[2 * v + i / 2] = r0 | (r1 << 16);
+        }
+      }
+      const int ch = c / 128, sub = (c % 128) / 16;
+      const int off = ch * (NH * 128) + h * 128 + 16 * (sub ^ (h & 7));
+      tc::sts128(sq + off, make_uint4(w1[0], w1[1], w1[2], w1[3]));
+      tc::sts128(sq + C::QW_BYTES + off, make_uint4(w2[0], w2[1], w2[2], w2[3]));
     }
   }
   tc::fence_proxy_async_smem();
+  tc::named_bar(1, 256);                               // zs[] complete before anyone reads it
 }
 
 // ---------------------------------------------------------------- the kernel
 template <int D>
-__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const int* __restrict__ tile_start,
+__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap wmap,
+                                                              const int* __restrict__ tile_start,
                                                               float* __restrict__ part_o,
                                                               float* __restrict__ part_lse) {
   using C = Cfg<D>;
@@ -296,19 +421,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   const long long T = tile_start[a.n_groups];
   const long long x0 = cta_start(T, G, cta), x1 = cta_start(T, G, cta + 1);
   const int g0 = tile_start[a.n_groups + 1 + cta];     // query row of tile x0 (from the plan)
+  const long long lim = a.wait_limit;
 
   if (tid == 0) {
-    for (int i = 0; i < NKR; ++i) {
+    for (int i = 0; i < NKS; ++i) {
       tc::mbar_init(&sh.kr_full[i], 1);
-      tc::mbar_init(&sh.kr_empty[i], NDEQ);
+      tc::mbar_init(&sh.kr_empty[i], 1);
     }
     for (int i = 0; i < NVR; ++i) {
       tc::mbar_init(&sh.vr_full[i], 1);
       tc::mbar_init(&sh.vr_empty[i], NDEQ);
     }
-    for (int i = 0; i < NKS; ++i) {
-      tc::mbar_init(&sh.kfull[i], NGRP);
-      tc::mbar_init(&sh.kempty[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sh.sfa_full[i], 4);
+      tc::mbar_init(&sh.sfa_empty[i], 1);
     }
     for (int i = 0; i < NVS; ++i) {
       tc::mbar_init(&sh.vfull[i], NGRP);
@@ -316,10 +442,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     }
     tc::mbar_init(&sh.s_full, 1);
     tc::mbar_init(&sh.s_empty, 8);
-    tc::mbar_init(&sh.p_full[0], 8);
-    tc::mbar_init(&sh.p_full[1], 8);
-    tc::mbar_init(&sh.p_empty[0], 1);
-    tc::mbar_init(&sh.p_empty[1], 1);
+    tc::mbar_init(&sh.p_full, 8);
+    tc::mbar_init(&sh.p_empty, 1);
     tc::mbar_init(&sh.q_full, 8);
     tc::mbar_init(&sh.o_empty, 8);
     tc::mbar_init(&sh.drain, 1);
@@ -327,7 +451,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     sh.abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == W_MMA) {
+  if (warp == W_QK) {
     tc::tmem_alloc(&sh.tmem_base, 512);
     tc::tmem_relinquish();
   }
@@ -345,20 +469,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   const size_t pdb = (size_t)C::PAGE_DATA, psb = (size_t)C::PAGE_SCALE;
 
   if (x0 < x1) {
-    // ======================================================== producers
-    // one warp streams K pages (codes + scales) into the K ring, another V pages
-    // into the V ring, one page per slot, with 1-D bulk copies.
-    if (warp == W_KPROD || warp == W_VPROD) {
-      // The whole warp walks the pages; page-table entries are read 32 at a time
-      // (one per lane, coalesced) and lane 0 issues the copies.
-      const bool isK = (warp == W_KPROD);
-      const int nslot = isK ? NKR : NVR;
-      uint64_t* fullb = isK ? sh.kr_full : sh.vr_full;
-      uint64_t* emptyb = isK ? sh.kr_empty : sh.vr_empty;
-      uint8_t* ring = isK ? sK : sV;
-      const uint8_t* gdata = isK ? a.cache.k_data : a.cache.v_data;
-      const uint8_t* gscale = isK ? a.cache.k_scale : a.cache.v_scale;
-      int pi = 0;     // pages issued
+    // ======================================================== K tile producer
+    // Tile j of a row: its two pages, each column block of a page one 1-D bulk
+    // copy into the tile slot ([column block][128 rows][RB]: rows 0-63 the first
+    // page, 64-127 the second); the window tile: its E4M3 K rows by TMA, 128
+    // channels (one 16 KB chunk, 128-byte swizzle) per copy.
+    if (warp == W_KPROD) {
+      int kt = 0;               // slot uses issued
+      int skipped = -1;         // copy left out by the testing hook
       bool ok = true;
       long long x = x0;
       int g = g0;
@@ -368,18 +486,88 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int nt = tile_start[g + 1] - tile_start[g];
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        const int npr = (u.n_glob + PKV_PAGE - 1) / PKV_PAGE;       // pages of the row
         if (lane == 0) {
-          // the next query row's Q (loaded by the softmax at this row's end): warm L2
-          if (isK && j0 == 0 && x1 > tile_start[g + 1] && g + 1 < a.n_groups && ((uintptr_t)a.q & 15u) == 0)
+          // the next query row's Q (read by the softmax at this row's end): warm L2
+          if (j0 == 0 && x1 > tile_start[g + 1] && g + 1 < a.n_groups && ((uintptr_t)a.q & 15u) == 0)
             tc::bulk_prefetch_l2(a.q + (size_t)(g + 1) * a.H * D, (uint32_t)(a.H * D * 2));
-          // the window tile (last of the row) is read from global memory by the
-          // dequant warps: warm L2 with it while the paged tiles stream
-          if (isK && j1 == nt && u.wk != last_win && (((uintptr_t)u.wk | (uintptr_t)u.wv) & 15u) == 0) {
-            tc::bulk_prefetch_l2(u.wk, (uint32_t)(PKV_WINDOW * D));    // window buffers are [B][128][d]
+          // the window V (read from global memory by the V dequantizers): warm L2
+          if (j1 == nt && u.wv != last_win && ((uintptr_t)u.wv & 15u) == 0) {
             tc::bulk_prefetch_l2(u.wv, (uint32_t)(PKV_WINDOW * D));
-            last_win = u.wk;
+            last_win = u.wv;
           }
         }
+        int pbase = -1, pl = -1;            // lane i holds page id pbase + i of the row
+        for (int j = j0; j < j1 && ok; ++j) {
+          const bool win = (j == nt - 1);
+          if (!win) {
+            const int p0 = 2 * j, npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
+            if (pbase < 0 || p0 + 1 >= pbase + 32) {
+              pbase = p0;
+              pl = (pbase + lane < npr) ? a.page_table[(size_t)u.b * a.max_pages + pbase + lane] : -1;
+            }
+            const int pid0 = __shfl_sync(0xffffffffu, pl, p0 - pbase);
+            const int pid1 = __shfl_sync(0xffffffffu, pl, p0 + 1 - pbase);
+            if (lane == 0) {
+              const int slot = kt % NKS, use = kt / NKS;
+              if (!tc::mbar_wait(&sh.kr_empty[slot], (use & 1) ^ 1, abort_p, lim)) { fail(sh, a.err); ok = false; }
+              if (ok) {
+                if (a.hook_skip_copy == kt && cta == 0) {
+                  skipped = kt;
+                } else {
+                  tc::mbar_arrive_expect_tx(&sh.kr_full[slot], (uint32_t)(npg * C::PAGE_DATA));
+                  uint8_t* dst = sK + slot * C::KSLOT;
+                  for (int p = 0; p < npg; ++p) {
+                    int pid = p ? pid1 : pid0;
+                    if (pid < 0 || pid >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); pid = 0; }
+                    for (int cb = 0; cb < C::NCB; ++cb)
+                      tc::bulk_g2s(dst + cb * (TILE * C::RB) + p * (PKV_PAGE * C::RB),
+                                   a.cache.k_data + (size_t)pid * pdb + cb * (PKV_PAGE * C::RB),
+                                   (uint32_t)(PKV_PAGE * C::RB), &sh.kr_full[slot]);
+                  }
+                }
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ++kt;
+          } else {
+            for (int s = 0; s < C::NWS && ok; ++s) {
+              if (lane == 0) {
+                const int slot = kt % NKS, use = kt / NKS;
+                if (!tc::mbar_wait(&sh.kr_empty[slot], (use & 1) ^ 1, abort_p, lim)) { fail(sh, a.err); ok = false; }
+                if (ok) {
+                  const int c0 = s * C::CPS, nc = min(C::CPS, C::NWC - c0);
+                  tc::mbar_arrive_expect_tx(&sh.kr_full[slot], (uint32_t)(nc * WCHUNK));
+                  for (int c = 0; c < nc; ++c)
+                    tc::tma_load_2d(sK + slot * C::KSLOT + c * WCHUNK, &wmap, (c0 + c) * 128, u.b * PKV_WINDOW,
+                                    &sh.kr_full[slot]);
+                }
+              }
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+              ++kt;
+            }
+          }
+        }
+        x = tile_start[g] + j1;
+        ++g;
+      }
+      // drain: every copy issued must have landed before this CTA may exit
+      // (the last use of each slot; earlier uses were waited for by the MMA warp)
+      if (lane == 0)
+        for (int k = (kt > NKS ? kt - NKS : 0); k < kt; ++k)
+          if (k != skipped && !tc::mbar_drain(&sh.kr_full[k % NKS], (k / NKS) & 1, lim)) report(a.err, PKV_DEVERR_TIMEOUT);
+    }
+    // ======================================================== V page producer
+    else if (warp == W_VPROD) {
+      int pi = 0;     // pages issued
+      bool ok = true;
+      long long x = x0;
+      int g = g0;
+      while (x < x1 && ok) {
+        const Unit u = unit_of(a, g);
+        const int nt = tile_start[g + 1] - tile_start[g];
+        const int j0 = (int)(x - tile_start[g]);
+        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         // pages [2*j0, pend) of the row: those of its NVFP4 tiles in this CTA's range
         const int jp = min(j1, nt - 1);
         const int pend = min(2 * jp, (u.n_glob + PKV_PAGE - 1) / PKV_PAGE);
@@ -391,13 +579,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             int p = __shfl_sync(0xffffffffu, pl, q);
             if (lane == 0) {
               if (p < 0 || p >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); p = 0; }
-              const int slot = pi % nslot, use = pi / nslot;
-              if (!tc::mbar_wait(&emptyb[slot], (use & 1) ^ 1, abort_p)) { fail(sh, a.err); ok = false; }
+              const int slot = pi % NVR, use = pi / NVR;
+              if (!tc::mbar_wait(&sh.vr_empty[slot], (use & 1) ^ 1, abort_p, lim)) { fail(sh, a.err); ok = false; }
               if (ok) {
-                tc::mbar_arrive_expect_tx(&fullb[slot], C::PSLOT);
-                uint8_t* dst = ring + slot * C::PSLOT;
-                tc::bulk_g2s(dst, gdata + (size_t)p * pdb, C::PAGE_DATA, &fullb[slot]);
-                tc::bulk_g2s(dst + C::PAGE_DATA, gscale + (size_t)p * psb, C::PAGE_SCALE, &fullb[slot]);
+                tc::mbar_arrive_expect_tx(&sh.vr_full[slot], C::PSLOT);
+                uint8_t* dst = sV + slot * C::PSLOT;
+                tc::bulk_g2s(dst, a.cache.v_data + (size_t)p * pdb, C::PAGE_DATA, &sh.vr_full[slot]);
+                tc::bulk_g2s(dst + C::PAGE_DATA, a.cache.v_scale + (size_t)p * psb, C::PAGE_SCALE, &sh.vr_full[slot]);
               }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -408,51 +596,87 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         x = tile_start[g] + j1;
         ++g;
       }
-      // drain: every copy issued must have landed before this CTA may exit
-      // (the last use of each slot; earlier uses were waited for by the consumers)
       if (lane == 0)
-        for (int k = (pi > nslot ? pi - nslot : 0); k < pi; ++k)
-          if (!tc::mbar_drain(&fullb[k % nslot], (k / nslot) & 1)) report(a.err, PKV_DEVERR_TIMEOUT);
+        for (int k = (pi > NVR ? pi - NVR : 0); k < pi; ++k)
+          if (!tc::mbar_drain(&sh.vr_full[k % NVR], (k / NVR) & 1, lim)) report(a.err, PKV_DEVERR_TIMEOUT);
     }
-    // ======================================================== MMA issuers
-    // One warp issues S^T = K Q^T (per 64-channel K chunk: 4 MMAs), another
-    // O^T += V^T P (per 128-channel x 64-token V chunk: 4 MMAs), each in the
-    // fixed order of its inputs with blocking waits.  The whole warp runs the
+    // ======================================================== QK MMA issuer
+    // Global tile: NQT x KS block-scaled FP4 MMAs (M128 N64 K64) into S; window
+    // tile: 2 terms x D/32 FP8 MMAs (M128 N64 K32).  The whole warp runs the
     // schedule and one elected lane issues (operands stay warp-uniform).
-    else if (warp == W_MMA) {
-      const uint32_t idK = tc::idesc_f16(128, NH, false, false);   // B = Q, K-major
-      // descriptor base; the start-address field (bits 0-13, address >> 4) is advanced by addition
-      const uint64_t dq0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
-      int ks = 0, nq = 0, iq = 0;
-      uint32_t kph = 0;          // K slot ring: slot, phase
+    else if (warp == W_QK) {
+      const uint32_t idq = tc::idesc_nvf4(128, NH), idw = tc::idesc_e4m3(128, NH);
+      const uint32_t sk = tc::smem_u32(sK), sq = tc::smem_u32(sQ);
+      const uint64_t dK = tc::sdesc_kmajor(sk, C::RB), dQ = tc::sdesc_kmajor(sq, C::RB);
+      const uint64_t dKw = tc::sdesc_kmajor(sk, 128), dQw = tc::sdesc_kmajor(sq, 128);
+      int kt = 0, gt = 0, nq = 0, iq = 0;
       bool ok = true;
       long long x = x0;
       int g = g0;
       while (x < x1 && ok) {
-        const int j1 = (int)min((long long)(tile_start[g + 1] - tile_start[g]), x1 - tile_start[g]);
-        // Q of this item in shared memory
-        ok = tc::mbar_wait(&sh.q_full, iq & 1, abort_p);
-        ++iq;
-        for (int j = (int)(x - tile_start[g]); j < j1 && ok; ++j) {
+        const int nt = tile_start[g + 1] - tile_start[g];
+        const int j0 = (int)(x - tile_start[g]);
+        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        for (int j = j0; j < j1 && ok; ++j) {
+          const bool win = (j == nt - 1);
+          // the query form this tile reads (FP4 terms from the row's first global
+          // tile on, E4M3 terms for the window) has been written
+          if (win || j == j0) {
+            ok = tc::mbar_wait(&sh.q_full, iq & 1, abort_p, lim);
+            ++iq;
+          }
           // S free (the previous tile copied out by the softmax)
-          ok = tc::mbar_wait(&sh.s_empty, (nq & 1) ^ 1, abort_p);
-          const uint32_t dS = tbase + COL_S;
-          for (int c = 0; c < C::NKCH && ok; ++c) {
-            const int slot = ks;
-            ok = tc::mbar_wait(&sh.kfull[slot], kph, abort_p);
-            tc::compiler_fence();          // issue strictly after the wait (measured: large effect)
+          ok = ok && tc::mbar_wait(&sh.s_empty, (nq & 1) ^ 1, abort_p, lim);
+          if (!win) {
+            const int slot = kt % NKS, buf = gt & 1;
+            ok = ok && tc::mbar_wait(&sh.kr_full[slot], (kt / NKS) & 1, abort_p, lim);
+            ok = ok && tc::mbar_wait(&sh.sfa_full[buf], (gt >> 1) & 1, abort_p, lim);
+            tc::compiler_fence();          // issue strictly after the waits
             if (!ok) break;
             tc::tc_fence_after();
-            const uint32_t aK = tbase + COL_K + 32 * slot;
-            const uint64_t bq = dq0 + (uint64_t)(c * (NH * 128 / 16));
             if (tc::elect_one()) {
+#pragma unroll 1
+              for (int t = 0; t < NQT; ++t) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) tc::mma_ts(dS, aK + 8 * k, bq + 2 * k, idK, (c | k) != 0);
-              tc::mma_commit(&sh.kempty[slot]);
-              if (c == C::NKCH - 1) tc::mma_commit(&sh.s_full);
+                for (int k = 0; k < C::KS; ++k) {
+                  const int cb = (32 * k) / C::RB, kk = (32 * k) % C::RB;
+                  const uint64_t ad = dK + (uint64_t)((slot * C::KSLOT + cb * TILE * C::RB + kk) >> 4);
+                  const uint64_t bd = dQ + (uint64_t)((t * C::QT_BYTES + cb * NH * C::RB + kk) >> 4);
+                  tc::mma_nvf4_ss(tbase + COL_S, ad, bd, idq, tbase + COL_SFA + 32 * buf + 4 * k, tbase + COL_SFB + 4 * t,
+                                  (t | k) != 0);
+                }
+              }
+              tc::mma_commit(&sh.sfa_empty[buf]);
+              tc::mma_commit(&sh.kr_empty[slot]);
+              tc::mma_commit(&sh.s_full);
             }
             __syncwarp();
-            if (++ks == NKS) { ks = 0; kph ^= 1; }
+            ++kt;
+            ++gt;
+          } else {
+            for (int s = 0; s < C::NWS && ok; ++s) {
+              const int slot = kt % NKS;
+              ok = ok && tc::mbar_wait(&sh.kr_full[slot], (kt / NKS) & 1, abort_p, lim);
+              tc::compiler_fence();
+              if (!ok) break;
+              tc::tc_fence_after();
+              if (tc::elect_one()) {
+                const int c0 = s * C::CPS, nc = min(C::CPS, C::NWC - c0);
+                for (int c = 0; c < nc; ++c)
+#pragma unroll
+                  for (int t = 0; t < 2; ++t)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                      const uint64_t ad = dKw + (uint64_t)((slot * C::KSLOT + c * WCHUNK + 32 * kk) >> 4);
+                      const uint64_t bd = dQw + (uint64_t)((t * C::QW_BYTES + (c0 + c) * NH * 128 + 32 * kk) >> 4);
+                      tc::mma_f8_ss(tbase + COL_S, ad, bd, idw, !(s == 0 && c == 0 && t == 0 && kk == 0));
+                    }
+                tc::mma_commit(&sh.kr_empty[slot]);
+                if (s == C::NWS - 1) tc::mma_commit(&sh.s_full);
+              }
+              __syncwarp();
+              ++kt;
+            }
           }
           ++nq;
         }
@@ -463,9 +687,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       // drain outstanding MMAs before TMEM is freed
       if (tc::elect_one()) tc::mma_commit(&sh.drain);
       __syncwarp();
-      if (!tc::mbar_drain(&sh.drain, 0) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
+      if (!tc::mbar_drain(&sh.drain, 0, lim) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     }
-    else if (warp == W_MMA2) {
+    // ======================================================== PV MMA issuer
+    else if (warp == W_PV) {
       const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
       const uint64_t dp0 = tc::sdesc_sw128(tc::smem_u32(sP), 8192, 1024);
       int vs = 0, np = 0, ip = 0;
@@ -477,15 +702,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)(tile_start[g + 1] - tile_start[g]), x1 - tile_start[g]);
         // O of the previous item read out by the epilogue
-        ok = tc::mbar_wait(&sh.o_empty, (ip & 1) ^ 1, abort_p);
+        ok = tc::mbar_wait(&sh.o_empty, (ip & 1) ^ 1, abort_p, lim);
         ++ip;
         for (int j = j0; j < j1 && ok; ++j) {
-          ok = tc::mbar_wait(&sh.p_full[np & 1], (np >> 1) & 1, abort_p);
-          const uint64_t bpn = dp0 + (uint64_t)(((np & 1) * C::P_BYTES) >> 4);
+          ok = tc::mbar_wait(&sh.p_full, np & 1, abort_p, lim);
+          const uint64_t bpn = dp0;
           // chunk order: page half 0 for every channel chunk, then page half 1
           for (int cp = 0; cp < 2 * C::NVCH && ok; ++cp) {
             const int slot = vs, half = cp / C::NVCH, c = cp % C::NVCH;
-            ok = tc::mbar_wait(&sh.vfull[slot], vph, abort_p);
+            ok = tc::mbar_wait(&sh.vfull[slot], vph, abort_p, lim);
             tc::compiler_fence();
             if (!ok) break;
             tc::tc_fence_after();
@@ -496,7 +721,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               for (int k = 0; k < 4; ++k)
                 tc::mma_ts(dO, aV + 8 * k, bp + (uint64_t)(k * (2048 >> 4)), idV, !(j == j0 && half == 0 && k == 0));
               tc::mma_commit(&sh.vempty[slot]);
-              if (cp == 2 * C::NVCH - 1) tc::mma_commit(&sh.p_empty[np & 1]);
+              if (cp == 2 * C::NVCH - 1) tc::mma_commit(&sh.p_empty);
             }
             __syncwarp();
             if (++vs == NVS) { vs = 0; vph ^= 1; }
@@ -509,20 +734,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       if (!ok && lane == 0) fail(sh, a.err);
       if (tc::elect_one()) tc::mma_commit(&sh.drain2);
       __syncwarp();
-      if (!tc::mbar_drain(&sh.drain2, 0) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
+      if (!tc::mbar_drain(&sh.drain2, 0, lim) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     }
-    // ======================================================== K dequantizer (thread = token)
-    // Two groups of four warps (one warp per TMEM lane quarter); group kg
-    // converts the 64-channel chunks c = kg, kg+2, ... of every tile, a full
-    // 32-column slot per chunk.  Chunks are numbered across tiles and use the
-    // slot ring in order; a group advances two chunks at a time.
-    else if (warp < W_VDEQ) {
-      const int t = 32 * (warp & 3) + lane;          // token lane 0..127
-      const int kg = (warp - W_KDEQ) >> 2;           // chunk parity of this group
+    // ======================================================== K block scales (thread = tile row)
+    // Thread m holds row m of the tile's S^T (page m/64, token m%64): it loads the
+    // 4 scale bytes of each 64-channel K step of its token and stores them where
+    // the block-scaled MMA reads row m's scales (lane m, column base + 4k + m/32).
+    // Two buffers: the scales of tile n+1 are written while tile n is contracted.
+    else if (warp < W_SF + 4) {
+      const int m = 32 * (warp - W_SF) + lane;
       const uint32_t lb = lane_base(warp);
-      int kp = 0;               // pages consumed
-      int ks = kg;              // slot of this group's next chunk (chunk number kg, kg+2, ...)
-      uint32_t kph = 0;         // its phase
+      {
+        // constant B-side block scales of the query terms, every lane quarter
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = i < 4 * NQT ? term_scale_code(i / 4) * 0x01010101u : 0u;
+        tc::tmem_st32(tbase + lb + COL_SFB, r);
+        tc::tc_wait_st();
+      }
+      int gt = 0;
       bool ok = true;
       long long x = x0;
       int g = g0;
@@ -531,79 +761,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int nt = tile_start[g + 1] - tile_start[g];
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
-        for (int j = j0; j < j1 && ok; ++j) {
-          const bool win = (j == nt - 1);
-          int npg = 0;
-          bool valid;
-          const uint8_t* row = nullptr;
-          uint32_t srow_s = 0, ssc_s = 0;     // shared addresses: token row, its scale bytes
-          int slot = 0;
-          if (!win) {
-            npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
-            bool w_ok = true;
-            for (int q = 0; q < npg; ++q)
-              w_ok = w_ok && tc::mbar_wait(&sh.kr_full[(kp + q) % NKR], ((kp + q) / NKR) & 1, abort_p);
-            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-            valid = (TILE * j + t) < u.n_glob;
-            const uint32_t page = tc::smem_u32(sK) + ((kp + (t >> 6)) % NKR) * C::PSLOT;
-            slot = t & 63;
-            srow_s = page + slot * (D / 2);
-            ssc_s = page + C::PAGE_DATA + slot * 8;
-          } else {
-            valid = t < u.n_win;
-            row = u.wk + (size_t)t * D;
-          }
-#pragma unroll 1
-          for (int c = kg; c < C::NKCH; c += 2) {
-            uint32_t r[32];
-            if (!valid) {
+        for (int j = j0; j < j1 && j < nt - 1; ++j) {
+          const int buf = gt & 1;
+          const int pos = TILE * j + m;
+          uint32_t wrd[C::KS];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = 0u;
-            } else if (!win) {
-              constexpr int SW = (D / 32 < 8 ? D / 32 : 8) - 1;
-              // channels 64c .. 64c+63: two 16-byte pieces, four scale blocks
-              const uint4 v0 = tc::lds128(srow_s + 16 * ((2 * c) ^ (slot & SW)));
-              const uint4 v1 = tc::lds128(srow_s + 16 * ((2 * c + 1) ^ (slot & SW)));
-              const uint32_t sc = tc::lds32(ssc_s + (c >> 1) * (PKV_PAGE * 8) + 4 * (c & 1));
-              const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-              uint32_t s4[2];                            // f16 scales: (s0, s1), (s2, s3)
-              tc::e4m3x4_to_f16x2x2(sc, s4);
+          for (int k = 0; k < C::KS; ++k) wrd[k] = 0u;
+          if (pos < u.n_glob) {
+            int pid = a.page_table[(size_t)u.b * a.max_pages + (pos >> 6)];
+            if (pid < 0 || pid >= a.cache.num_pages) pid = 0;      // the producer reports it
+            const uint8_t* sp = a.cache.k_scale + (size_t)pid * psb + (pos & 63) * 8;
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {              // word q: channels 8q .. 8q+7 of the chunk (block q/2)
-                uint32_t e[4];
-                tc::e2m1x8_to_f16x2x4(w[q], e);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  r[4 * q + i] = (q & 2) ? tc::hmul2_hi(e[i], s4[q >> 2]) : tc::hmul2_lo(e[i], s4[q >> 2]);
-              }
-            } else {
-              const uint4* p4 = reinterpret_cast<const uint4*>(row + 64 * c);
-#pragma unroll
-              for (int h4 = 0; h4 < 4; ++h4) {
-                const uint4 v = __ldg(p4 + h4);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) tc::e4m3x4_to_f16x2x2(w[i], &r[8 * h4 + 2 * i]);
-              }
+            for (int q = 0; q < C::KS / 2; ++q) {
+              const uint2 v = __ldg(reinterpret_cast<const uint2*>(sp + q * (PKV_PAGE * 8)));
+              wrd[2 * q] = v.x;
+              wrd[2 * q + 1] = v.y;
             }
-            tc::reg_fence32(r);               // conversion done before the (blocking) slot wait
-            const bool w_ok = tc::mbar_wait(&sh.kempty[ks], kph ^ 1, abort_p);
-            if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-            tc::tmem_st32(tbase + lb + COL_K + 32 * ks, r);
-            tc::tc_wait_st();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.kfull[ks]);
-            ks += 2;
-            if (ks >= NKS) { ks -= NKS; kph ^= 1; }
           }
-          if (!ok) break;
-          if (!win) {
-            __syncwarp();
-            if (lane == 0)
-              for (int q = 0; q < npg; ++q) tc::mbar_arrive(&sh.kr_empty[(kp + q) % NKR]);
-            kp += npg;
-          }
+          const bool w_ok = tc::mbar_wait(&sh.sfa_empty[buf], ((gt >> 1) & 1) ^ 1, abort_p, lim);
+          if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
+          tc::tc_fence_after();
+          uint32_t r[4 * C::KS];
+#pragma unroll
+          for (int k = 0; k < C::KS; ++k)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) r[4 * k + q] = (q == (warp - W_SF)) ? wrd[k] : 0u;
+          st_sfa<C::KS>(tbase + lb + COL_SFA + 32 * buf, r);
+          tc::tc_wait_st();
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sh.sfa_full[buf]);
+          ++gt;
         }
         x = tile_start[g] + j1;
         ++g;
@@ -640,7 +828,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           for (int half = 0; half < 2 && ok; ++half) {       // tokens 64*half .. 64*half+63
             const bool paged = half < npg;
             if (paged) {
-              const bool w_ok = tc::mbar_wait(&sh.vr_full[(vp + half) % NVR], ((vp + half) / NVR) & 1, abort_p);
+              const bool w_ok = tc::mbar_wait(&sh.vr_full[(vp + half) % NVR], ((vp + half) / NVR) & 1, abort_p, lim);
               if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
             }
             const uint32_t base = tc::smem_u32(sV) + ((vp + half) % NVR) * C::PSLOT;
@@ -684,7 +872,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = 0u;      // second page absent: no valid token
               }
-              // zero the tokens beyond the valid count (their K rows are zero too)
+              // zero the tokens beyond the valid count
               const int t0 = 64 * half;
               if (t0 + 64 > nvalid) {
 #pragma unroll
@@ -695,7 +883,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 }
               }
               tc::reg_fence32(r);             // conversion done before the (blocking) slot wait
-              const bool w_ok = tc::mbar_wait(&sh.vempty[vs], vph ^ 1, abort_p);
+              const bool w_ok = tc::mbar_wait(&sh.vempty[vs], vph ^ 1, abort_p, lim);
               if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
               tc::tmem_st32(tbase + lb + COL_V + 32 * vs, r);
               tc::tc_wait_st();
@@ -732,9 +920,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       bool ok = true;
       long long x = x0;
       int g = g0;
-      load_q<D>(a, g, sQ, st);
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sh.q_full);
+      {
+        // the first query form this CTA needs: FP4 terms, or E4M3 terms when the
+        // range starts at a window tile
+        const int nt = tile_start[g + 1] - tile_start[g];
+        const bool first_win = (x0 - tile_start[g]) == nt - 1;
+        write_q<D>(a, g, first_win, sQ, first_win ? sh.zsw : sh.zsg, st);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sh.q_full);
+      }
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
         const int nt = tile_start[g + 1] - tile_start[g];
@@ -749,12 +943,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         for (int j = j0; j < j1; ++j) {
           const bool win = (j == nt - 1);
           const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
-          const float zs = a.scale * (win ? a.tw_k : a.cache.ts_k) * LOG2E;
+          const uint32_t zs_s = tc::smem_u32(win ? sh.zsw : sh.zsg);
           const float pr = win ? ratio : 1.f;
           const bool valid = t < nvalid;
           // ---- S tile ready?  Copy this token's 32 logits out of TMEM at once and
           // free S for the next tile's QK.
-          bool w_ok = tc::mbar_wait(&sh.s_full, ntile & 1, abort_p);
+          bool w_ok = tc::mbar_wait(&sh.s_full, ntile & 1, abort_p, lim);
           if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
           tc::tc_fence_after();
           float sa[32];
@@ -768,36 +962,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sh.s_empty);
-          // P buffer ntile&1 is free once the P.V of tile ntile-2 is done
-          const int pb = ntile & 1;
-          w_ok = tc::mbar_wait(&sh.p_empty[pb], ((ntile >> 1) & 1) ^ 1, abort_p);
-          if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
-          const uint32_t prow = tc::smem_u32(sP) + pb * C::P_BYTES + (t >> 3) * 1024 + (t & 7) * 128;
-          // two passes of 16 heads (keeps 16 logits live instead of 32)
+          // two passes of 16 heads (keeps 16 logits live instead of 32); the first
+          // pass's f16 P values wait in registers until the P buffer is free
+          const uint32_t prow = tc::smem_u32(sP) + (t >> 3) * 1024 + (t & 7) * 128;
 #pragma unroll
           for (int hq = 0; hq < 2; ++hq) {
             const int h0 = 32 * hh + 16 * hq;            // first head of this pass
-            // raw S^T of this token for heads h0 .. h0+15 (scaled below: d = S * zs - m)
-            float sv[16];
+            // logits of this token for heads h0 .. h0+15, log2 units: S * zs_h (in place)
+            float* sv = sa + 16 * hq;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sv[i] = sa[16 * hq + i];
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const uint4 zb = tc::lds128(zs_s + 4 * (h0 + 4 * i4));
+              sv[4 * i4] *= __uint_as_float(zb.x);
+              sv[4 * i4 + 1] *= __uint_as_float(zb.y);
+              sv[4 * i4 + 2] *= __uint_as_float(zb.z);
+              sv[4 * i4 + 3] *= __uint_as_float(zb.w);
+            }
             // does any logit exceed its running max by more than TAU?
             bool need = false;
             if (valid) {
 #pragma unroll
               for (int i4 = 0; i4 < 4; ++i4) {
                 const uint4 mb = tc::lds128(m_s + 4 * (h0 + 4 * i4));
-                need |= (fmaf(sv[4 * i4], zs, -__uint_as_float(mb.x)) > TAU) |
-                        (fmaf(sv[4 * i4 + 1], zs, -__uint_as_float(mb.y)) > TAU) |
-                        (fmaf(sv[4 * i4 + 2], zs, -__uint_as_float(mb.z)) > TAU) |
-                        (fmaf(sv[4 * i4 + 3], zs, -__uint_as_float(mb.w)) > TAU);
+                need |= (sv[4 * i4] - __uint_as_float(mb.x) > TAU) | (sv[4 * i4 + 1] - __uint_as_float(mb.y) > TAU) |
+                        (sv[4 * i4 + 2] - __uint_as_float(mb.z) > TAU) | (sv[4 * i4 + 3] - __uint_as_float(mb.w) > TAU);
               }
             }
             if (tc::named_bar_or(2, 256, need)) {
               // tile max per head: over the 32 tokens of the warp, then the 4 lane quarters
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
-                float v = valid ? sv[i] * zs : -INFINITY;
+                float v = valid ? sv[i] : -INFINITY;
 #pragma unroll
                 for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
                 if (lane == 0) sh.red[q4][h0 + i] = v;
@@ -815,8 +1010,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               l[hq] *= sh.alpha[h0 + hs];
               if (j > j0) {
                 // every P.V into O so far (tile ntile-1 and earlier) must be complete
-                const int kp = ntile - 1;
-                const bool pv_ok = tc::mbar_wait(&sh.p_empty[kp & 1], (kp >> 1) & 1, abort_p);
+                const bool pv_ok = tc::mbar_wait(&sh.p_empty, (ntile & 1) ^ 1, abort_p, lim);
                 if (tc::named_bar_or(3, 256, !pv_ok)) { fail(sh, a.err); ok = false; break; }
                 tc::tc_fence_after();
                 // O^T columns of these 16 heads, every channel chunk, times alpha
@@ -834,12 +1028,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                 tc::tc_wait_st();
               }
             }
-            // ---- P = exp2(S * zs - m) (f16): row t of P (MN-major, 128-byte swizzle),
-            // heads h0 .. h0+15 = two 16-byte chunks; l sums the FP32 values.  The
+            // ---- P = exp2(S * zs - m) (f16); l sums the FP32 values.  The
             // arguments are <= TAU, so the approximate exp2 stays in range.
+            uint32_t pk[8];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              uint32_t pk[4];
               const uint4 ma = tc::lds128(m_s + 4 * (h0 + 8 * k));
               const uint4 mb = tc::lds128(m_s + 4 * (h0 + 8 * k + 4));
               const float mk[8] = {__uint_as_float(ma.x), __uint_as_float(ma.y), __uint_as_float(ma.z),
@@ -848,26 +1041,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
 #pragma unroll
               for (int i2 = 0; i2 < 4; ++i2) {
                 const int i = 4 * k + i2;        // head pair index within the pass
-                const float p0 = ex2_approx(valid ? fmaf(sv[2 * i], zs, -mk[2 * i2]) : -INFINITY);
-                const float p1 = ex2_approx(valid ? fmaf(sv[2 * i + 1], zs, -mk[2 * i2 + 1]) : -INFINITY);
+                const float p0 = ex2_approx(valid ? sv[2 * i] - mk[2 * i2] : -INFINITY);
+                const float p1 = ex2_approx(valid ? sv[2 * i + 1] - mk[2 * i2 + 1] : -INFINITY);
                 sv[2 * i] = p0;
                 sv[2 * i + 1] = p1;
-                pk[i2] = f32_to_f16x2(p0 * pr, p1 * pr);
+                pk[i] = f32_to_f16x2(p0 * pr, p1 * pr);
               }
-              tc::sts128(prow + 16 * (((h0 >> 3) + k) ^ (t & 7)), make_uint4(pk[0], pk[1], pk[2], pk[3]));
             }
             l[hq] += warp_sum16(sv, lane);
+            if (hq == 0) {
+              // the P buffer is free once the P.V of the previous tile is done
+              w_ok = tc::mbar_wait(&sh.p_empty, (ntile & 1) ^ 1, abort_p, lim);
+              if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
+            }
+            // row t of P (MN-major, 128-byte swizzle): heads 8c .. 8c+7 = 16-byte chunk c
+            tc::sts128(prow + 16 * ((4 * hh + 2 * hq) ^ (t & 7)), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+            tc::sts128(prow + 16 * ((4 * hh + 2 * hq + 1) ^ (t & 7)), make_uint4(pk[4], pk[5], pk[6], pk[7]));
           }
           if (!ok) break;
           tc::fence_proxy_async_smem();
           tc::tc_fence_before();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sh.p_full[pb]);
+          if (lane == 0) tc::mbar_arrive(&sh.p_full);
           ++ntile;
-          // all S of this item consumed: Q of the next item may replace this one
-          // (done here, where few registers are live across the call)
-          if (j == j1 - 1 && xn < x1) {
-            load_q<D>(a, g + 1, sQ, st);
+          // the query form of the next tile (done here, where few registers are live):
+          // the window's E4M3 terms after the row's last global tile, the next
+          // row's first form after this row's last tile in range.  Every S that
+          // read the current form has been consumed, so its MMAs are complete.
+          if (j == nt - 2 && j1 == nt) {
+            write_q<D>(a, g, true, sQ, sh.zsw, st);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.q_full);
+          } else if (j == j1 - 1 && xn < x1) {
+            const bool nwin = (tile_start[g + 2] - tile_start[g + 1]) == 1;
+            write_q<D>(a, g + 1, nwin, sQ, nwin ? sh.zsw : sh.zsg, st);
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&sh.q_full);
           }
@@ -875,7 +1082,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         if (!ok) break;
         // ---- end of the item: wait for its last P.V, then write the partial
         const int klast = ntile - 1;       // P.V of the item's last tile done -> O complete
-        bool w_ok = tc::mbar_wait(&sh.p_empty[klast & 1], (klast >> 1) & 1, abort_p);
+        bool w_ok = tc::mbar_wait(&sh.p_empty, klast & 1, abort_p, lim);
         if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
         tc::tc_fence_after();
         // l over all 128 token lanes: the four lane quarters are summed below
@@ -926,7 +1133,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == W_MMA) tc::tmem_dealloc(tbase, 512);
+  if (warp == W_QK) tc::tmem_dealloc(tbase, 512);
 }
 
 // Output side of a fused decode, applied by the merge to the final O.
@@ -1046,12 +1253,34 @@ cudaError_t set_attrs() {
   return cudaFuncSetAttribute(pkv::tcattn::attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               pkv::tcattn::Cfg<D>::DYN);
 }
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// tensor map of a window K buffer [rows][d] (uint8): boxes of 128 rows x 128 bytes, 128-byte swizzle
+cudaError_t window_map(const uint8_t* wk, int d, int rows, CUtensorMap* map) {
+  if (!g_encode) return cudaErrorInitializationError;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(wk), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 }  // namespace
 
 cudaError_t pkv_attn_tc_init(int) {
   cudaError_t e = set_attrs<128>();
   if (e == cudaSuccess) e = set_attrs<256>();
   if (e == cudaSuccess) e = set_attrs<512>();
+  if (e == cudaSuccess && !g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && (q != cudaDriverEntryPointSuccess || !fn)) e = cudaErrorNotSupported;
+    if (e == cudaSuccess) g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  }
   return e;
 }
 
@@ -1089,14 +1318,18 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   float* part_o = (float*)p;
   p += rows * a.H * a.D * 4;
   float* part_lse = (float*)p;
+  CUtensorMap wmap;
+  const int nseq = a.replay ? a.n_groups / PKV_WINDOW : a.n_groups;
+  cudaError_t e = window_map(a.wk, a.D, nseq * PKV_WINDOW, &wmap);
+  if (e != cudaSuccess) return e;
   plan_kernel<<<1, 1024, 0, st>>>(a, tile_start, G);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (e0 && e1) cudaEventRecord(e0, st);
   switch (a.D) {
-    case 128: attn_tc_kernel<128><<<G, NTHREADS, Cfg<128>::DYN, st>>>(a, tile_start, part_o, part_lse); break;
-    case 256: attn_tc_kernel<256><<<G, NTHREADS, Cfg<256>::DYN, st>>>(a, tile_start, part_o, part_lse); break;
-    case 512: attn_tc_kernel<512><<<G, NTHREADS, Cfg<512>::DYN, st>>>(a, tile_start, part_o, part_lse); break;
+    case 128: attn_tc_kernel<128><<<G, NTHREADS, Cfg<128>::DYN, st>>>(a, wmap, tile_start, part_o, part_lse); break;
+    case 256: attn_tc_kernel<256><<<G, NTHREADS, Cfg<256>::DYN, st>>>(a, wmap, tile_start, part_o, part_lse); break;
+    case 512: attn_tc_kernel<512><<<G, NTHREADS, Cfg<512>::DYN, st>>>(a, wmap, tile_start, part_o, part_lse); break;
     default: return cudaErrorInvalidValue;
   }
   e = cudaGetLastError();

@@ -19,7 +19,6 @@ __global__ void __launch_bounds__(256) gather_kernel(pkv_kv_cache src, const int
                                                      int npb, pkv_kv_cache dst, int32_t* __restrict__ dst_len,
                                                      int* err) {
   constexpr int PD = PKV_PAGE * D / 2, PS = PKV_PAGE * D / 16;
-  constexpr int SW = (D / 32 < 8 ? D / 32 : 8) - 1;
   __shared__ int spage[8], sslot[8];
   const int page = blockIdx.x >> 3, o = blockIdx.x & 7;
   const int b = page / npb, jp = page % npb;
@@ -61,9 +60,9 @@ __global__ void __launch_bounds__(256) gather_kernel(pkv_kv_cache src, const int
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (spage[i] >= 0) {
       const int ss = sslot[i];
-      v = *reinterpret_cast<const uint4*>(src.k_data + (size_t)spage[i] * PD + ss * (D / 2) + 16 * (c ^ (ss & SW)));
+      v = *reinterpret_cast<const uint4*>(src.k_data + (size_t)spage[i] * PD + KLayout<D>::chunk(ss, c));
     }
-    *reinterpret_cast<uint4*>(dst.k_data + op * PD + s * (D / 2) + 16 * (c ^ (s & SW))) = v;
+    *reinterpret_cast<uint4*>(dst.k_data + op * PD + KLayout<D>::chunk(s, c)) = v;
   }
   // ---- K scales: 8-byte words ([d/128][64][8])
   for (int w = tid; w < 8 * (D / 128); w += 256) {

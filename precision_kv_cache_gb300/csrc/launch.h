@@ -19,9 +19,6 @@ cudaError_t pkv_launch_append_index(const float* x, const int32_t* seq_idx, cons
                                     const pkv_idx_cache& ic, const int32_t* page_table, int max_pages,
                                     int* err, cudaStream_t st);
 cudaError_t pkv_launch_quantize_fp8(const float* x, size_t n, float tw, uint8_t* out, cudaStream_t st);
-cudaError_t pkv_launch_attn_simple(int d, const pkv::AttnArgs& a, cudaStream_t st);
-cudaError_t pkv_launch_merge_splits(const float* part_o, const float* part_lse, int n_split, int rows_g,
-                                    int H, int D, float* out, float* out_lse, cudaStream_t st);
 cudaError_t pkv_launch_merge2(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
                               float* o, float* lse, int rows, int dv, cudaStream_t st);
 size_t pkv_topk_ws_bytes(int B, int k, int Lmax);

@@ -59,6 +59,8 @@ extern "C" pkv_status pkv_decode_attn_noalloc(pkv_ctx* ctx, const void* q_bf16,
                                               float softmax_scale, float* out, float* out_lse,
                                               void* stream) {
   if (!ctx || B <= 0 || max_pages <= 0) return PKV_ERR_INVALID_ARG;
+  // the same length limit as pkv_decode_attn, checked before the length is formed in int
+  if ((long long)max_pages * 64 > (1LL << 30)) return PKV_ERR_UNSUPPORTED;
   const size_t need = sel_idx ? pkv_workspace_bytes(ctx, PKV_OP_DECODE_SPARSE, B, k)
                               : pkv_workspace_bytes(ctx, PKV_OP_DECODE, B, max_pages * 64);
   if (need == 0) return PKV_ERR_INVALID_ARG;

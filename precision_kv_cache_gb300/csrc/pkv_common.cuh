@@ -70,18 +70,33 @@ __device__ __forceinline__ float e2m1_value(uint32_t c) {
 }
 
 // ---------------------------------------------------------------- page layout
+// K cache: a token's d/2 code bytes are cut into column blocks of RB = min(128, d/2)
+// bytes stored [column block][64 tokens][RB]; inside a block the 16-byte chunk c
+// of token t sits at chunk position c ^ w(t), w = t mod 8 (RB = 128) or
+// (t / 2) mod 4 (RB = 64): the K-major operand layout (128- / 64-byte swizzle)
+// of the block-scaled FP4 contraction, so pages are consumed as copied.
 template <int D>
 struct KLayout {
-  static constexpr int kRowBytes = D / 2;
-  static constexpr int kSwz = (D / 32 < 8 ? D / 32 : 8) - 1;
-  // byte offset of channel pair j of token t inside a page's data block
-  __device__ __forceinline__ static int data(int t, int j) {
-    return t * kRowBytes + 16 * ((j >> 4) ^ (t & kSwz)) + (j & 15);
+  static constexpr int RB = D / 2 < 128 ? D / 2 : 128;
+  static constexpr int CPR = RB / 16;          // 16-byte chunks per row of a column block
+  __host__ __device__ static constexpr int swz(int t) { return RB == 128 ? (t & 7) : ((t >> 1) & 3); }
+  // byte offset of 16-byte chunk c (channels 32c .. 32c+31) of token t
+  __device__ __forceinline__ static int chunk(int t, int c) {
+    return (c / CPR) * (PKV_PAGE * RB) + t * RB + 16 * ((c % CPR) ^ swz(t));
   }
+  // byte offset of channel pair j (channels 2j, 2j+1) of token t
+  __device__ __forceinline__ static int data(int t, int j) { return chunk(t, j >> 4) + (j & 15); }
   // byte offset of the scale of block j of token t
   __device__ __forceinline__ static int scale(int t, int j) {
     return (((j >> 3) * PKV_PAGE + t) << 3) + (j & 7);
   }
+};
+
+// Index keys (128 channels): rows of 64 bytes, 16-byte chunk c of token t at
+// chunk position c ^ (t mod 4); scales as the K cache.
+struct IdxLayout {
+  __device__ __forceinline__ static int data(int t, int j) { return t * 64 + 16 * ((j >> 4) ^ (t & 3)) + (j & 15); }
+  __device__ __forceinline__ static int scale(int t, int j) { return (((j >> 3) * PKV_PAGE + t) << 3) + (j & 7); }
 };
 
 template <int D>

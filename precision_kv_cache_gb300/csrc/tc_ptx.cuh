@@ -1,6 +1,7 @@
-// Thin inline-PTX wrappers for sm_103a: mbarriers (bounded waits), bulk
-// global->shared copies, tcgen05 (TMEM alloc, MMA, commit, ld/st, fences) and
-// the shared-memory / instruction descriptors of tcgen05.mma kind::f16.
+// Thin inline-PTX wrappers for sm_103a: mbarriers (bounded waits), bulk and
+// tensor (TMA) global->shared copies, tcgen05 (TMEM alloc, MMA of kinds f16,
+// f8f6f4 and block-scaled mxf4nvf4, commit, ld/st, fences), the shared-memory
+// and instruction descriptors, and the packed FP4 / FP8 conversions.
 // Written from the public PTX ISA description of these instructions.
 #pragma once
 #include <stdint.h>
@@ -126,6 +127,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 2-D tiled tensor copy global -> shared through a tensor map (TMA), completion
+// as transaction bytes on `bar`.  x is the innermost coordinate (bytes for a
+// uint8 map; a multiple of 16), y the row.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---------------------------------------------------------------- fences
 // hint: bring [src, src + bytes) into L2 (src 16-byte aligned, bytes a multiple of 16)
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
@@ -199,6 +211,32 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Shared-memory matrix descriptor of a K-major operand stored as 8-row groups of
+// `row_bytes` (128: 128-byte swizzle, 64: 64-byte swizzle), groups row_bytes*8
+// apart, 1024-byte aligned atoms.  The start-address field is advanced by adding
+// (byte offset >> 4) for the K steps inside a row.
+__device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr, int row_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;                                        // leading offset: unused for swizzled K-major
+  d |= (uint64_t)(((uint32_t)(8 * row_bytes) >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(row_bytes == 128 ? 2 : 4) << 61;               // 128-byte / 64-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf4nvf4 with block scaling:
+// E2M1 x E2M1, one UE4M3 scale per 16 elements of K (scale_vec::4X), f32
+// accumulator, both operands K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Instruction descriptor of tcgen05.mma kind::f8f6f4: E4M3 x E4M3, f32
+// accumulator, both operands K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: f32 accumulator, A/B f16
 // (or bf16), K-major unless *_mn, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn, bool bf16 = false) {
@@ -226,6 +264,30 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= (A[smem] x SFA) * (B[smem] x SFB): block-scaled FP4, the scale
+// factors in TMEM (column sfa + (row / 32) of each lane quarter for A; for B the
+// scale of column n at lane n % 32, column sfb + n / 32, in every quarter).
+__device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem], FP8 operands (kind::f8f6f4)
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // true in exactly one lane of the (converged) calling warp
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;
@@ -340,6 +402,30 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
       : "r"(two_bytes));
   return out;
 }
+// two f32 -> two E2M1 codes (nearest, ties to even, saturating at 6; sign kept):
+// lo in the low nibble, hi in the high nibble
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// two f32 -> two E4M3 codes (nearest, ties to even, saturating at 448): lo in the low byte
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
 // a * (lo half of s, lo half of s) and a * (hi, hi): f16x2 products by one broadcast scale
 __device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t s) {
   uint32_t d;

@@ -85,3 +85,26 @@ def assert_fp8_codes(gc, Or, out_scale, what, atol=ATOL, rtol=RTOL):
     one = lo == hi
     rc = F.fp8_quantize(Or, out_scale)
     assert np.array_equal(g[one], F.fp8_dequantize(rc, out_scale)[one]), what
+
+
+def assert_scores_close(g, qhat, w, khat, what):
+    """Element-wise bound on index scores sum_h w_h ReLU(qhat_h . k_t): each head's
+    128-term dot product is accumulated in FP32 from exact products (a tensor-core
+    contraction on f16 operands that hold the FP8 / NVFP4 values exactly), so its
+    error is at most 128 * 2^-23 * sum_i |q_hi k_ti| even with truncating adds; the
+    epilogue adds at most 66 roundings of 2^-24 (tensor scales, weight, ReLU'd sum of
+    64 non-negative terms).  Bound per position t: 2^-23 * (128 + 66) * R_t, with
+    R_t = sum_h |w_h| sum_i |qhat_hi khat_ti|."""
+    qhat = np.asarray(qhat, np.float64)
+    khat = np.asarray(khat, np.float64)
+    w = np.asarray(w, np.float64)
+    ref = np.maximum(khat @ qhat.T, 0.0) @ w
+    R = (np.abs(khat) @ np.abs(qhat).T) @ np.abs(w)
+    lim = 2.0 ** -23 * (128 + 66) * R
+    err = np.abs(np.asarray(g, np.float64) - ref)
+    bad = err > lim
+    if bad.any():
+        i = int(np.argmax(np.where(bad, err / np.maximum(lim, 1e-300), 0)))
+        raise AssertionError(f"{what}: {int(bad.sum())} of {len(ref)} scores outside the bound; worst at {i}: "
+                             f"gpu={g[i]} oracle={ref[i]} bound={lim[i]:.3e}")
+    return float((err / np.maximum(lim, 1e-300)).max())

@@ -88,7 +88,7 @@ def test_index_append_and_fp8_encode_match_oracle():
     ts = np.float32(48 / 2688)
     ic = P.IdxCache.empty(wl.num_pages, float(ts))
     ctx = P.Context(512, 64)
-    ref = C.Pools(wl.num_pages, 128, "k")
+    ref = C.Pools(wl.num_pages, 128, "i")
     bs, ps, rows = [], [], []
     for b in range(wl.B):
         for j in range((int(wl.seq_len[b]) + 63) // 64):

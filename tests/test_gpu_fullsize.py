@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 
 import workloads as W
-from helpers import assert_close, i32, torch_dev
+from helpers import assert_close, assert_scores_close, i32, torch_dev
 from oracle import attention as A
 from oracle import cache as C
 from oracle import formats as F
@@ -160,9 +160,9 @@ def test_fullsize_sparse_scoring_topk_and_decode(pool):
             p = int(wl.page_table[b, j])
             c, s = F.nvfp4_quantize(wl.index_rows(p), ts)
             khat[64 * j:64 * j + 64] = F.nvfp4_dequantize(c, s, ts)
-        ref = A.index_score(F.fp8_dequantize(qc[b], tq), w[b].astype(np.float64), khat)
-        err = np.abs(gsc[b, :L] - ref).max() / np.abs(ref).max()
-        assert err <= 1e-5, f"c3 scores seq {b}: rel err {err}"
+        qhat = F.fp8_dequantize(qc[b], tq)
+        ref = A.index_score(qhat, w[b].astype(np.float64), khat)
+        assert_scores_close(gsc[b, :L], qhat, w[b], khat, f"c3 scores seq {b}")
         ok, why = A.topk_matches(gsel[b], ref, k)
         assert ok, f"c3 top-k seq {b}: {why}"
         ref_sel[b] = A.topk(ref, k)

@@ -66,7 +66,7 @@ def test_sparse_step_graph_replay_matches_eager():
     Kp, Vp = C.fill_pages(wl, ts, ts)
     cache = upload_cache(Kp, Vp, ts, ts)
     win, _, _ = window_tensors(wl, tw, tw)
-    pool = C.Pools(wl.num_pages, 128, "k")
+    pool = C.Pools(wl.num_pages, 128, "i")
     for p in range(wl.num_pages):
         c, s = F.nvfp4_quantize(wl.index_rows(p), ts)
         pool.store(p, np.arange(64), c, s)

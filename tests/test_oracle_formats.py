@@ -216,3 +216,27 @@ def test_tensor_scale_fp8_worked_and_rounded():
     x = (g.standard_normal(4096) * 7).astype(np.float32)
     tw = F.tensor_scale_fp8(x)
     assert np.abs(F.fp8_dequantize(F.fp8_quantize(x, tw), tw)).max() <= 448 * float(tw)
+
+
+# ---------------------------------------------------------------- float32 -> bf16
+def test_f32_to_bf16_hand_worked_ties():
+    def f(bits):
+        return np.array([bits], np.uint32).view(np.float32)
+    def b(bits16):
+        return float(np.array([bits16 << 16], np.uint32).view(np.float32)[0])
+    cases = [(0x3F800000, 0x3F80), (0x3F808000, 0x3F80),   # exact half between 1.0 and the next: even (down)
+             (0x3F818000, 0x3F82),                          # half between 0x3F81 and 0x3F82: even (up)
+             (0x3F808001, 0x3F81), (0x3F807FFF, 0x3F80),    # just above / below the half
+             (0xBF818000, 0xBF82), (0x00000000, 0x0000), (0x80000000, 0x8000),
+             (0x7F7F7FFF, 0x7F7F)]                          # below the half under the largest finite
+    for src, want in cases:
+        got = F.f32_to_bf16(f(src))[0]
+        assert got == b(want) and np.signbit(got) == bool(want & 0x8000), hex(src)
+
+
+def test_f32_to_bf16_matches_ml_dtypes():
+    ml = pytest.importorskip("ml_dtypes")
+    g = np.random.default_rng(6)
+    x = np.concatenate([g.standard_normal(50000).astype(np.float32) * np.float32(3),
+                        (g.standard_normal(1000) * 1e-30).astype(np.float32)])
+    assert (F.f32_to_bf16(x) == x.astype(ml.bfloat16).astype(np.float64)).all()

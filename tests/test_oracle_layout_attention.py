@@ -25,6 +25,9 @@ def test_layout_golden_addresses():
         if kind == "kdata":
             assert LY.k_data_index(d)[t, j] == int(f[4]), line
             assert LY._k_data_addr(t, j, d) == int(f[4]), line
+        elif kind == "idata":
+            assert LY.i_data_index()[t, j] == int(f[4]), line
+            assert LY._i_data_addr(t, j) == int(f[4]), line
         elif kind == "kscale":
             assert LY.k_scale_index(d)[t, j] == int(f[4]), line
         elif kind == "vdata":
@@ -34,11 +37,14 @@ def test_layout_golden_addresses():
             assert LY.v_scale_index(d)[t, j] == int(f[4]), line
 
 
-@pytest.mark.parametrize("d", [128, 512])
+@pytest.mark.parametrize("d", [128, 256, 512])
 def test_layout_is_a_bijection_and_roundtrips(d):
     # every byte of a page is used exactly once (K: one pair per byte; V: two nibbles per byte)
     kd = LY.k_data_index(d).ravel()
     assert np.array_equal(np.sort(kd), np.arange(LY.k_data_bytes(d)))
+    if d == 128:
+        idd = LY.i_data_index().ravel()
+        assert np.array_equal(np.sort(idd), np.arange(LY.k_data_bytes(d)))
     ks = LY.k_scale_index(d).ravel()
     assert np.array_equal(np.sort(ks), np.arange(LY.k_scale_bytes(d)))
     va, vh = LY.v_data_index(d)
@@ -47,7 +53,7 @@ def test_layout_is_a_bijection_and_roundtrips(d):
     g = np.random.default_rng(5)
     codes = g.integers(0, 16, (64, d)).astype(np.uint8)
     sc = g.integers(0, 127, (64, d // 16)).astype(np.uint8)
-    for kind in ("k", "v"):
+    for kind in (("k", "v", "i") if d == 128 else ("k", "v")):
         p = C.Pools(3, d, kind)
         # write odd then even slots in two calls, then all again: same bytes
         p.store(1, np.arange(1, 64, 2), codes[1::2], sc[1::2])
@@ -56,8 +62,10 @@ def test_layout_is_a_bijection_and_roundtrips(d):
         assert (c2 == codes).all() and (s2 == sc).all()
         assert not p.data[0].any() and not p.data[2].any()
         # the per-token (loop) form reads the same values
-        load = LY.load_k_token if kind == "k" else LY.load_v_token
-        c3, s3 = load(p.data, p.scale, 1, 37, d)
+        if kind == "v":
+            c3, s3 = LY.load_v_token(p.data, p.scale, 1, 37, d)
+        else:
+            c3, s3 = LY.load_k_token(p.data, p.scale, 1, 37, d, index_keys=kind == "i")
         assert (c3 == codes[37]).all() and (s3 == sc[37]).all()
 
 
@@ -277,3 +285,26 @@ def test_topk_cand_brute_force_small():
         best = sorted(range(n), key=lambda i: (-sc[i], cand[i]))[:k]
         want = sorted(int(cand[i]) for i in best) + [-1] * (k - min(k, n))
         assert list(A.topk_cand(sc, cand, k)) == want
+
+
+@pytest.mark.parametrize("d", [128, 256, 512])
+def test_k_layout_rows_are_swizzled_operand_rows(d):
+    # Read back by the rule of a K-major swizzled operand: the 16-byte chunk at
+    # position p of row t in column block b holds logical chunk p XOR w(t), and a
+    # row's column blocks are 64*R bytes apart; each column block of a page is a
+    # [64][R] array of rows.  (A second formulation, by chunk position instead of
+    # by channel, of the same byte map.)
+    R = min(128, d // 2)
+    g = np.random.default_rng(8)
+    codes = g.integers(0, 16, (64, d)).astype(np.uint8)
+    p = C.Pools(1, d, "k")
+    p.store(0, np.arange(64), codes, np.zeros((64, d // 16), np.uint8))
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)        # [64][d/2]
+    page = p.data[0]
+    for t in range(64):
+        w = t % 8 if R == 128 else (t // 2) % 4
+        for b in range(d // 2 // R):
+            row = page[b * 64 * R + t * R: b * 64 * R + (t + 1) * R]
+            for pos in range(R // 16):
+                logical = b * (R // 16) + (pos ^ w)
+                assert (row[16 * pos:16 * pos + 16] == packed[t, 16 * logical:16 * logical + 16]).all()

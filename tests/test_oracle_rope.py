@@ -110,8 +110,9 @@ def test_fused_with_identity_table_is_the_plain_decode():
 
 
 def test_fused_equals_keys_turned_the_other_way():
-    # <R q, k> = <q, R^-1 k>: attend with the unrotated query over inversely turned
-    # keys (complex formulation), then turn the output back
+    # <q', k> = <R^-1 q', R^-1 k>: the rotated query q' (float32 rotation rounded to
+    # bf16) turned back by the exact inverse, attending over inversely turned keys
+    # (complex formulation), then the output turned back
     wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v = _small_workload()
     table = W.rope_table(wl.seed, 400, 64)
     for b in range(wl.B):
@@ -126,10 +127,8 @@ def test_fused_equals_keys_turned_the_other_way():
         Kall = np.concatenate([K, Kw], 0)
         Vall = np.concatenate([V, Vw], 0)
         q = F.bf16_to_f64(wl.q_bits_seq(b))
-        # scale the rotated query part by the table's radius (fp32 cos^2 + sin^2 != 1 exactly)
-        qs = q.copy()
-        qs[:, 64::2] *= rad
-        qs[:, 65::2] *= rad
+        qp = A.rope_query_bf16(q, table[pos, :32], table[pos, 32:], 64)
+        qs = _complex_rotate(qp, th, 64, sign=-1.0)
         Kinv = _complex_rotate(Kall, th, 64, sign=-1.0)
         z = (qs @ Kinv.T) / np.sqrt(128)
         m = z.max(1, keepdims=True)
@@ -165,3 +164,68 @@ def test_fused_sparse_selection_matches_dense_on_all_positions():
     a = C.expected_decode_fused(wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b, table, 64, W.OUT_SCALE)
     s = C.expected_decode_fused(wl, Kp, Vp, ts_k, ts_v, tw_k, tw_v, b, table, 64, W.OUT_SCALE, sel=sel)
     assert all(np.array_equal(x, y) for x, y in zip(s, a))
+
+
+def _f32_round(fr):
+    """Nearest float32 (ties to even) of an exact rational, by comparing neighbours."""
+    from fractions import Fraction
+    c = np.float32(float(fr))
+    best = None
+    for v in (np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))):
+        dv = abs(Fraction(float(v)) - fr)
+        if best is None or dv < best[0] or (dv == best[0] and (int(np.float32(v).view(np.uint32)) & 1) == 0):
+            best = (dv, v)
+    return np.float32(best[1])
+
+
+def _bf16_round(v32):
+    """Nearest bf16 value of a float32 (ties to even), by comparing the two bf16 neighbours exactly."""
+    from fractions import Fraction
+    u = int(np.array([v32], np.float32).view(np.uint32)[0])
+    lo = u & 0xFFFF0000
+    cands = [lo, lo + 0x10000]
+    fv = Fraction(float(v32))
+    best = None
+    for cb in cands:
+        val = Fraction(float(np.array([cb & 0xFFFFFFFF], np.uint32).view(np.float32)[0]))
+        dv = abs(val - fv)
+        if best is None or dv < best[0] or (dv == best[0] and ((cb >> 16) & 1) == 0):
+            best = (dv, float(val))
+    return best[1]
+
+
+def test_rope_query_bf16_by_exact_rationals():
+    # second formulation: products and difference / sum as exact rationals, each
+    # rounded to float32 by neighbour comparison, then to bf16 the same way
+    from fractions import Fraction
+    r = np.random.default_rng(9)
+    d, rd = 32, 16
+    q = F.bf16_to_f64(W.to_bf16_bits(r.standard_normal((3, d)).astype(np.float32)))
+    th = r.random(rd // 2) * 2 * np.pi
+    cos, sin = np.cos(th).astype(np.float32), np.sin(th).astype(np.float32)
+    got = A.rope_query_bf16(q, cos, sin, rd)
+    for h in range(3):
+        for c in range(d):
+            if c < d - rd:
+                assert got[h, c] == q[h, c]
+                continue
+            i = (c - (d - rd)) // 2
+            x0, x1 = Fraction(float(q[h, c - (c - (d - rd)) % 2])), Fraction(float(q[h, c - (c - (d - rd)) % 2 + 1]))
+            cc, ss = Fraction(float(cos[i])), Fraction(float(sin[i]))
+            if (c - (d - rd)) % 2 == 0:
+                y = _f32_round(Fraction(float(_f32_round(x0 * cc))) - Fraction(float(_f32_round(x1 * ss))))
+            else:
+                y = _f32_round(Fraction(float(_f32_round(x0 * ss))) + Fraction(float(_f32_round(x1 * cc))))
+            assert got[h, c] == _bf16_round(y), (h, c)
+
+
+def test_rope_query_bf16_is_the_rotation_to_bf16_precision():
+    r = np.random.default_rng(10)
+    q = F.bf16_to_f64(W.to_bf16_bits(r.standard_normal((8, 128)).astype(np.float32)))
+    th = r.random(32) * 2 * np.pi
+    cos, sin = np.cos(th).astype(np.float32), np.sin(th).astype(np.float32)
+    exact = A.rope(q, cos.astype(np.float64), sin.astype(np.float64), 64)
+    got = A.rope_query_bf16(q, cos, sin, 64)
+    # within half a bf16 ulp (2^-9 relative) plus the float32 rotation's own rounding
+    assert (np.abs(got - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-30).all()
+    assert np.array_equal(got[:, :64], q[:, :64])
