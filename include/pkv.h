@@ -48,8 +48,9 @@
  *   Index-key layout (index keys, d_index = 128): data [64][64]: channel pair j
  *     of token t at t*64 + 16*((j/16) ^ (t & 3)) + j%16; scales as K.
  *   V-layout (V):
- *     data  [8][d][4]: channel c of token t is nibble t%8 of the little-endian
- *           32-bit word (t/8)*d + c;
+ *     data  [d/128][8][128][4]: channel c of token t is nibble t%8 of the
+ *           little-endian 32-bit word ((c/128)*8 + t/8)*128 + c%128 (each
+ *           128-channel block of a page is one contiguous 4 KB run);
  *     scale [d/16][64]: block j of token t at j*64 + t.
  *   Window: FP8 codes [B][128][d], row-major.  Queries: bf16 [.][H][d].
  *   Outputs: O float32 [.][H][d], LSE float32 [.][H] (natural log; -inf and

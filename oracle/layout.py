@@ -19,10 +19,12 @@ K-layout (the K cache), d channels: a token's d/2 code bytes are cut into
 Index-key layout (the 128-wide index keys): data [64 tokens][64 bytes], channel
   pair j of token t in byte t*64 + 16*((j div 16) XOR (t AND 3)) + (j mod 16);
   scales as the K-layout.
-V-layout (V), d channels:
-  data  [8 octets][d channels][4 bytes]: channel ch of token t is nibble
-        (t mod 8) of the little-endian 32-bit word ((t div 8)*d + ch), i.e.
-        byte 4*((t div 8)*d + ch) + (t mod 8) div 2, low nibble for even t.
+V-layout (V), d channels: 32-bit words grouped by 128-channel chunk,
+  data  [d/128 chunks][8 octets][128 channels][4 bytes]: channel ch of token t
+        is nibble (t mod 8) of the little-endian 32-bit word
+        ((ch div 128)*8 + (t div 8))*128 + (ch mod 128), i.e. byte
+        4*(that word) + (t mod 8) div 2, low nibble for even t (one 128-channel
+        chunk of a page is one contiguous run of 4 KB).
   scale [d/16 blocks][64 tokens]: block j of token t sits in byte j*64 + t.
 Each pool is an array [num_pages][bytes per page] of uint8.
 """
@@ -61,7 +63,7 @@ def _k_scale_addr(t: int, j: int) -> int:
 
 
 def _v_data_addr(t: int, ch: int, d: int) -> tuple:
-    return 4 * ((t // 8) * d + ch) + (t % 8) // 2, (t % 2)
+    return 4 * (((ch // 128) * 8 + t // 8) * 128 + ch % 128) + (t % 8) // 2, (t % 2)
 
 
 def _v_scale_addr(t: int, j: int) -> int:
@@ -142,7 +144,7 @@ def v_data_index(d: int) -> tuple:
     """([64][d] byte address, [64][d] high-nibble flag) of channel ch of token t."""
     t = np.arange(PAGE)[:, None]
     ch = np.arange(d)[None, :]
-    return 4 * ((t // 8) * d + ch) + (t % 8) // 2, np.broadcast_to(t % 2 == 1, (PAGE, d))
+    return 4 * (((ch // 128) * 8 + t // 8) * 128 + ch % 128) + (t % 8) // 2, np.broadcast_to(t % 2 == 1, (PAGE, d))
 
 
 def v_scale_index(d: int) -> np.ndarray:

@@ -63,23 +63,27 @@ constexpr int W_KPROD = 20;            // K tile producer
 constexpr int W_QK = 21;               // QK MMA issuer, TMEM owner
 constexpr int W_VPROD = 22;            // V page producer
 constexpr int W_PV = 23;               // PV MMA issuer
-constexpr uint32_t NDEQ = 8;           // arrivals per V page release: one per dequant warp
-constexpr uint32_t NGRP = 4;           // arrivals per V chunk: one per warp of a group
+constexpr uint32_t NGRP = 4;           // arrivals per V ring slot release / V chunk: one per warp of a group
 constexpr float TAU = 8.f;             // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
 // TMEM columns (512 allocated)
-constexpr int NVS = 3;                 // V chunk slots
+constexpr int NVS = 2;                 // V chunk slots (one per dequant group)
 constexpr uint32_t COL_S = 0;          // S^T tile: 64 columns (fp32)
-constexpr uint32_t COL_SFA = 64;       // K block scales: 2 buffers x 32 columns (4 per 64-channel K step)
-constexpr uint32_t COL_SFB = 128;      // query term weights: 4 columns per term
-constexpr uint32_t COL_V = 160;        // V^T chunk slots: NVS x 32 columns (64 tokens, f16 pairs)
+constexpr uint32_t COL_SFA = 64;       // K block scales of a tile: 32 columns (4 per 64-channel K step)
+constexpr uint32_t COL_SFB = 96;       // query term weights: 4 columns per term
+constexpr uint32_t COL_KA = 128;       // the tile's K codes, A operand of S^T: 8 columns per 64-channel K step
+constexpr uint32_t COL_V = 192;        // V^T chunk slots: NVS x 32 columns (128 channels x 64 tokens, f16 pairs)
 constexpr uint32_t COL_O = 256;        // O^T: 4 chunks x 64 columns
-static_assert(COL_SFA + 64 <= COL_SFB && COL_SFB + 32 <= COL_V && COL_V + 32 * NVS <= COL_O, "TMEM map");
+static_assert(COL_SFA + 32 <= COL_SFB && COL_SFB + 32 <= COL_KA && COL_KA + 64 <= COL_V && COL_V + 32 * NVS <= COL_O,
+              "TMEM map");
 
 constexpr int NKS = 2;                 // K tile slots (two pages each, or window chunks)
-constexpr int NVR = 3;                 // V ring: page slots (released page by page)
+constexpr int NVR = 10;                // V ring: slots of one 128-channel chunk of one page
+constexpr int VCODES = 8 * 128 * 4;    // V codes of a 128-channel chunk of a page (8 octets x 128 words)
+constexpr int VSCALES = 8 * PKV_PAGE;  // its block scales (8 blocks x 64 tokens)
+constexpr int VSLOT = VCODES + VSCALES;
 constexpr int WCHUNK = 128 * 128;      // window K chunk: 128 entries x 128 channels of E4M3
 
 template <int D>
@@ -89,7 +93,6 @@ struct Cfg {
   static constexpr int KS = D / 64;                          // K steps of the FP4 contraction
   static constexpr int PAGE_DATA = PKV_PAGE * D / 2;
   static constexpr int PAGE_SCALE = PKV_PAGE * D / 16;
-  static constexpr int PSLOT = PAGE_DATA + PAGE_SCALE;       // one V page: codes + scales
   static constexpr int QT_BYTES = NH * D / 2;                // one FP4 query term [NCB][64][RB]
   static constexpr int QW_BYTES = NH * D;                    // one E4M3 query term [D/128][64][128]
   static constexpr int Q_BYTES = NQT * QT_BYTES > 2 * QW_BYTES ? NQT * QT_BYTES : 2 * QW_BYTES;
@@ -100,10 +103,10 @@ struct Cfg {
   static constexpr int NWS = (NWC + CPS - 1) / CPS;          // K slots one window tile uses
   static constexpr int NVCH = D / 128;                       // V chunks of 128 channels
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_P = OFF_Q + Q_BYTES;              // P (one buffer)
-  static constexpr int OFF_K = OFF_P + P_BYTES;              // K tile slots
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;              // 2 P buffers
+  static constexpr int OFF_K = OFF_P + 2 * P_BYTES;          // K tile slots
   static constexpr int OFF_V = OFF_K + NKS * KSLOT;          // V ring
-  static constexpr int DYN = OFF_V + NVR * PSLOT + 1024;     // + alignment slack
+  static constexpr int DYN = OFF_V + NVR * VSLOT + 1024;     // + alignment slack
   static_assert(QT_BYTES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_K % 1024 == 0 && KSLOT % 1024 == 0 &&
                 OFF_V % 16 == 0, "operand tiles stay 1024-aligned");
   static_assert(KS * 4 <= 32, "K scales of a tile fit one 32-column buffer");
@@ -111,9 +114,9 @@ struct Cfg {
 
 struct Shared {
   uint64_t kr_full[NKS], kr_empty[NKS], vr_full[NVR], vr_empty[NVR];
-  uint64_t sfa_full[2], sfa_empty[2];
+  uint64_t sfa_full, sfa_empty;
   uint64_t vfull[NVS], vempty[NVS];
-  uint64_t s_full, s_empty, p_full, p_empty, q_full, o_empty, drain, drain2;
+  uint64_t s_full, s_empty, p_full[2], p_empty[2], q_full, o_empty, drain, drain2;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float m[NH];     // running max per head (log2 units)
@@ -430,20 +433,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     }
     for (int i = 0; i < NVR; ++i) {
       tc::mbar_init(&sh.vr_full[i], 1);
-      tc::mbar_init(&sh.vr_empty[i], NDEQ);
+      tc::mbar_init(&sh.vr_empty[i], NGRP);
     }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sh.sfa_full[i], 4);
-      tc::mbar_init(&sh.sfa_empty[i], 1);
-    }
+    tc::mbar_init(&sh.sfa_full, 4);
+    tc::mbar_init(&sh.sfa_empty, 1);
     for (int i = 0; i < NVS; ++i) {
       tc::mbar_init(&sh.vfull[i], NGRP);
       tc::mbar_init(&sh.vempty[i], 1);
     }
     tc::mbar_init(&sh.s_full, 1);
     tc::mbar_init(&sh.s_empty, 8);
-    tc::mbar_init(&sh.p_full, 8);
-    tc::mbar_init(&sh.p_empty, 1);
+    tc::mbar_init(&sh.p_full[0], 8);
+    tc::mbar_init(&sh.p_full[1], 8);
+    tc::mbar_init(&sh.p_empty[0], 1);
+    tc::mbar_init(&sh.p_empty[1], 1);
     tc::mbar_init(&sh.q_full, 8);
     tc::mbar_init(&sh.o_empty, 8);
     tc::mbar_init(&sh.drain, 1);
@@ -558,8 +561,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           if (k != skipped && !tc::mbar_drain(&sh.kr_full[k % NKS], (k / NKS) & 1, lim)) report(a.err, PKV_DEVERR_TIMEOUT);
     }
     // ======================================================== V page producer
+    // For every global tile, every 128-channel chunk c, both pages: chunk c of the
+    // page (4 KB of codes, contiguous in the V layout) and its 512 bytes of block
+    // scales into one ring slot, in the order the dequantizers consume them.
     else if (warp == W_VPROD) {
-      int pi = 0;     // pages issued
+      int vi = 0;     // ring slots issued
       bool ok = true;
       long long x = x0;
       int g = g0;
@@ -568,36 +574,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int nt = tile_start[g + 1] - tile_start[g];
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
-        // pages [2*j0, pend) of the row: those of its NVFP4 tiles in this CTA's range
-        const int jp = min(j1, nt - 1);
-        const int pend = min(2 * jp, (u.n_glob + PKV_PAGE - 1) / PKV_PAGE);
-        for (int pb = 2 * j0; pb < pend && ok; pb += 32) {
-          int pl = -1;
-          if (pb + lane < pend) pl = a.page_table[(size_t)u.b * a.max_pages + pb + lane];
-          const int cnt = min(32, pend - pb);
-          for (int q = 0; q < cnt; ++q) {
-            int p = __shfl_sync(0xffffffffu, pl, q);
-            if (lane == 0) {
-              if (p < 0 || p >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); p = 0; }
-              const int slot = pi % NVR, use = pi / NVR;
-              if (!tc::mbar_wait(&sh.vr_empty[slot], (use & 1) ^ 1, abort_p, lim)) { fail(sh, a.err); ok = false; }
-              if (ok) {
-                tc::mbar_arrive_expect_tx(&sh.vr_full[slot], C::PSLOT);
-                uint8_t* dst = sV + slot * C::PSLOT;
-                tc::bulk_g2s(dst, a.cache.v_data + (size_t)p * pdb, C::PAGE_DATA, &sh.vr_full[slot]);
-                tc::bulk_g2s(dst + C::PAGE_DATA, a.cache.v_scale + (size_t)p * psb, C::PAGE_SCALE, &sh.vr_full[slot]);
-              }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            ++pi;
+        const int npr = (u.n_glob + PKV_PAGE - 1) / PKV_PAGE;
+        int pbase = -1, pl = -1;            // lane i holds page id pbase + i of the row
+        for (int j = j0; j < j1 && j < nt - 1 && ok; ++j) {
+          const int p0 = 2 * j, npg = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
+          if (pbase < 0 || p0 + 1 >= pbase + 32) {
+            pbase = p0;
+            pl = (pbase + lane < npr) ? a.page_table[(size_t)u.b * a.max_pages + pbase + lane] : -1;
           }
+          const int pid0 = __shfl_sync(0xffffffffu, pl, p0 - pbase);
+          const int pid1 = __shfl_sync(0xffffffffu, pl, p0 + 1 - pbase);
+          if (lane == 0) {
+            for (int c = 0; c < C::NVCH && ok; ++c)
+              for (int p = 0; p < npg && ok; ++p) {
+                int pid = p ? pid1 : pid0;
+                if (pid < 0 || pid >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); pid = 0; }
+                const int slot = vi % NVR, use = vi / NVR;
+                if (!tc::mbar_wait(&sh.vr_empty[slot], (use & 1) ^ 1, abort_p, lim)) { fail(sh, a.err); ok = false; }
+                if (ok) {
+                  tc::mbar_arrive_expect_tx(&sh.vr_full[slot], VSLOT);
+                  uint8_t* dst = sV + slot * VSLOT;
+                  tc::bulk_g2s(dst, a.cache.v_data + (size_t)pid * pdb + c * VCODES, VCODES, &sh.vr_full[slot]);
+                  tc::bulk_g2s(dst + VCODES, a.cache.v_scale + (size_t)pid * psb + c * VSCALES, VSCALES, &sh.vr_full[slot]);
+                  ++vi;
+                }
+              }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          vi = __shfl_sync(0xffffffffu, vi, 0);
         }
         x = tile_start[g] + j1;
         ++g;
       }
       if (lane == 0)
-        for (int k = (pi > NVR ? pi - NVR : 0); k < pi; ++k)
+        for (int k = (vi > NVR ? vi - NVR : 0); k < vi; ++k)
           if (!tc::mbar_drain(&sh.vr_full[k % NVR], (k / NVR) & 1, lim)) report(a.err, PKV_DEVERR_TIMEOUT);
     }
     // ======================================================== QK MMA issuer
@@ -628,26 +638,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           // S free (the previous tile copied out by the softmax)
           ok = ok && tc::mbar_wait(&sh.s_empty, (nq & 1) ^ 1, abort_p, lim);
           if (!win) {
-            const int slot = kt % NKS, buf = gt & 1;
+            const int slot = kt % NKS;
             ok = ok && tc::mbar_wait(&sh.kr_full[slot], (kt / NKS) & 1, abort_p, lim);
-            ok = ok && tc::mbar_wait(&sh.sfa_full[buf], (gt >> 1) & 1, abort_p, lim);
+            ok = ok && tc::mbar_wait(&sh.sfa_full, gt & 1, abort_p, lim);
             tc::compiler_fence();          // issue strictly after the waits
             if (!ok) break;
             tc::tc_fence_after();
             if (tc::elect_one()) {
+              // the tile's K codes into TMEM (read from shared memory once), then the
+              // shared-memory slot is released as soon as the copies are done
+#pragma unroll
+              for (int k = 0; k < C::KS; ++k) {
+                const int cb = (32 * k) / C::RB, kk = (32 * k) % C::RB;
+                tc::tmem_cp_128x256b(tbase + COL_KA + 8 * k,
+                                     dK + (uint64_t)((slot * C::KSLOT + cb * TILE * C::RB + kk) >> 4));
+              }
+              tc::mma_commit(&sh.kr_empty[slot]);
 #pragma unroll 1
               for (int t = 0; t < NQT; ++t) {
 #pragma unroll
                 for (int k = 0; k < C::KS; ++k) {
                   const int cb = (32 * k) / C::RB, kk = (32 * k) % C::RB;
-                  const uint64_t ad = dK + (uint64_t)((slot * C::KSLOT + cb * TILE * C::RB + kk) >> 4);
                   const uint64_t bd = dQ + (uint64_t)((t * C::QT_BYTES + cb * NH * C::RB + kk) >> 4);
-                  tc::mma_nvf4_ss(tbase + COL_S, ad, bd, idq, tbase + COL_SFA + 32 * buf + 4 * k, tbase + COL_SFB + 4 * t,
-                                  (t | k) != 0);
+                  tc::mma_nvf4_ts(tbase + COL_S, tbase + COL_KA + 8 * k, bd, idq, tbase + COL_SFA + 4 * k,
+                                  tbase + COL_SFB + 4 * t, (t | k) != 0);
                 }
               }
-              tc::mma_commit(&sh.sfa_empty[buf]);
-              tc::mma_commit(&sh.kr_empty[slot]);
+              tc::mma_commit(&sh.sfa_empty);
               tc::mma_commit(&sh.s_full);
             }
             __syncwarp();
@@ -690,41 +707,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       if (!tc::mbar_drain(&sh.drain, 0, lim) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     }
     // ======================================================== PV MMA issuer
+    // Per 128-channel chunk of a tile: O^T[chunk] += V^T P, 8 MMAs (M128 N64 K16)
+    // over the tile's 128 tokens; chunks come in order from the two dequant
+    // groups, alternating TMEM slots.
     else if (warp == W_PV) {
       const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
       const uint64_t dp0 = tc::sdesc_sw128(tc::smem_u32(sP), 8192, 1024);
-      int vs = 0, np = 0, ip = 0;
-      uint32_t vph = 0;          // V slot ring: slot, phase
+      int ci = 0, np = 0, ip = 0;   // chunks consumed, P tiles consumed, rows done
       bool ok = true;
       long long x = x0;
       int g = g0;
       while (x < x1 && ok) {
+        const Unit u = unit_of(a, g);
+        const int nt = tile_start[g + 1] - tile_start[g];
         const int j0 = (int)(x - tile_start[g]);
-        const int j1 = (int)min((long long)(tile_start[g + 1] - tile_start[g]), x1 - tile_start[g]);
+        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         // O of the previous item read out by the epilogue
         ok = tc::mbar_wait(&sh.o_empty, (ip & 1) ^ 1, abort_p, lim);
         ++ip;
         for (int j = j0; j < j1 && ok; ++j) {
-          ok = tc::mbar_wait(&sh.p_full, np & 1, abort_p, lim);
-          const uint64_t bpn = dp0;
-          // chunk order: page half 0 for every channel chunk, then page half 1
-          for (int cp = 0; cp < 2 * C::NVCH && ok; ++cp) {
-            const int slot = vs, half = cp / C::NVCH, c = cp % C::NVCH;
-            ok = tc::mbar_wait(&sh.vfull[slot], vph, abort_p, lim);
+          ok = tc::mbar_wait(&sh.p_full[np & 1], (np >> 1) & 1, abort_p, lim);
+          const uint64_t bpn = dp0 + (uint64_t)(((np & 1) * C::P_BYTES) >> 4);
+          // chunk k of the tile: 128 channels (c = k / halves) x 64 tokens (page half h = k % halves)
+          const int halves = (j == nt - 1 || TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
+          for (int k = 0; k < C::NVCH * halves && ok; ++k) {
+            const int slot = ci & 1, c = k / halves, h = k % halves;
+            ok = tc::mbar_wait(&sh.vfull[slot], (ci >> 1) & 1, abort_p, lim);
             tc::compiler_fence();
             if (!ok) break;
             tc::tc_fence_after();
             const uint32_t dO = tbase + COL_O + 64 * c, aV = tbase + COL_V + 32 * slot;
-            const uint64_t bp = bpn + (uint64_t)((half * 8192) >> 4);
+            const uint64_t bp = bpn + (uint64_t)((h * 8192) >> 4);
             if (tc::elect_one()) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                tc::mma_ts(dO, aV + 8 * k, bp + (uint64_t)(k * (2048 >> 4)), idV, !(j == j0 && half == 0 && k == 0));
+              for (int kk = 0; kk < 4; ++kk)
+                tc::mma_ts(dO, aV + 8 * kk, bp + (uint64_t)(kk * (2048 >> 4)), idV, !(j == j0 && h == 0 && kk == 0));
               tc::mma_commit(&sh.vempty[slot]);
-              if (cp == 2 * C::NVCH - 1) tc::mma_commit(&sh.p_empty);
+              if (k == C::NVCH * halves - 1) tc::mma_commit(&sh.p_empty[np & 1]);
             }
             __syncwarp();
-            if (++vs == NVS) { vs = 0; vph ^= 1; }
+            ++ci;
           }
           ++np;
         }
@@ -740,7 +762,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     // Thread m holds row m of the tile's S^T (page m/64, token m%64): it loads the
     // 4 scale bytes of each 64-channel K step of its token and stores them where
     // the block-scaled MMA reads row m's scales (lane m, column base + 4k + m/32).
-    // Two buffers: the scales of tile n+1 are written while tile n is contracted.
+    // One buffer: the scales of tile n+1 are loaded while tile n is contracted and
+    // stored as soon as its MMAs are complete.
     else if (warp < W_SF + 4) {
       const int m = 32 * (warp - W_SF) + lane;
       const uint32_t lb = lane_base(warp);
@@ -762,7 +785,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         for (int j = j0; j < j1 && j < nt - 1; ++j) {
-          const int buf = gt & 1;
           const int pos = TILE * j + m;
           uint32_t wrd[C::KS];
 #pragma unroll
@@ -778,7 +800,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               wrd[2 * q + 1] = v.y;
             }
           }
-          const bool w_ok = tc::mbar_wait(&sh.sfa_empty[buf], ((gt >> 1) & 1) ^ 1, abort_p, lim);
+          const bool w_ok = tc::mbar_wait(&sh.sfa_empty, (gt & 1) ^ 1, abort_p, lim);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
           tc::tc_fence_after();
           uint32_t r[4 * C::KS];
@@ -786,11 +808,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           for (int k = 0; k < C::KS; ++k)
 #pragma unroll
             for (int q = 0; q < 4; ++q) r[4 * k + q] = (q == (warp - W_SF)) ? wrd[k] : 0u;
-          st_sfa<C::KS>(tbase + lb + COL_SFA + 32 * buf, r);
+          st_sfa<C::KS>(tbase + lb + COL_SFA, r);
           tc::tc_wait_st();
           tc::tc_fence_before();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sh.sfa_full[buf]);
+          if (lane == 0) tc::mbar_arrive(&sh.sfa_full);
           ++gt;
         }
         x = tile_start[g] + j1;
@@ -798,20 +820,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       }
     }
     // ======================================================== V dequantizer (thread = channel)
-    // Two groups of four warps (one warp per TMEM lane quarter); the V^T chunks
-    // of a tile (128 channels x 64 tokens) are taken page-major - every channel
-    // chunk of page half 0, then of half 1 - and group vg converts the chunks of
-    // parity vg, a full 32-column slot each.  Each warp converts the E4M3 block
-    // scales it needs once (two per lane) and shares them through shared memory.
+    // Two groups of four warps (one warp per TMEM lane quarter) take the chunks of
+    // the tiles in turn: chunk k of a tile is 128 channels (k / halves) x the 64
+    // tokens of page half (k % halves), one V ring slot; group vg takes the chunk
+    // numbers (counted over the CTA's tiles) of parity vg, into its own 32-column
+    // TMEM slot.  Each warp converts the E4M3 block scales it needs once per chunk
+    // (two per lane) and shares them through shared memory; the ring slot is
+    // released as soon as its codes are read.
     else if (warp < W_SMAX) {
       const int vw = warp - W_VDEQ;                  // 0..7
       const int dl = 32 * (vw & 3) + lane;           // channel lane 0..127 within a chunk
-      const int vg = vw >> 2;                        // chunk parity of this group
+      const int vg = vw >> 2;                        // group: chunks of parity vg
       const uint32_t lb = lane_base(warp);
       const uint32_t vsc_s = tc::smem_u32(sh.vsc[vw]);
-      int vp = 0;               // pages consumed
-      int vs = vg;              // slot of this group's next chunk
-      uint32_t vph = 0;         // its phase
+      const uint32_t sv0 = tc::smem_u32(sV);
+      int vbase = 0;            // ring slots of the tiles before this one
+      int ci = 0;               // chunks of both groups before this one
+      int use = 0;              // uses of this group's TMEM slot
       bool ok = true;
       long long x = x0;
       int g = g0;
@@ -822,86 +847,75 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         for (int j = j0; j < j1 && ok; ++j) {
           const bool win = (j == nt - 1);
-          const int npg = win ? 0 : ((TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1);
+          const int halves = (win || TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
           const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
 #pragma unroll 1
-          for (int half = 0; half < 2 && ok; ++half) {       // tokens 64*half .. 64*half+63
-            const bool paged = half < npg;
-            if (paged) {
-              const bool w_ok = tc::mbar_wait(&sh.vr_full[(vp + half) % NVR], ((vp + half) / NVR) & 1, abort_p, lim);
+          for (int k = 0; k < C::NVCH * halves && ok; ++k, ++ci) {
+            if ((ci & 1) != vg) continue;
+            const int c = k / halves, h = k % halves;
+            const int d = 128 * c + dl;
+            uint32_t r[32];
+            if (!win) {
+              const int ri = vbase + k, rs = ri % NVR;
+              const bool w_ok = tc::mbar_wait(&sh.vr_full[rs], (ri / NVR) & 1, abort_p, lim);
               if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-            }
-            const uint32_t base = tc::smem_u32(sV) + ((vp + half) % NVR) * C::PSLOT;
-            // chunk cp = half * NVCH + c belongs to group cp & 1
-#pragma unroll 1
-            for (int c = (vg ^ (half * C::NVCH)) & 1; c < C::NVCH; c += 2) {
-              const int d = 128 * c + dl;
-              uint32_t r[32];
-              if (paged) {
-                // block scales of this warp's two channel blocks x 64 tokens: lane
-                // converts token pairs (lane & 15) and 16 + (lane & 15) of block (lane >> 4)
-                const int blk = ((128 * c + 32 * (vw & 3)) >> 4) + (lane >> 4);
-                const uint32_t sb = base + C::PAGE_DATA + blk * PKV_PAGE + 2 * (lane & 15);
-                const uint32_t s2a = tc::e4m3x2_to_f16x2(tc::lds16(sb));
-                const uint32_t s2b = tc::e4m3x2_to_f16x2(tc::lds16(sb + 32));
-                __syncwarp();                            // previous readers of vsc are done
-                tc::sts32(vsc_s + 4 * (lane >> 4) * 32 + 4 * (lane & 15), s2a);
-                tc::sts32(vsc_s + 4 * (lane >> 4) * 32 + 64 + 4 * (lane & 15), s2b);
-                __syncwarp();
-                const uint32_t sp = vsc_s + 128 * (lane >> 4);   // this channel's block: 32 pairs
-                const uint32_t wd = base + 4 * d;
-#pragma unroll
-                for (int o = 0; o < 8; ++o) {              // octet o of the page: tokens 8o .. 8o+7
-                  const uint32_t w = tc::lds32(wd + 4 * o * D);
-                  const uint4 s4 = tc::lds128(sp + 16 * o);
-                  const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
-                  uint32_t e[4];
-                  tc::e2m1x8_to_f16x2x4(w, e);
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) r[4 * o + i] = tc::hmul2(e[i], sv[i]);
-                }
-              } else if (win) {
-                const uint8_t* col = u.wv + d;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const int e = 64 * half + 2 * i;
-                  const uint32_t b0 = __ldg(col + (size_t)e * D), b1 = __ldg(col + (size_t)(e + 1) * D);
-                  r[i] = tc::e4m3x2_to_f16x2(b0 | (b1 << 8));
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = 0u;      // second page absent: no valid token
-              }
-              // zero the tokens beyond the valid count
-              const int t0 = 64 * half;
-              if (t0 + 64 > nvalid) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const int tt = t0 + 2 * i;
-                  if (tt >= nvalid) r[i] = 0u;
-                  else if (tt + 1 >= nvalid) r[i] &= 0xFFFFu;
-                }
-              }
-              tc::reg_fence32(r);             // conversion done before the (blocking) slot wait
-              const bool w_ok = tc::mbar_wait(&sh.vempty[vs], vph ^ 1, abort_p, lim);
-              if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-              tc::tmem_st32(tbase + lb + COL_V + 32 * vs, r);
-              tc::tc_wait_st();
-              tc::tc_fence_before();
+              const uint32_t base = sv0 + rs * VSLOT;
+              // block scales of this warp's two channel blocks x 64 tokens: lane
+              // converts token pairs (lane & 15) and 16 + (lane & 15) of block (lane >> 4)
+              const uint32_t sb = base + VCODES + (2 * (vw & 3) + (lane >> 4)) * PKV_PAGE + 2 * (lane & 15);
+              const uint32_t s2a = tc::e4m3x2_to_f16x2(tc::lds16(sb));
+              const uint32_t s2b = tc::e4m3x2_to_f16x2(tc::lds16(sb + 32));
+              __syncwarp();                            // previous readers of vsc are done
+              tc::sts32(vsc_s + 4 * (lane >> 4) * 32 + 4 * (lane & 15), s2a);
+              tc::sts32(vsc_s + 4 * (lane >> 4) * 32 + 64 + 4 * (lane & 15), s2b);
               __syncwarp();
-              if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
-              vs += 2;
-              if (vs >= NVS) { vs -= NVS; vph ^= 1; }
-            }
-            if (!ok) break;
-            if (paged) {
-              // every code of this page this warp needs is in TMEM now: release it
+              const uint32_t sp = vsc_s + 128 * (lane >> 4);   // this channel's block: 32 pairs
+              const uint32_t wd = base + 4 * dl;               // word (octet o, channel dl): o*512 + 4*dl
+#pragma unroll
+              for (int o = 0; o < 8; ++o) {              // octet o of the page: tokens 8o .. 8o+7
+                const uint32_t w = tc::lds32(wd + 512 * o);
+                const uint4 s4 = tc::lds128(sp + 16 * o);
+                const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+                uint32_t e[4];
+                tc::e2m1x8_to_f16x2x4(w, e);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) r[4 * o + i] = tc::hmul2(e[i], sv[i]);
+              }
+              tc::reg_fence32(r);                      // the slot's codes are in registers: release it
               __syncwarp();
-              if (lane == 0) tc::mbar_arrive(&sh.vr_empty[(vp + half) % NVR]);
+              if (lane == 0) tc::mbar_arrive(&sh.vr_empty[rs]);
+            } else {
+              const uint8_t* col = u.wv + d;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int e = 64 * h + 2 * i;
+                const uint32_t b0 = __ldg(col + (size_t)e * D), b1 = __ldg(col + (size_t)(e + 1) * D);
+                r[i] = tc::e4m3x2_to_f16x2(b0 | (b1 << 8));
+              }
             }
+            // zero the tokens beyond the valid count
+            const int t0 = 64 * h;
+            if (t0 + 64 > nvalid) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int tt = t0 + 2 * i;
+                if (tt >= nvalid) r[i] = 0u;
+                else if (tt + 1 >= nvalid) r[i] &= 0xFFFFu;
+              }
+            }
+            tc::reg_fence32(r);             // conversion done before the (blocking) slot wait
+            // the PV of this group's previous chunk has read the TMEM slot
+            const bool s_ok = tc::mbar_wait(&sh.vempty[vg], (use & 1) ^ 1, abort_p, lim);
+            if (!__all_sync(0xffffffffu, s_ok)) { fail(sh, a.err); ok = false; break; }
+            tc::tc_fence_after();
+            tc::tmem_st32(tbase + lb + COL_V + 32 * vg, r);
+            tc::tc_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.vfull[vg]);
+            ++use;
           }
-          if (!ok) break;
-          vp += npg;
+          if (!win) vbase += C::NVCH * halves;
         }
         x = tile_start[g] + j1;
         ++g;
@@ -963,8 +977,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sh.s_empty);
           // two passes of 16 heads (keeps 16 logits live instead of 32); the first
-          // pass's f16 P values wait in registers until the P buffer is free
-          const uint32_t prow = tc::smem_u32(sP) + (t >> 3) * 1024 + (t & 7) * 128;
+          // pass's f16 P values wait in registers until its P buffer is free
+          const int pb = ntile & 1;
+          const uint32_t prow = tc::smem_u32(sP) + pb * C::P_BYTES + (t >> 3) * 1024 + (t & 7) * 128;
 #pragma unroll
           for (int hq = 0; hq < 2; ++hq) {
             const int h0 = 32 * hh + 16 * hq;            // first head of this pass
@@ -1010,7 +1025,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               l[hq] *= sh.alpha[h0 + hs];
               if (j > j0) {
                 // every P.V into O so far (tile ntile-1 and earlier) must be complete
-                const bool pv_ok = tc::mbar_wait(&sh.p_empty, (ntile & 1) ^ 1, abort_p, lim);
+                const int kp = ntile - 1;
+                const bool pv_ok = tc::mbar_wait(&sh.p_empty[kp & 1], (kp >> 1) & 1, abort_p, lim);
                 if (tc::named_bar_or(3, 256, !pv_ok)) { fail(sh, a.err); ok = false; break; }
                 tc::tc_fence_after();
                 // O^T columns of these 16 heads, every channel chunk, times alpha
@@ -1050,8 +1066,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             }
             l[hq] += warp_sum16(sv, lane);
             if (hq == 0) {
-              // the P buffer is free once the P.V of the previous tile is done
-              w_ok = tc::mbar_wait(&sh.p_empty, (ntile & 1) ^ 1, abort_p, lim);
+              // P buffer ntile&1 is free once the P.V of tile ntile-2 is done
+              w_ok = tc::mbar_wait(&sh.p_empty[pb], ((ntile >> 1) & 1) ^ 1, abort_p, lim);
               if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
             }
             // row t of P (MN-major, 128-byte swizzle): heads 8c .. 8c+7 = 16-byte chunk c
@@ -1062,7 +1078,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           tc::fence_proxy_async_smem();
           tc::tc_fence_before();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sh.p_full);
+          if (lane == 0) tc::mbar_arrive(&sh.p_full[pb]);
           ++ntile;
           // the query form of the next tile (done here, where few registers are live):
           // the window's E4M3 terms after the row's last global tile, the next
@@ -1082,7 +1098,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         if (!ok) break;
         // ---- end of the item: wait for its last P.V, then write the partial
         const int klast = ntile - 1;       // P.V of the item's last tile done -> O complete
-        bool w_ok = tc::mbar_wait(&sh.p_empty, klast & 1, abort_p, lim);
+        bool w_ok = tc::mbar_wait(&sh.p_empty[klast & 1], (klast >> 1) & 1, abort_p, lim);
         if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
         tc::tc_fence_after();
         // l over all 128 token lanes: the four lane quarters are summed below

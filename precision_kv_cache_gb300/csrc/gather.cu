@@ -79,11 +79,11 @@ __global__ void __launch_bounds__(256) gather_kernel(pkv_kv_cache src, const int
     for (int i = 0; i < 8; ++i) {
       if (spage[i] >= 0) {
         const int ss = sslot[i];
-        const uint32_t sw = __ldg(reinterpret_cast<const uint32_t*>(src.v_data + (size_t)spage[i] * PD) + (ss >> 3) * D + c);
+        const uint32_t sw = __ldg(reinterpret_cast<const uint32_t*>(src.v_data + (size_t)spage[i] * PD) + VLayout<D>::word(ss, c));
         word |= ((sw >> (4 * (ss & 7))) & 0xFu) << (4 * i);
       }
     }
-    reinterpret_cast<uint32_t*>(dst.v_data + op * PD)[o * D + c] = word;
+    reinterpret_cast<uint32_t*>(dst.v_data + op * PD)[VLayout<D>::word(8 * o, c)] = word;
   }
   // ---- V scales: byte (block j, token s)
   for (int w = tid; w < 8 * (D / 16); w += 256) {

@@ -99,10 +99,13 @@ struct IdxLayout {
   __device__ __forceinline__ static int scale(int t, int j) { return (((j >> 3) * PKV_PAGE + t) << 3) + (j & 7); }
 };
 
+// V cache: channel-major 32-bit words grouped by 128-channel chunk,
+// [d/128 chunks][8 token octets][128 channels]: word (chunk c/128, octet t/8,
+// channel c%128) holds channel c of tokens 8*(t/8) .. 8*(t/8)+7 (nibble t%8), so
+// one 128-channel chunk of a page is one contiguous 4 KB run.
 template <int D>
 struct VLayout {
-  // 32-bit word holding channel c of tokens 8*(t/8) .. 8*(t/8)+7 (nibble t%8)
-  __device__ __forceinline__ static int word(int t, int c) { return (t >> 3) * D + c; }
+  __device__ __forceinline__ static int word(int t, int c) { return (((c >> 7) * 8 + (t >> 3)) << 7) + (c & 127); }
   __device__ __forceinline__ static int scale(int t, int j) { return j * PKV_PAGE + t; }
 };
 

@@ -308,3 +308,18 @@ def test_k_layout_rows_are_swizzled_operand_rows(d):
             for pos in range(R // 16):
                 logical = b * (R // 16) + (pos ^ w)
                 assert (row[16 * pos:16 * pos + 16] == packed[t, 16 * logical:16 * logical + 16]).all()
+
+
+def test_v_layout_chunks_are_contiguous_runs():
+    # d = 512: the words of channels 128c .. 128c+127 of all 64 tokens form one
+    # contiguous 4 KB run (chunk c), octet-major inside it
+    d = 512
+    p = C.Pools(1, d, "v")
+    codes = np.zeros((64, d), np.uint8)
+    codes[8:16, 300] = np.arange(1, 9)        # tokens 8..15 (octet 1), channel 300 (chunk 2, lane 44)
+    codes[0:8, 511] = 15                      # octet 0, last channel
+    p.store(0, np.arange(64), codes, np.zeros((64, 32), np.uint8))
+    w = p.data[0].view("<u4")
+    assert int(w[(2 * 8 + 1) * 128 + 44]) == 0x87654321
+    assert int(w[(3 * 8 + 0) * 128 + 127]) == 0xFFFFFFFF
+    assert np.count_nonzero(w) == 2
