@@ -69,18 +69,17 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
 // TMEM columns (512 allocated)
-constexpr int NVS = 2;                 // V chunk slots (one per dequant group)
+constexpr int NVS = 4;                 // V chunk slots (chunk i of the CTA in slot i % NVS)
 constexpr uint32_t COL_S = 0;          // S^T tile: 64 columns (fp32)
 constexpr uint32_t COL_SFA = 64;       // K block scales of a tile: 32 columns (4 per 64-channel K step)
 constexpr uint32_t COL_SFB = 96;       // query term weights: 4 columns per term
-constexpr uint32_t COL_KA = 128;       // the tile's K codes, A operand of S^T: 8 columns per 64-channel K step
-constexpr uint32_t COL_V = 192;        // V^T chunk slots: NVS x 32 columns (128 channels x 64 tokens, f16 pairs)
+constexpr uint32_t COL_V = 128;        // V^T chunk slots: NVS x 32 columns (128 channels x 64 tokens, f16 pairs)
 constexpr uint32_t COL_O = 256;        // O^T: 4 chunks x 64 columns
-static_assert(COL_SFA + 32 <= COL_SFB && COL_SFB + 32 <= COL_KA && COL_KA + 64 <= COL_V && COL_V + 32 * NVS <= COL_O,
-              "TMEM map");
+static_assert(COL_SFA + 32 <= COL_SFB && COL_SFB + 32 <= COL_V && COL_V + 32 * NVS <= COL_O, "TMEM map");
 
 constexpr int NKS = 2;                 // K tile slots (two pages each, or window chunks)
 constexpr int NVR = 10;                // V ring: slots of one 128-channel chunk of one page
+constexpr int VGRP = 4;                // V ring slots filled by one warp instruction (one lane each)
 constexpr int VCODES = 8 * 128 * 4;    // V codes of a 128-channel chunk of a page (8 octets x 128 words)
 constexpr int VSCALES = 8 * PKV_PAGE;  // its block scales (8 blocks x 64 tokens)
 constexpr int VSLOT = VCODES + VSCALES;
@@ -256,8 +255,7 @@ static_assert(NQT <= 5 && 4 * NQT <= 32, "term_scale_code covers five terms; one
 // rounded back to bf16 (nearest, ties to even) - the rotated query is a bf16
 // tensor like the query itself
 template <int D>
-__device__ __forceinline__ void load_q8(const AttnArgs& a, const uint16_t* qh, int c, int pos, float* x) {
-  const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + c));
+__device__ __forceinline__ void cvt_q8(const AttnArgs& a, uint4 v, int c, int pos, float* x) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -279,6 +277,11 @@ __device__ __forceinline__ void load_q8(const AttnArgs& a, const uint16_t* qh, i
       x[2 * i + 1] = __bfloat162float(__float2bfloat16_rn(y1));
     }
   }
+}
+
+template <int D>
+__device__ __forceinline__ void load_q8(const AttnArgs& a, const uint16_t* qh, int c, int pos, float* x) {
+  cvt_q8<D>(a, __ldg(reinterpret_cast<const uint4*>(qh + c)), c, pos, x);
 }
 
 // Write the query of row g into shared memory as the B operand of S^T = K Q^T,
@@ -311,14 +314,23 @@ __device__ __noinline__ void write_q(const AttnArgs& a, int g, bool e4m3_form, u
       pos = -1;
     }
   }
+  // max |q| over the head (of the rotated query in a fused decode); the
+  // 16-byte loads of a batch are all in flight at once
   float amax = 0.f;
   if (live) {
+    constexpr int NB = CPT / 8 < 8 ? CPT / 8 : 8;        // loads per batch
 #pragma unroll 1
-    for (int c = c0; c < c0 + CPT; c += 8) {
-      float x[8];
-      load_q8<D>(a, qh, c, pos, x);
+    for (int cb = c0; cb < c0 + CPT; cb += 8 * NB) {
+      uint4 raw[NB];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      for (int v = 0; v < NB; ++v) raw[v] = __ldg(reinterpret_cast<const uint4*>(qh + cb + 8 * v));
+#pragma unroll
+      for (int v = 0; v < NB; ++v) {
+        float x[8];
+        cvt_q8<D>(a, raw[v], cb + 8 * v, pos, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      }
     }
   }
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
@@ -511,27 +523,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             }
             const int pid0 = __shfl_sync(0xffffffffu, pl, p0 - pbase);
             const int pid1 = __shfl_sync(0xffffffffu, pl, p0 + 1 - pbase);
-            if (lane == 0) {
-              const int slot = kt % NKS, use = kt / NKS;
-              if (!tc::mbar_wait(&sh.kr_empty[slot], (use & 1) ^ 1, abort_p, lim)) { fail(sh, a.err); ok = false; }
-              if (ok) {
-                if (a.hook_skip_copy == kt && cta == 0) {
-                  skipped = kt;
-                } else {
-                  tc::mbar_arrive_expect_tx(&sh.kr_full[slot], (uint32_t)(npg * C::PAGE_DATA));
-                  uint8_t* dst = sK + slot * C::KSLOT;
-                  for (int p = 0; p < npg; ++p) {
-                    int pid = p ? pid1 : pid0;
-                    if (pid < 0 || pid >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); pid = 0; }
-                    for (int cb = 0; cb < C::NCB; ++cb)
-                      tc::bulk_g2s(dst + cb * (TILE * C::RB) + p * (PKV_PAGE * C::RB),
-                                   a.cache.k_data + (size_t)pid * pdb + cb * (PKV_PAGE * C::RB),
-                                   (uint32_t)(PKV_PAGE * C::RB), &sh.kr_full[slot]);
-                  }
+            const int slot = kt % NKS, use = kt / NKS;
+            if (lane == 0 && !tc::mbar_wait(&sh.kr_empty[slot], (use & 1) ^ 1, abort_p, lim)) {
+              fail(sh, a.err);
+              ok = false;
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok) {
+              if (a.hook_skip_copy == kt && cta == 0) {
+                skipped = kt;
+              } else {
+                if (lane == 0) tc::mbar_arrive_expect_tx(&sh.kr_full[slot], (uint32_t)(npg * C::PAGE_DATA));
+                __syncwarp();
+                // one lane per (page, column block): the tile's copies leave in one instruction
+                if (lane < npg * C::NCB) {
+                  const int p = lane / C::NCB, cb = lane % C::NCB;
+                  int pid = p ? pid1 : pid0;
+                  if (pid < 0 || pid >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); pid = 0; }
+                  tc::bulk_g2s(sK + slot * C::KSLOT + cb * (TILE * C::RB) + p * (PKV_PAGE * C::RB),
+                               a.cache.k_data + (size_t)pid * pdb + cb * (PKV_PAGE * C::RB),
+                               (uint32_t)(PKV_PAGE * C::RB), &sh.kr_full[slot]);
                 }
               }
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
             ++kt;
           } else {
             for (int s = 0; s < C::NWS && ok; ++s) {
@@ -584,24 +598,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           }
           const int pid0 = __shfl_sync(0xffffffffu, pl, p0 - pbase);
           const int pid1 = __shfl_sync(0xffffffffu, pl, p0 + 1 - pbase);
-          if (lane == 0) {
-            for (int c = 0; c < C::NVCH && ok; ++c)
-              for (int p = 0; p < npg && ok; ++p) {
-                int pid = p ? pid1 : pid0;
-                if (pid < 0 || pid >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); pid = 0; }
-                const int slot = vi % NVR, use = vi / NVR;
-                if (!tc::mbar_wait(&sh.vr_empty[slot], (use & 1) ^ 1, abort_p, lim)) { fail(sh, a.err); ok = false; }
-                if (ok) {
-                  tc::mbar_arrive_expect_tx(&sh.vr_full[slot], VSLOT);
-                  uint8_t* dst = sV + slot * VSLOT;
-                  tc::bulk_g2s(dst, a.cache.v_data + (size_t)pid * pdb + c * VCODES, VCODES, &sh.vr_full[slot]);
-                  tc::bulk_g2s(dst + VCODES, a.cache.v_scale + (size_t)pid * psb + c * VSCALES, VSCALES, &sh.vr_full[slot]);
-                  ++vi;
-                }
-              }
+          // the tile's chunk-pages (chunk c of page p is number c * npg + p) in groups
+          // of VGRP: lane i waits for the ring slot of chunk-page k + i and issues its
+          // two copies, so the copies of a group leave in one warp instruction
+          const int n = C::NVCH * npg;
+          for (int k = 0; k < n && ok; k += VGRP) {
+            const int ni = min(VGRP, n - k);
+            const int cp = k + lane, c = cp / npg, p = cp % npg;
+            const int slot = (vi + lane) % NVR, use = (vi + lane) / NVR;
+            bool w_ok = true;
+            if (lane < ni) w_ok = tc::mbar_wait(&sh.vr_empty[slot], (use & 1) ^ 1, abort_p, lim);
+            if (!__all_sync(0xffffffffu, w_ok)) {
+              if (lane == 0) fail(sh, a.err);
+              ok = false;
+              break;
+            }
+            if (lane < ni) {
+              int pid = p ? pid1 : pid0;
+              if (pid < 0 || pid >= a.cache.num_pages) { report(a.err, PKV_DEVERR_BAD_PAGE); pid = 0; }
+              tc::mbar_arrive_expect_tx(&sh.vr_full[slot], VSLOT);
+              uint8_t* dst = sV + slot * VSLOT;
+              tc::bulk_g2s(dst, a.cache.v_data + (size_t)pid * pdb + c * VCODES, VCODES, &sh.vr_full[slot]);
+              tc::bulk_g2s(dst + VCODES, a.cache.v_scale + (size_t)pid * psb + c * VSCALES, VSCALES, &sh.vr_full[slot]);
+            }
+            vi += ni;
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          vi = __shfl_sync(0xffffffffu, vi, 0);
         }
         x = tile_start[g] + j1;
         ++g;
@@ -645,25 +666,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             if (!ok) break;
             tc::tc_fence_after();
             if (tc::elect_one()) {
-              // the tile's K codes into TMEM (read from shared memory once), then the
-              // shared-memory slot is released as soon as the copies are done
-#pragma unroll
-              for (int k = 0; k < C::KS; ++k) {
-                const int cb = (32 * k) / C::RB, kk = (32 * k) % C::RB;
-                tc::tmem_cp_128x256b(tbase + COL_KA + 8 * k,
-                                     dK + (uint64_t)((slot * C::KSLOT + cb * TILE * C::RB + kk) >> 4));
-              }
-              tc::mma_commit(&sh.kr_empty[slot]);
 #pragma unroll 1
               for (int t = 0; t < NQT; ++t) {
 #pragma unroll
                 for (int k = 0; k < C::KS; ++k) {
                   const int cb = (32 * k) / C::RB, kk = (32 * k) % C::RB;
+                  const uint64_t ad = dK + (uint64_t)((slot * C::KSLOT + cb * TILE * C::RB + kk) >> 4);
                   const uint64_t bd = dQ + (uint64_t)((t * C::QT_BYTES + cb * NH * C::RB + kk) >> 4);
-                  tc::mma_nvf4_ts(tbase + COL_S, tbase + COL_KA + 8 * k, bd, idq, tbase + COL_SFA + 4 * k,
-                                  tbase + COL_SFB + 4 * t, (t | k) != 0);
+                  tc::mma_nvf4_ss(tbase + COL_S, ad, bd, idq, tbase + COL_SFA + 4 * k, tbase + COL_SFB + 4 * t,
+                                  (t | k) != 0);
                 }
               }
+              tc::mma_commit(&sh.kr_empty[slot]);
               tc::mma_commit(&sh.sfa_empty);
               tc::mma_commit(&sh.s_full);
             }
@@ -707,9 +721,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       if (!tc::mbar_drain(&sh.drain, 0, lim) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     }
     // ======================================================== PV MMA issuer
-    // Per 128-channel chunk of a tile: O^T[chunk] += V^T P, 8 MMAs (M128 N64 K16)
-    // over the tile's 128 tokens; chunks come in order from the two dequant
-    // groups, alternating TMEM slots.
+    // Per V chunk (128 channels x the 64 tokens of one page): O^T[chunk] += V^T P,
+    // 4 MMAs (M128 N64 K16); chunk i of the CTA comes from dequant group i % 2
+    // in TMEM slot i % NVS.
     else if (warp == W_PV) {
       const uint32_t idV = tc::idesc_f16(128, NH, false, true);    // B = P, MN-major
       const uint64_t dp0 = tc::sdesc_sw128(tc::smem_u32(sP), 8192, 1024);
@@ -731,8 +745,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           // chunk k of the tile: 128 channels (c = k / halves) x 64 tokens (page half h = k % halves)
           const int halves = (j == nt - 1 || TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
           for (int k = 0; k < C::NVCH * halves && ok; ++k) {
-            const int slot = ci & 1, c = k / halves, h = k % halves;
-            ok = tc::mbar_wait(&sh.vfull[slot], (ci >> 1) & 1, abort_p, lim);
+            const int slot = ci % NVS, c = k / halves, h = k % halves;
+            ok = tc::mbar_wait(&sh.vfull[slot], (ci / NVS) & 1, abort_p, lim);
             tc::compiler_fence();
             if (!ok) break;
             tc::tc_fence_after();
@@ -823,8 +837,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     // Two groups of four warps (one warp per TMEM lane quarter) take the chunks of
     // the tiles in turn: chunk k of a tile is 128 channels (k / halves) x the 64
     // tokens of page half (k % halves), one V ring slot; group vg takes the chunk
-    // numbers (counted over the CTA's tiles) of parity vg, into its own 32-column
-    // TMEM slot.  Each warp converts the E4M3 block scales it needs once per chunk
+    // numbers i (counted over the CTA's tiles) of parity vg, into the 32-column
+    // TMEM slot i % NVS.  Each warp converts the E4M3 block scales it needs once per chunk
     // (two per lane) and shares them through shared memory; the ring slot is
     // released as soon as its codes are read.
     else if (warp < W_SMAX) {
@@ -836,7 +850,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const uint32_t sv0 = tc::smem_u32(sV);
       int vbase = 0;            // ring slots of the tiles before this one
       int ci = 0;               // chunks of both groups before this one
-      int use = 0;              // uses of this group's TMEM slot
       bool ok = true;
       long long x = x0;
       int g = g0;
@@ -904,16 +917,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               }
             }
             tc::reg_fence32(r);             // conversion done before the (blocking) slot wait
-            // the PV of this group's previous chunk has read the TMEM slot
-            const bool s_ok = tc::mbar_wait(&sh.vempty[vg], (use & 1) ^ 1, abort_p, lim);
+            // the PV of the chunk NVS before this one has read the TMEM slot
+            const int vs = ci % NVS;
+            const bool s_ok = tc::mbar_wait(&sh.vempty[vs], ((ci / NVS) & 1) ^ 1, abort_p, lim);
             if (!__all_sync(0xffffffffu, s_ok)) { fail(sh, a.err); ok = false; break; }
             tc::tc_fence_after();
-            tc::tmem_st32(tbase + lb + COL_V + 32 * vg, r);
+            tc::tmem_st32(tbase + lb + COL_V + 32 * vs, r);
             tc::tc_wait_st();
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.vfull[vg]);
-            ++use;
+            if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
           }
           if (!win) vbase += C::NVCH * halves;
         }
