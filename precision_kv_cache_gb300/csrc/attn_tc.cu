@@ -17,7 +17,8 @@
 //     range per CTA (balanced to one tile).
 //   * S^T = K Q^T (M = 128 tokens, N = 64 heads) runs on the block-scaled FP4
 //     tensor-core contraction: A = the two K pages of a tile as stored (E2M1
-//     codes, K-major with the 128/64-byte swizzle), their E4M3 block scales in
+//     codes, K-major with the 128/64-byte swizzle; copied from shared memory
+//     into TMEM once per tile with tcgen05.cp), their E4M3 block scales in
 //     TMEM (written by warps 0-3, thread = tile row), B = the query written as a
 //     sum of NQT FP4 terms, q ~ sigma_h * sum_t c_t 8^-t (c_t E2M1 codes, one
 //     factor sigma_h per head applied to the logits; the term weights 8^-t are
@@ -69,13 +70,15 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
 // TMEM columns (512 allocated)
-constexpr int NVS = 4;                 // V chunk slots (chunk i of the CTA in slot i % NVS)
+constexpr int NVS = 2;                 // V chunk slots (chunk i of the CTA in slot i % NVS)
 constexpr uint32_t COL_S = 0;          // S^T tile: 64 columns (fp32)
 constexpr uint32_t COL_SFA = 64;       // K block scales of a tile: 32 columns (4 per 64-channel K step)
 constexpr uint32_t COL_SFB = 96;       // query term weights: 4 columns per term
-constexpr uint32_t COL_V = 128;        // V^T chunk slots: NVS x 32 columns (128 channels x 64 tokens, f16 pairs)
+constexpr uint32_t COL_KA = 128;       // the tile's K codes, A operand of S^T: 8 columns per 64-channel K step
+constexpr uint32_t COL_V = 192;        // V^T chunk slots: NVS x 32 columns (128 channels x 64 tokens, f16 pairs)
 constexpr uint32_t COL_O = 256;        // O^T: 4 chunks x 64 columns
-static_assert(COL_SFA + 32 <= COL_SFB && COL_SFB + 32 <= COL_V && COL_V + 32 * NVS <= COL_O, "TMEM map");
+static_assert(COL_SFA + 32 <= COL_SFB && COL_SFB + 32 <= COL_KA && COL_KA + 64 <= COL_V && COL_V + 32 * NVS <= COL_O,
+              "TMEM map");
 
 constexpr int NKS = 2;                 // K tile slots (two pages each, or window chunks)
 constexpr int NVR = 10;                // V ring: slots of one 128-channel chunk of one page
@@ -318,7 +321,7 @@ __device__ __noinline__ void write_q(const AttnArgs& a, int g, bool e4m3_form, u
   // 16-byte loads of a batch are all in flight at once
   float amax = 0.f;
   if (live) {
-    constexpr int NB = CPT / 8 < 8 ? CPT / 8 : 8;        // loads per batch
+    constexpr int NB = CPT / 8 < 4 ? CPT / 8 : 4;        // loads per batch
 #pragma unroll 1
     for (int cb = c0; cb < c0 + CPT; cb += 8 * NB) {
       uint4 raw[NB];
@@ -666,18 +669,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             if (!ok) break;
             tc::tc_fence_after();
             if (tc::elect_one()) {
+              // the tile's K codes into TMEM (read from shared memory once: the
+              // contraction then reads only the query terms from shared memory);
+              // the slot is released as soon as the copies are done
+#pragma unroll
+              for (int k = 0; k < C::KS; ++k) {
+                const int cb = (32 * k) / C::RB, kk = (32 * k) % C::RB;
+                tc::tmem_cp_128x256b(tbase + COL_KA + 8 * k,
+                                     dK + (uint64_t)((slot * C::KSLOT + cb * TILE * C::RB + kk) >> 4));
+              }
+              tc::mma_commit(&sh.kr_empty[slot]);
 #pragma unroll 1
               for (int t = 0; t < NQT; ++t) {
 #pragma unroll
                 for (int k = 0; k < C::KS; ++k) {
                   const int cb = (32 * k) / C::RB, kk = (32 * k) % C::RB;
-                  const uint64_t ad = dK + (uint64_t)((slot * C::KSLOT + cb * TILE * C::RB + kk) >> 4);
                   const uint64_t bd = dQ + (uint64_t)((t * C::QT_BYTES + cb * NH * C::RB + kk) >> 4);
-                  tc::mma_nvf4_ss(tbase + COL_S, ad, bd, idq, tbase + COL_SFA + 4 * k, tbase + COL_SFB + 4 * t,
-                                  (t | k) != 0);
+                  tc::mma_nvf4_ts(tbase + COL_S, tbase + COL_KA + 8 * k, bd, idq, tbase + COL_SFA + 4 * k,
+                                  tbase + COL_SFB + 4 * t, (t | k) != 0);
                 }
               }
-              tc::mma_commit(&sh.kr_empty[slot]);
               tc::mma_commit(&sh.sfa_empty);
               tc::mma_commit(&sh.s_full);
             }
