@@ -7,6 +7,7 @@ namespace pkv {
 
 struct AttnArgs {
   const uint16_t* q;          // bf16 bits [n_groups][H][D]
+  const uint8_t* qs;          // the query rows split into tensor-core terms (workspace, set by the launcher)
   pkv_kv_cache cache;
   const int32_t* page_table;  // [B][max_pages]
   int max_pages;

@@ -109,6 +109,13 @@ struct Cfg {
   static constexpr int OFF_K = OFF_P + 2 * P_BYTES;          // K tile slots
   static constexpr int OFF_V = OFF_K + NKS * KSLOT;          // V ring
   static constexpr int DYN = OFF_V + NVR * VSLOT + 1024;     // + alignment slack
+  // a query row split ahead of the attention (qsplit_kernel), in global memory:
+  // the FP4 terms, the E4M3 terms, then the two logit-factor vectors
+  static constexpr int QS_E4M3 = NQT * QT_BYTES;
+  static constexpr int QS_ZSG = QS_E4M3 + 2 * QW_BYTES;
+  static constexpr int QS_ZSW = QS_ZSG + NH * 4;
+  static constexpr int QS_ROW = (QS_ZSW + NH * 4 + 1023) / 1024 * 1024;
+  static constexpr int QSPLIT_DYN = QS_ZSG + 1024;
   static_assert(QT_BYTES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_K % 1024 == 0 && KSLOT % 1024 == 0 &&
                 OFF_V % 16 == 0, "operand tiles stay 1024-aligned");
   static_assert(KS * 4 <= 32, "K scales of a tile fit one 32-column buffer");
@@ -118,7 +125,7 @@ struct Shared {
   uint64_t kr_full[NKS], kr_empty[NKS], vr_full[NVR], vr_empty[NVR];
   uint64_t sfa_full, sfa_empty;
   uint64_t vfull[NVS], vempty[NVS];
-  uint64_t s_full, s_empty, p_full[2], p_empty[2], q_full, o_empty, drain, drain2;
+  uint64_t s_full, s_empty, p_full[2], p_empty[2], q_full, q_empty, o_empty, drain, drain2;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float m[NH];     // running max per head (log2 units)
@@ -301,7 +308,7 @@ __device__ __forceinline__ void load_q8(const AttnArgs& a, const uint16_t* qh, i
 //     factor is scale * tw_k * 2^k_h.
 // Writes the per-head logit factors (log2 units) to zs[h].
 template <int D>
-__device__ __noinline__ void write_q(const AttnArgs& a, int g, bool e4m3_form, uint8_t* sQ, float* zs, int st) {
+__device__ __forceinline__ void write_q(const AttnArgs& a, int g, bool e4m3_form, uint8_t* sQ, float* zs, int st) {
   using C = Cfg<D>;
   using KL = KLayout<D>;
   constexpr int CPT = D / 4;                 // channels per thread
@@ -321,7 +328,7 @@ __device__ __noinline__ void write_q(const AttnArgs& a, int g, bool e4m3_form, u
   // 16-byte loads of a batch are all in flight at once
   float amax = 0.f;
   if (live) {
-    constexpr int NB = CPT / 8 < 4 ? CPT / 8 : 4;        // loads per batch
+    constexpr int NB = CPT / 8 < 8 ? CPT / 8 : 8;        // loads per batch
 #pragma unroll 1
     for (int cb = c0; cb < c0 + CPT; cb += 8 * NB) {
       uint4 raw[NB];
@@ -423,6 +430,30 @@ __device__ __noinline__ void write_q(const AttnArgs& a, int g, bool e4m3_form, u
   tc::named_bar(1, 256);                               // zs[] complete before anyone reads it
 }
 
+// ---------------------------------------------------------------- query split
+// One CTA of 256 threads per query row: both forms of the row's query (FP4
+// terms for the NVFP4 tiles, E4M3 terms for the window tile) and their logit
+// factors, written once per row to global memory, where the attention CTAs of
+// the row copy them from.
+template <int D>
+__global__ void __launch_bounds__(256, 1) qsplit_kernel(AttnArgs a, uint8_t* __restrict__ qs) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t qs_raw[];
+  uint8_t* sq = (uint8_t*)(((uintptr_t)qs_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ alignas(16) float zs[2][NH];
+  const int g = blockIdx.x, st = threadIdx.x;
+  write_q<D>(a, g, false, sq, zs[0], st);
+  write_q<D>(a, g, true, sq + C::QS_E4M3, zs[1], st);
+  __syncthreads();
+  uint8_t* dst = qs + (size_t)g * C::QS_ROW;
+  for (int i = st; i < C::QS_ZSG / 16; i += 256)
+    reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(sq)[i];
+  if (st < NH) {
+    reinterpret_cast<float*>(dst + C::QS_ZSG)[st] = zs[0][st];
+    reinterpret_cast<float*>(dst + C::QS_ZSW)[st] = zs[1][st];
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap wmap,
@@ -462,7 +493,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     tc::mbar_init(&sh.p_full[1], 8);
     tc::mbar_init(&sh.p_empty[0], 1);
     tc::mbar_init(&sh.p_empty[1], 1);
-    tc::mbar_init(&sh.q_full, 8);
+    tc::mbar_init(&sh.q_full, 1);
+    tc::mbar_init(&sh.q_empty, 1);
     tc::mbar_init(&sh.o_empty, 8);
     tc::mbar_init(&sh.drain, 1);
     tc::mbar_init(&sh.drain2, 1);
@@ -506,9 +538,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         const int npr = (u.n_glob + PKV_PAGE - 1) / PKV_PAGE;       // pages of the row
         if (lane == 0) {
-          // the next query row's Q (read by the softmax at this row's end): warm L2
-          if (j0 == 0 && x1 > tile_start[g + 1] && g + 1 < a.n_groups && ((uintptr_t)a.q & 15u) == 0)
-            tc::bulk_prefetch_l2(a.q + (size_t)(g + 1) * a.H * D, (uint32_t)(a.H * D * 2));
           // the window V (read from global memory by the V dequantizers): warm L2
           if (j1 == nt && u.wv != last_win && ((uintptr_t)u.wv & 15u) == 0) {
             tc::bulk_prefetch_l2(u.wv, (uint32_t)(PKV_WINDOW * D));
@@ -644,6 +673,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const uint64_t dK = tc::sdesc_kmajor(sk, C::RB), dQ = tc::sdesc_kmajor(sq, C::RB);
       const uint64_t dKw = tc::sdesc_kmajor(sk, 128), dQw = tc::sdesc_kmajor(sq, 128);
       int kt = 0, gt = 0, nq = 0, iq = 0;
+      bool q_landed = true;      // the last query copy issued has been seen complete
       bool ok = true;
       long long x = x0;
       int g = g0;
@@ -654,10 +684,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         for (int j = j0; j < j1 && ok; ++j) {
           const bool win = (j == nt - 1);
           // the query form this tile reads (FP4 terms from the row's first global
-          // tile on, E4M3 terms for the window) has been written
+          // tile in range on, E4M3 terms for the window tile), copied from the
+          // rows split ahead once the previous form's MMAs are complete
           if (win || j == j0) {
+            if (iq > 0) ok = tc::mbar_wait(&sh.q_empty, (iq - 1) & 1, abort_p, lim);
+            if (!ok) break;
+            const uint32_t nb = win ? 2 * C::QW_BYTES : NQT * C::QT_BYTES;
+            const uint8_t* src = a.qs + (size_t)g * C::QS_ROW + (win ? C::QS_E4M3 : 0);
+            if (lane == 0) tc::mbar_arrive_expect_tx(&sh.q_full, nb);
+            __syncwarp();
+            if (lane < 16) tc::bulk_g2s(sQ + lane * (nb / 16), src + lane * (nb / 16), nb / 16, &sh.q_full);
             ok = tc::mbar_wait(&sh.q_full, iq & 1, abort_p, lim);
             ++iq;
+            q_landed = ok;
           }
           // S free (the previous tile copied out by the softmax)
           ok = ok && tc::mbar_wait(&sh.s_empty, (nq & 1) ^ 1, abort_p, lim);
@@ -691,6 +730,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               }
               tc::mma_commit(&sh.sfa_empty);
               tc::mma_commit(&sh.s_full);
+              // the row's last global tile in range: its FP4 query terms are free
+              if (j == min(j1, nt - 1) - 1) tc::mma_commit(&sh.q_empty);
             }
             __syncwarp();
             ++kt;
@@ -714,7 +755,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                       tc::mma_f8_ss(tbase + COL_S, ad, bd, idw, !(s == 0 && c == 0 && t == 0 && kk == 0));
                     }
                 tc::mma_commit(&sh.kr_empty[slot]);
-                if (s == C::NWS - 1) tc::mma_commit(&sh.s_full);
+                if (s == C::NWS - 1) {
+                  tc::mma_commit(&sh.s_full);
+                  tc::mma_commit(&sh.q_empty);       // the E4M3 query terms are free
+                }
               }
               __syncwarp();
               ++kt;
@@ -726,6 +770,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         ++g;
       }
       if (!ok && lane == 0) fail(sh, a.err);
+      // a query copy whose wait gave up must still land before the CTA exits
+      if (!q_landed && lane == 0 && !tc::mbar_drain(&sh.q_full, (iq - 1) & 1, lim)) report(a.err, PKV_DEVERR_TIMEOUT);
       // drain outstanding MMAs before TMEM is freed
       if (tc::elect_one()) tc::mma_commit(&sh.drain);
       __syncwarp();
@@ -958,22 +1004,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       bool ok = true;
       long long x = x0;
       int g = g0;
-      {
-        // the first query form this CTA needs: FP4 terms, or E4M3 terms when the
-        // range starts at a window tile
-        const int nt = tile_start[g + 1] - tile_start[g];
-        const bool first_win = (x0 - tile_start[g]) == nt - 1;
-        write_q<D>(a, g, first_win, sQ, first_win ? sh.zsw : sh.zsg, st);
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sh.q_full);
-      }
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
         const int nt = tile_start[g + 1] - tile_start[g];
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
-        const long long xn = tile_start[g] + j1;
-        if (st < NH) sh.m[st] = -INFINITY;
+        // the running max and the logit factors of the row's two query forms
+        // (split ahead, in global memory); every thread passed the previous
+        // row's closing barrier, so nobody reads the old ones any more
+        if (st < NH) {
+          const float* zr = reinterpret_cast<const float*>(a.qs + (size_t)g * C::QS_ROW);
+          sh.m[st] = -INFINITY;
+          sh.zsg[st] = __ldg(zr + C::QS_ZSG / 4 + st);
+          sh.zsw[st] = __ldg(zr + C::QS_ZSW / 4 + st);
+        }
         tc::named_bar(1, 256);
         // l of head 32*hh + 16*hq + hs over this warp's 32 tokens (both lanes of a pair hold it)
         const int hs = (lane >> 1) & 15;
@@ -1104,20 +1148,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sh.p_full[pb]);
           ++ntile;
-          // the query form of the next tile (done here, where few registers are live):
-          // the window's E4M3 terms after the row's last global tile, the next
-          // row's first form after this row's last tile in range.  Every S that
-          // read the current form has been consumed, so its MMAs are complete.
-          if (j == nt - 2 && j1 == nt) {
-            write_q<D>(a, g, true, sQ, sh.zsw, st);
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.q_full);
-          } else if (j == j1 - 1 && xn < x1) {
-            const bool nwin = (tile_start[g + 2] - tile_start[g + 1]) == 1;
-            write_q<D>(a, g + 1, nwin, sQ, nwin ? sh.zsw : sh.zsg, st);
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sh.q_full);
-          }
         }
         if (!ok) break;
         // ---- end of the item: wait for its last P.V, then write the partial
@@ -1163,9 +1193,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           }
         }
         tc::tc_fence_before();
-        tc::named_bar(1, 256);                 // sh.red / sh.m reads done before the next item resets them
+        tc::named_bar(1, 256);                 // sh.red / sh.m / zs reads done before the next item resets them
         if (lane == 0) tc::mbar_arrive(&sh.o_empty);
-        x = xn;
+        x = tile_start[g] + j1;
         ++g;
       }
     }
@@ -1290,8 +1320,11 @@ __global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups
 namespace {
 template <int D>
 cudaError_t set_attrs() {
-  return cudaFuncSetAttribute(pkv::tcattn::attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              pkv::tcattn::Cfg<D>::DYN);
+  const cudaError_t e = cudaFuncSetAttribute(pkv::tcattn::attn_tc_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, pkv::tcattn::Cfg<D>::DYN);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(pkv::tcattn::qsplit_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              pkv::tcattn::Cfg<D>::QSPLIT_DYN);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -1341,10 +1374,17 @@ static int tc_grid(int num_sms, int n_groups, int max_entries) {
   return (int)(tmax < num_sms ? tmax : num_sms);
 }
 
+static size_t qs_row_bytes(int D) {
+  using namespace pkv::tcattn;
+  return D == 128 ? Cfg<128>::QS_ROW : D == 256 ? Cfg<256>::QS_ROW : Cfg<512>::QS_ROW;
+}
+
+// [plan][partial O][partial LSE][split query rows (1024-aligned)]
 size_t pkv_attn_tc_ws_bytes(int num_sms, int H, int D, int n_groups, int max_entries) {
   const size_t rows = (size_t)tc_grid(num_sms, n_groups, max_entries) + n_groups;
   const size_t plan = (size_t)(n_groups + 1 + tc_grid(num_sms, n_groups, max_entries)) * 4;
-  return 256 + (plan + 255) / 256 * 256 + rows * H * D * 4 + rows * H * 4 + 256;
+  const size_t head = (plan + 255) / 256 * 256 + rows * H * D * 4 + rows * H * 4;
+  return 256 + (head + 1023) / 1024 * 1024 + (size_t)n_groups * qs_row_bytes(D) + 1024;
 }
 
 cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, float* out, float* out_lse,
@@ -1358,11 +1398,22 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   float* part_o = (float*)p;
   p += rows * a.H * a.D * 4;
   float* part_lse = (float*)p;
+  p += rows * a.H * 4;
+  p = (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+  a.qs = p;
   CUtensorMap wmap;
   const int nseq = a.replay ? a.n_groups / PKV_WINDOW : a.n_groups;
   cudaError_t e = window_map(a.wk, a.D, nseq * PKV_WINDOW, &wmap);
   if (e != cudaSuccess) return e;
   plan_kernel<<<1, 1024, 0, st>>>(a, tile_start, G);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  switch (a.D) {
+    case 128: qsplit_kernel<128><<<a.n_groups, 256, Cfg<128>::QSPLIT_DYN, st>>>(a, p); break;
+    case 256: qsplit_kernel<256><<<a.n_groups, 256, Cfg<256>::QSPLIT_DYN, st>>>(a, p); break;
+    case 512: qsplit_kernel<512><<<a.n_groups, 256, Cfg<512>::QSPLIT_DYN, st>>>(a, p); break;
+    default: return cudaErrorInvalidValue;
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (e0 && e1) cudaEventRecord(e0, st);
@@ -1387,6 +1438,6 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   ep.err = a.err;
   merge_tc_kernel<<<a.n_groups * a.H, a.D / 4, 0, st>>>(tile_start, a.n_groups, G, a.H, a.D, part_o, part_lse,
                                                         out, out_lse, ep);
-  *n_launches = 3;
+  *n_launches = 4;
   return cudaGetLastError();
 }
