@@ -115,7 +115,6 @@ struct Cfg {
   static constexpr int QS_ZSG = QS_E4M3 + 2 * QW_BYTES;
   static constexpr int QS_ZSW = QS_ZSG + NH * 4;
   static constexpr int QS_ROW = (QS_ZSW + NH * 4 + 1023) / 1024 * 1024;
-  static constexpr int QSPLIT_DYN = QS_ZSG + 1024;
   static_assert(QT_BYTES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_K % 1024 == 0 && KSLOT % 1024 == 0 &&
                 OFF_V % 16 == 0, "operand tiles stay 1024-aligned");
   static_assert(KS * 4 <= 32, "K scales of a tile fit one 32-column buffer");
@@ -289,14 +288,10 @@ __device__ __forceinline__ void cvt_q8(const AttnArgs& a, uint4 v, int c, int po
   }
 }
 
-template <int D>
-__device__ __forceinline__ void load_q8(const AttnArgs& a, const uint16_t* qh, int c, int pos, float* x) {
-  cvt_q8<D>(a, __ldg(reinterpret_cast<const uint4*>(qh + c)), c, pos, x);
-}
 
-// Write the query of row g into shared memory as the B operand of S^T = K Q^T,
-// called by the 256 softmax threads; thread st takes head st/4, channels
-// (st%4)*D/4 .. +D/4.  Heads >= H are zero.
+// ---------------------------------------------------------------- query split
+// Both forms of a query row as the B operand of S^T = K Q^T, written once per
+// row to global memory (the attention CTAs of the row copy them in):
 //   fp4 form (global tiles): per head, x = q * 4/amax_h in [-4, 4];
 //     c_0 = E2M1(x), c_t = E2M1(8 (r_{t-1} ...)): x ~ sum_t c_t 8^-t, the codes
 //     stored as NQT K-major FP4 terms [NCB][64 heads][RB] (swizzle as the K
@@ -306,85 +301,80 @@ __device__ __forceinline__ void load_q8(const AttnArgs& a, const uint16_t* qh, i
 //     |x| <= 448), t1 = E4M3(x), t2 = E4M3(x - t1) (exact for a bf16 q), two
 //     K-major E4M3 terms [D/128][64 heads][128] (128-byte swizzle); the logit
 //     factor is scale * tw_k * 2^k_h.
-// Writes the per-head logit factors (log2 units) to zs[h].
+// plus the per-head logit factors (log2 units) of each form.  Grid: (row,
+// group of 256 / (D/32) heads); thread st takes head st / (D/32) of the group
+// and its 32 channels 32 * (st % (D/32)) ..; heads >= H are written as zero.
 template <int D>
-__device__ __forceinline__ void write_q(const AttnArgs& a, int g, bool e4m3_form, uint8_t* sQ, float* zs, int st) {
+__global__ void __launch_bounds__(256) qsplit_kernel(AttnArgs a, uint8_t* __restrict__ qs) {
   using C = Cfg<D>;
   using KL = KLayout<D>;
-  constexpr int CPT = D / 4;                 // channels per thread
-  const int h = st >> 2, part = st & 3;
-  const int c0 = part * CPT;
+  constexpr int PARTS = D / 32;              // threads per head
+  constexpr int HPB = 256 / PARTS;           // heads per block
+  const int g = blockIdx.x, st = threadIdx.x;
+  const int h = blockIdx.y * HPB + st / PARTS, part = st % PARTS;
+  const int c0 = 32 * part;
   const bool live = h < a.H;
-  const uint16_t* qh = a.q + ((size_t)g * a.H + (live ? h : 0)) * D;
   int pos = -1;
   if (a.rope_dim > 0) {
     pos = a.rope_pos[g];
     if (pos < 0 || pos >= a.max_pos) {
-      if (st == 0) report(a.err, PKV_DEVERR_BAD_PAGE);
+      if (st == 0 && blockIdx.y == 0) report(a.err, PKV_DEVERR_BAD_PAGE);
       pos = -1;
     }
   }
-  // max |q| over the head (of the rotated query in a fused decode); the
-  // 16-byte loads of a batch are all in flight at once
-  float amax = 0.f;
+  // the thread's 32 channels (turned in a fused decode), all loads in flight at once
+  float x[32];
   if (live) {
-    constexpr int NB = CPT / 8 < 8 ? CPT / 8 : 8;        // loads per batch
-#pragma unroll 1
-    for (int cb = c0; cb < c0 + CPT; cb += 8 * NB) {
-      uint4 raw[NB];
+    const uint16_t* qh = a.q + ((size_t)g * a.H + h) * D + c0;
+    uint4 raw[4];
 #pragma unroll
-      for (int v = 0; v < NB; ++v) raw[v] = __ldg(reinterpret_cast<const uint4*>(qh + cb + 8 * v));
+    for (int v = 0; v < 4; ++v) raw[v] = __ldg(reinterpret_cast<const uint4*>(qh) + v);
 #pragma unroll
-      for (int v = 0; v < NB; ++v) {
-        float x[8];
-        cvt_q8<D>(a, raw[v], cb + 8 * v, pos, x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-      }
-    }
-  }
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  const uint32_t sq = tc::smem_u32(sQ);
-  if (!e4m3_form) {
-    const float inv = amax > 0.f ? 4.f / amax : 0.f;
-    if (part == 0) zs[h] = amax > 0.f ? a.scale * a.cache.ts_k * LOG2E / (8.f * inv) : 0.f;
-#pragma unroll 1
-    for (int c = c0; c < c0 + CPT; c += 32) {          // one 16-byte chunk of each term
-      uint32_t w[NQT][4];
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        float x[8];
-        if (live) {
-          load_q8<D>(a, qh, c + 8 * v, pos, x);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] *= inv;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = 0.f;
-        }
-#pragma unroll
-        for (int t = 0; t < NQT; ++t) {
-          uint32_t word = 0u;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t b = tc::f32x2_to_e2m1x2(x[2 * i], x[2 * i + 1]);
-            word |= b << (8 * i);
-            if (t + 1 < NQT) {
-              const uint32_t v2 = tc::e2m1x2_to_f16x2(b);
-              x[2 * i] = 8.f * (x[2 * i] - tc::f16_lo_to_f32(v2));
-              x[2 * i + 1] = 8.f * (x[2 * i + 1] - tc::f16_hi_to_f32(v2));
-            }
-          }
-          w[t][v] = word;
-        }
-      }
-      const int off = KL::chunk(h, c / 32);            // head row h of a term, as token row h of a page
-#pragma unroll
-      for (int t = 0; t < NQT; ++t)
-        tc::sts128(sq + t * C::QT_BYTES + off, make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]));
-    }
+    for (int v = 0; v < 4; ++v) cvt_q8<D>(a, raw[v], c0 + 8 * v, pos, x + 8 * v);
   } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = 0.f;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int o = 1; o < PARTS; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  uint8_t* dst = qs + (size_t)g * C::QS_ROW;
+  {
+    // FP4 terms: one 16-byte chunk of each term
+    const float inv = amax > 0.f ? 4.f / amax : 0.f;
+    if (part == 0)
+      reinterpret_cast<float*>(dst + C::QS_ZSG)[h] = amax > 0.f ? a.scale * a.cache.ts_k * LOG2E / (8.f * inv) : 0.f;
+    uint32_t w[NQT][4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = x[8 * v + i] * inv;
+#pragma unroll
+      for (int t = 0; t < NQT; ++t) {
+        uint32_t word = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t b = tc::f32x2_to_e2m1x2(y[2 * i], y[2 * i + 1]);
+          word |= b << (8 * i);
+          if (t + 1 < NQT) {
+            const uint32_t v2 = tc::e2m1x2_to_f16x2(b);
+            y[2 * i] = 8.f * (y[2 * i] - tc::f16_lo_to_f32(v2));
+            y[2 * i + 1] = 8.f * (y[2 * i + 1] - tc::f16_hi_to_f32(v2));
+          }
+        }
+        w[t][v] = word;
+      }
+    }
+    const int off = KL::chunk(h, part);            // head row h of a term, as token row h of a page
+#pragma unroll
+    for (int t = 0; t < NQT; ++t)
+      *reinterpret_cast<uint4*>(dst + t * C::QT_BYTES + off) = make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]);
+  }
+  {
+    // E4M3 terms: two 16-channel chunks of each term
     int k = 0;
     if (amax > 0.f) {
       const uint32_t u = __float_as_uint(amax / 448.f);
@@ -393,64 +383,28 @@ __device__ __forceinline__ void write_q(const AttnArgs& a, int g, bool e4m3_form
     }
     const float down = __uint_as_float((uint32_t)(127 - k) << 23);   // 2^-k
     const float up = __uint_as_float((uint32_t)(127 + k) << 23);     // 2^k
-    if (part == 0) zs[h] = amax > 0.f ? a.scale * a.tw_k * up * LOG2E : 0.f;
-#pragma unroll 1
-    for (int c = c0; c < c0 + CPT; c += 16) {          // 16 channels = one 16-byte chunk of each term
+    if (part == 0) reinterpret_cast<float*>(dst + C::QS_ZSW)[h] = amax > 0.f ? a.scale * a.tw_k * up * LOG2E : 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int c = c0 + 16 * half;
       uint32_t w1[4], w2[4];
 #pragma unroll
-      for (int v = 0; v < 2; ++v) {
-        float x[8];
-        if (live) {
-          load_q8<D>(a, qh, c + 8 * v, pos, x);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] *= down;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; i += 2) {
-          const uint32_t b0 = tc::f32x2_to_e4m3x2(x[2 * i], x[2 * i + 1]);
-          const uint32_t b1 = tc::f32x2_to_e4m3x2(x[2 * i + 2], x[2 * i + 3]);
-          const uint32_t v0 = tc::e4m3x2_to_f16x2(b0), v1 = tc::e4m3x2_to_f16x2(b1);
-          const uint32_t r0 = tc::f32x2_to_e4m3x2(x[2 * i] - tc::f16_lo_to_f32(v0), x[2 * i + 1] - tc::f16_hi_to_f32(v0));
-          const uint32_t r1 = tc::f32x2_to_e4m3x2(x[2 * i + 2] - tc::f16_lo_to_f32(v1),
-                                                  x[2 * i + 3] - tc::f16_hi_to_f32(v1));
-          w1[2 * v + i / 2] = b0 | (b1 << 16);
-          w2[2 * v + i / 2] = r0 | (r1 << 16);
-        }
+      for (int i = 0; i < 8; i += 2) {
+        const float* y = x + 16 * half + 2 * i;
+        const float y0 = y[0] * down, y1 = y[1] * down, y2 = y[2] * down, y3 = y[3] * down;
+        const uint32_t b0 = tc::f32x2_to_e4m3x2(y0, y1);
+        const uint32_t b1 = tc::f32x2_to_e4m3x2(y2, y3);
+        const uint32_t v0 = tc::e4m3x2_to_f16x2(b0), v1 = tc::e4m3x2_to_f16x2(b1);
+        const uint32_t r0 = tc::f32x2_to_e4m3x2(y0 - tc::f16_lo_to_f32(v0), y1 - tc::f16_hi_to_f32(v0));
+        const uint32_t r1 = tc::f32x2_to_e4m3x2(y2 - tc::f16_lo_to_f32(v1), y3 - tc::f16_hi_to_f32(v1));
+        w1[i / 2] = b0 | (b1 << 16);
+        w2[i / 2] = r0 | (r1 << 16);
       }
       const int ch = c / 128, sub = (c % 128) / 16;
       const int off = ch * (NH * 128) + h * 128 + 16 * (sub ^ (h & 7));
-      tc::sts128(sq + off, make_uint4(w1[0], w1[1], w1[2], w1[3]));
-      tc::sts128(sq + C::QW_BYTES + off, make_uint4(w2[0], w2[1], w2[2], w2[3]));
+      *reinterpret_cast<uint4*>(dst + C::QS_E4M3 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+      *reinterpret_cast<uint4*>(dst + C::QS_E4M3 + C::QW_BYTES + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
     }
-  }
-  tc::fence_proxy_async_smem();
-  tc::named_bar(1, 256);                               // zs[] complete before anyone reads it
-}
-
-// ---------------------------------------------------------------- query split
-// One CTA of 256 threads per query row: both forms of the row's query (FP4
-// terms for the NVFP4 tiles, E4M3 terms for the window tile) and their logit
-// factors, written once per row to global memory, where the attention CTAs of
-// the row copy them from.
-template <int D>
-__global__ void __launch_bounds__(256, 1) qsplit_kernel(AttnArgs a, uint8_t* __restrict__ qs) {
-  using C = Cfg<D>;
-  extern __shared__ uint8_t qs_raw[];
-  uint8_t* sq = (uint8_t*)(((uintptr_t)qs_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ alignas(16) float zs[2][NH];
-  const int g = blockIdx.x, st = threadIdx.x;
-  write_q<D>(a, g, false, sq, zs[0], st);
-  write_q<D>(a, g, true, sq + C::QS_E4M3, zs[1], st);
-  __syncthreads();
-  uint8_t* dst = qs + (size_t)g * C::QS_ROW;
-  for (int i = st; i < C::QS_ZSG / 16; i += 256)
-    reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(sq)[i];
-  if (st < NH) {
-    reinterpret_cast<float*>(dst + C::QS_ZSG)[st] = zs[0][st];
-    reinterpret_cast<float*>(dst + C::QS_ZSW)[st] = zs[1][st];
   }
 }
 
@@ -1320,11 +1274,8 @@ __global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups
 namespace {
 template <int D>
 cudaError_t set_attrs() {
-  const cudaError_t e = cudaFuncSetAttribute(pkv::tcattn::attn_tc_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, pkv::tcattn::Cfg<D>::DYN);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(pkv::tcattn::qsplit_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              pkv::tcattn::Cfg<D>::QSPLIT_DYN);
+  return cudaFuncSetAttribute(pkv::tcattn::attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              pkv::tcattn::Cfg<D>::DYN);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -1409,9 +1360,9 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   switch (a.D) {
-    case 128: qsplit_kernel<128><<<a.n_groups, 256, Cfg<128>::QSPLIT_DYN, st>>>(a, p); break;
-    case 256: qsplit_kernel<256><<<a.n_groups, 256, Cfg<256>::QSPLIT_DYN, st>>>(a, p); break;
-    case 512: qsplit_kernel<512><<<a.n_groups, 256, Cfg<512>::QSPLIT_DYN, st>>>(a, p); break;
+    case 128: qsplit_kernel<128><<<dim3(a.n_groups, 1), 256, 0, st>>>(a, p); break;
+    case 256: qsplit_kernel<256><<<dim3(a.n_groups, 2), 256, 0, st>>>(a, p); break;
+    case 512: qsplit_kernel<512><<<dim3(a.n_groups, 4), 256, 0, st>>>(a, p); break;
     default: return cudaErrorInvalidValue;
   }
   e = cudaGetLastError();
