@@ -51,6 +51,7 @@ FUSED = ("c1f", "c3f")             # the decode as one fused call: query RoPE, a
 SWEEP = {f"s{L // 1024}k": L for L in W.LONG_CONTEXT}     # long-context decode sweep (--sweep)
 SCORE_SWEEP = {f"x{L // 1024}k": L for L in W.LONG_CONTEXT}   # index-scoring sweep (--score-sweep)
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 << 20
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -357,6 +358,14 @@ def run_gpu(args, rank, world, pool):
         pos = (seq_len - 1).to(torch.int32)
     torch.cuda.synchronize()
     setup_s = time.time() - t_setup
+    # L2 flush between timed steps when the step's bytes would largely fit the 129 MB L2
+    ws_bytes = needed_bytes(wl, fused=fused)[0] if not wl.topk else 0
+    flush_l2 = args.flush_l2 == "on" or (args.flush_l2 == "auto" and (wl.topk or ws_bytes < 4 * L2_BYTES))
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush_l2 else None
+
+    def flush():
+        if flush_buf is not None:
+            flush_buf.fill_(1)          # writes twice the L2 capacity: nothing of the step stays resident
 
     def step(ev=None):
         if wl.append:
@@ -393,9 +402,13 @@ def run_gpu(args, rank, world, pool):
     n0 = ctx.pkv_launch_count()
     if args.profile_region:
         torch.cuda.profiler.start()
+    step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t0e.record()
     for i in range(args.steps):
+        flush()
+        step_evs[i][0].record()
         step(evs[i])
+        step_evs[i][1].record()
     t1e.record()
     torch.cuda.synchronize()
     if args.profile_region:
@@ -404,8 +417,9 @@ def run_gpu(args, rank, world, pool):
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms_step = t0e.elapsed_time(t1e) / args.steps
-    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # medians over the timed steps (each step between its own pair of events)
+    ms_step = statistics.median(a.elapsed_time(b) for a, b in step_evs)
+    kern_ms = statistics.median(a.elapsed_time(b) for a, b in evs)
     ms_step, kern_ms = max_over_ranks([ms_step, kern_ms], world, dev)
     ms_eager = ms_step
     graph = getattr(args, "graph", False)
@@ -425,13 +439,14 @@ def run_gpu(args, rank, world, pool):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record()
-        for _ in range(args.steps):
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush()
+            gev[i][0].record()
             g.replay()
-        g1.record()
+            gev[i][1].record()
         torch.cuda.synchronize()
-        ms_step = max_over_ranks([g0.elapsed_time(g1) / args.steps], world, dev)[0]
+        ms_step = max_over_ranks([statistics.median(a.elapsed_time(b) for a, b in gev)], world, dev)[0]
     if ctx.pkv_get_error() != P.OK:
         raise RuntimeError("device error in the timed region")
 
@@ -480,41 +495,53 @@ def run_gpu(args, rank, world, pool):
                     "hbm_gbs": round(achieved, 2)}
     launches_per_step = (n1 - n0) / args.steps
 
-    # ---- end to end through the public API with host buffers
-    e2e = None
-    if not wl.topk:
-        qh = torch.from_numpy(q_host.view(np.int16)).pin_memory()
-        o_dev = out8 if fused else out
-        oh = torch.empty(o_dev.shape, dtype=o_dev.dtype).pin_memory()
-        lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-        kh = vh = None
-        if wl.append:
-            kh = torch.from_numpy(wl.new_rows(W.T_KNEW)).pin_memory()
-            vh = torch.from_numpy(wl.new_rows(W.T_VNEW)).pin_memory()
-        n_e2e = max(3, min(args.steps, 50))
+    # ---- end to end through the public API with host buffers: every step copies its
+    # inputs in from pinned host memory (the bf16 query, the appended K/V rows, for
+    # the sparse path the float32 index query, quantized to FP8 on the device) and
+    # its results out (O or its FP8 form, LSE, the selected positions)
+    qh = torch.from_numpy(q_host.view(np.int16)).pin_memory()
+    o_dev = out8 if fused else out
+    oh = torch.empty(o_dev.shape, dtype=o_dev.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    kh = vh = None
+    if wl.append:
+        kh = torch.from_numpy(wl.new_rows(W.T_KNEW)).pin_memory()
+        vh = torch.from_numpy(wl.new_rows(W.T_VNEW)).pin_memory()
+    qfh = qf_dev = selh = None
+    if wl.topk:
+        qfh = torch.from_numpy(np.ascontiguousarray(qf)).pin_memory()
+        qf_dev = torch.empty(qfh.shape, dtype=torch.float32, device=dev)
+        selh = torch.empty(sel.shape, dtype=torch.int32).pin_memory()
+    n_e2e = max(3, min(args.steps, 50))
 
-        def e2e_step():
-            q.view(torch.int16).copy_(qh, non_blocking=True)
-            if wl.append:
-                knew.copy_(kh, non_blocking=True)
-                vnew.copy_(vh, non_blocking=True)
-            step()
-            oh.copy_(o_dev, non_blocking=True)
-            lh.copy_(lse, non_blocking=True)
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(n_e2e):
-            e2e_step()
-        b2.record()
-        torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b2) / n_e2e
-        bi = qh.numel() * 2 + (kh.numel() * 4 * 2 if wl.append else 0)
-        bo = oh.numel() * oh.element_size() + lh.numel() * 4
-        e2e = {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+    def e2e_step():
+        q.view(torch.int16).copy_(qh, non_blocking=True)
+        if wl.append:
+            knew.copy_(kh, non_blocking=True)
+            vnew.copy_(vh, non_blocking=True)
+        if wl.topk:
+            qf_dev.copy_(qfh, non_blocking=True)
+            P.pkv_quantize_fp8(qf_dev, tq, qidx)
+        step()
+        oh.copy_(o_dev, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+        if wl.topk:
+            selh.copy_(sel, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
+    for i in range(n_e2e):
+        flush()
+        e2e_evs[i][0].record()
+        e2e_step()
+        e2e_evs[i][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = statistics.median(a.elapsed_time(b) for a, b in e2e_evs)
+    bi = qh.numel() * 2 + (kh.numel() * 4 * 2 if wl.append else 0) + (qfh.numel() * 4 if wl.topk else 0)
+    bo = oh.numel() * oh.element_size() + lh.numel() * 4 + (selh.numel() * 4 if wl.topk else 0)
+    e2e = {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+           "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
 
     res = {
         "metric": "decode-attention KV GB/s (needed bytes / step time)",
@@ -525,7 +552,9 @@ def run_gpu(args, rank, world, pool):
         "data": "synthetic (seeded N(0,1), 2% channels x8, bf16 Q; no trained weights)",
         "config": {"workload": workload_desc(name), "name": wl.name, "batch": B, "heads": H, "d": d,
                    "tokens_read": int(tokens), "needed_bytes_per_step": int(step_bytes),
-                   "l2": "working set > 129 MB L2; no flush between steps"},
+                   "l2": ("L2 flushed (256 MB written) before every timed step" if flush_l2
+                          else "working set > 4x the 129 MB L2; no flush between steps"),
+                   "timing": "median over the timed steps"},
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2), "hbm_peak_kind": peak_kind,
         "pct_of_8TBps_nominal": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "seq_per_s": round(B * world / (ms_step * 1e-3), 1),
@@ -534,8 +563,7 @@ def run_gpu(args, rank, world, pool):
         "setup_s": round(setup_s, 1),
         "step_mode": "cuda graph replay" if graph else "eager", "ms_per_step_eager": round(ms_eager, 4),
     }
-    if e2e:
-        res["e2e"] = e2e
+    res["e2e"] = e2e
     return res, wl
 
 
@@ -768,6 +796,8 @@ def main():
                     help="long-context decode sweep (32K-512K tokens, >= 1 GiB of KV per step): one line per length")
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flush-l2", choices=["auto", "on", "off"], default="auto",
+                    help="write 256 MB before every timed step (auto: when the step's bytes are < 4x the L2)")
     ap.add_argument("--profile-region", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()
