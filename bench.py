@@ -49,6 +49,7 @@ WORKLOADS = {"c1": 1, "c2": 2, "c3": 3, "c4": 4, "c3c": 3, "c1f": 1, "c3f": 3}
 CAND_C3C = 16384                   # c3c: the sparse workload scoring a fixed candidate set per sequence
 FUSED = ("c1f", "c3f")             # the decode as one fused call: query RoPE, attention, inverse RoPE, FP8 O
 SWEEP = {f"s{L // 1024}k": L for L in W.LONG_CONTEXT}     # long-context decode sweep (--sweep)
+PROFILE = ("p2", "p4")              # smaller c2 / c4 runs for multi-pass ncu captures (not bench lines)
 SCORE_SWEEP = {f"x{L // 1024}k": L for L in W.LONG_CONTEXT}   # index-scoring sweep (--score-sweep)
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 << 20
@@ -79,7 +80,12 @@ def _wl_cache(name):
             _WL[name] = W.make_dense(f"sweep_scoring_{L // 1024}k", 0, 4, 64, 512, [L] * 4, perm_seed_key=L + 1)
             _WL[name].topk = 2048
         else:
-            _WL[name] = W.long_context(SWEEP[name]) if name in SWEEP else W.config(WORKLOADS[name])
+            if name in SWEEP:
+                _WL[name] = W.long_context(SWEEP[name])
+            elif name in PROFILE:
+                _WL[name] = W.profile_case(name)
+            else:
+                _WL[name] = W.config(WORKLOADS[name])
         if name == "c3c":
             _WL[name].n_cand = CAND_C3C
         if name in FUSED:
@@ -93,6 +99,10 @@ def workload_desc(name):
         return f"long-context decode sweep: batch {wl.B}, 64 heads, d=512, {SWEEP[name]} global tokens each + window"
     if name == "c3c":
         return W.CONFIGS[3] + f", scoring only a fixed {CAND_C3C}-position candidate set per sequence"
+    if name == "p2":
+        return "profiling case: c2's shape at batch 16 (two 8-sequence prefix groups), 1-token append"
+    if name == "p4":
+        return "profiling case: c4's shape at batch 2, prefix H U[32K,64K]"
     if name in FUSED:
         return (W.CONFIGS[WORKLOADS[name]] + f"; fused decode: query RoPE on the last {W.ROPE_DIM} channels, "
                 "inverse RoPE on O, E4M3 output")
@@ -787,7 +797,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(SWEEP), default="c2")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(SWEEP) + list(PROFILE), default="c2",
+                    help="c1-c4 (and c3c, c1f, c3f): the bench workloads; s32k..s512k: one sweep length; "
+                         "p2, p4: smaller c2 / c4 runs used as ncu capture cases")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time eager calls instead of the step captured as one CUDA graph (the default)")
     ap.add_argument("--score-sweep", action="store_true",

@@ -197,10 +197,11 @@ pkv_status pkv_score_topk_cand(pkv_ctx* ctx, const uint8_t* q_idx, float tq, con
  *   k_hat/v_hat the exact dequantized values.  Writes out float32 [B][H][d]
  *   and out_lse float32 [B][H] (may be NULL).
  * The contraction with the NVFP4 keys runs on block-scaled FP4 tensor cores:
- * q enters it as four FP4 terms per head, sigma_h * sum_t c_t 8^-t with c_t
- * E2M1 codes and sigma_h = max_i |q_h,i| / 4 (error at most sigma_h * 8^-3 / 2
+ * q enters it as five FP4 terms per head, sigma_h * sum_{t<5} c_t 8^-t with c_t
+ * E2M1 codes and sigma_h = max_i |q_h,i| / 4 (error at most sigma_h * 8^-4 / 2
  * per channel); the contraction with the FP8 window keys takes q as two E4M3
- * terms scaled by a power of two per head (exact for a bf16 q).
+ * terms scaled by a power of two per head (exact for a bf16 q).  Each query
+ * row is split into its terms once per call, into the workspace.
  * PKV_ERR_UNSUPPORTED when win->tw_v / cache->ts_v lies outside [2^-7, 2^7]
  * (the window's V scale is folded into the f16 softmax weights). */
 pkv_status pkv_decode_attn(pkv_ctx* ctx, const void* q_bf16, const pkv_kv_cache* cache,
@@ -230,9 +231,11 @@ typedef struct {
  *   out_fp8 uint8 [B][H][d] = E4M3(fp32(O' / out_scale)) (nearest, ties to
  *   even, saturating at 448, sign kept);
  *   out float32 [B][H][d] = O' and out_lse float32 [B][H] when not NULL.
- * Channels outside the rotated part pass through.  q' (rotated in FP32) enters
- * the contractions as the terms of pkv_decode_attn (four FP4 terms; two E4M3
- * terms for the window, about bf16 precision for a rotated q').  A position
+ * Channels outside the rotated part pass through.  q' is a bf16 tensor like
+ * q: each rotated value is computed in FP32 (every product, the difference and
+ * the sum rounded separately, no fused multiply-add) and rounded to bf16
+ * (nearest, ties to even); q' then enters the contractions as the terms of
+ * pkv_decode_attn (five FP4 terms; two E4M3 terms for the window, exact).  A position
  * outside [0, max_pos) sets the error
  * word (PKV_ERR_BAD_PAGE: an index out of range) and that row is not rotated.
  * Workspace as pkv_decode_attn.  PKV_ERR_UNSUPPORTED unless the tensor-core

@@ -268,6 +268,18 @@ def config(i: int, seed: int = 0) -> Workload:
     raise ValueError(i)
 
 
+# Profiling cases: smaller runs of the c2 and c4 kernels for multi-pass ncu
+# captures (a few hundred MB on the device, launches of milliseconds at most).
+def profile_case(name: str, seed: int = 0) -> Workload:
+    if name == "p2":   # c2's shape at 16 sequences (two prefix groups of 8)
+        lens = uniform_lengths(seed, 12, 16, 16384, 32768)
+        return make_shared_prefix("p2_ragged_paged_decode_small", seed, 16, 64, 512, lens, 8, 4096)
+    if name == "p4":   # c4's shape at 2 sequences
+        hl = uniform_lengths(seed, 14, 2, 32768, 65536)
+        return make_replay("p4_bounded_replay_small", seed, 2, 64, 512, hl)
+    raise ValueError(name)
+
+
 # Long-context decode sweep: the dense 64-head d=512 decode shape at one length
 # L, with the batch sized so that the NVFP4 K/V read per step is at least 1 GiB.
 LONG_CONTEXT = (32768, 65536, 131072, 262144, 524288)
