@@ -244,13 +244,6 @@ __device__ __forceinline__ float warp_sum16(const float* v, int lane) {
   return d + __shfl_xor_sync(0xffffffffu, d, 1);
 }
 
-// TMEM store of the 4*KS scale columns of a K tile (32 lanes of one quarter)
-template <int KS>
-__device__ __forceinline__ void st_sfa(uint32_t taddr, const uint32_t* r) {
-  if constexpr (KS == 8) tc::tmem_st32(taddr, r);
-  else if constexpr (KS == 4) tc::tmem_st16(taddr, r);
-  else tc::tmem_st8(taddr, r);
-}
 
 // E4M3 code of 8 * 8^-t: the B-side block scale of query term t
 __host__ __device__ constexpr uint32_t term_scale_code(int t) {
@@ -786,7 +779,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     // ======================================================== K block scales (thread = tile row)
     // Thread m holds row m of the tile's S^T (page m/64, token m%64): it loads the
     // 4 scale bytes of each 64-channel K step of its token and stores them where
-    // the block-scaled MMA reads row m's scales (lane m, column base + 4k + m/32).
+    // the block-scaled MMA reads row m's scales (lane m, column base + 4k + m/32;
+    // the other three columns of a K step are not read for these rows).
     // One buffer: the scales of tile n+1 are loaded while tile n is contracted and
     // stored as soon as its MMAs are complete.
     else if (warp < W_SF + 4) {
@@ -828,12 +822,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           const bool w_ok = tc::mbar_wait(&sh.sfa_empty, (gt & 1) ^ 1, abort_p, lim);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
           tc::tc_fence_after();
-          uint32_t r[4 * C::KS];
+          // only the column this lane quarter's rows are read from, per K step
 #pragma unroll
-          for (int k = 0; k < C::KS; ++k)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) r[4 * k + q] = (q == (warp - W_SF)) ? wrd[k] : 0u;
-          st_sfa<C::KS>(tbase + lb + COL_SFA, r);
+          for (int k = 0; k < C::KS; ++k) tc::tmem_st1(tbase + lb + COL_SFA + 4 * k + (warp - W_SF), wrd[k]);
           tc::tc_wait_st();
           tc::tc_fence_before();
           __syncwarp();
