@@ -945,6 +945,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const uint32_t lb = lane_base(warp);
       const float ratio = a.tw_v / a.cache.ts_v;
       const uint32_t m_s = tc::smem_u32(sh.m);
+      // the partial results stay in L2 for the merge that follows (the K/V stream
+      // would evict them otherwise)
+      const uint64_t pol = tc::l2_evict_last();
       int ntile = 0;
       bool ok = true;
       long long x = x0;
@@ -1111,7 +1114,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         if (st < NH) {
           const float lh = sh.red[0][st] + sh.red[1][st] + sh.red[2][st] + sh.red[3][st];
           sh.alpha[st] = lh > 0.f ? a.cache.ts_v / lh : 0.f;
-          if (st < a.H) part_lse[prow_i * a.H + st] = lh > 0.f ? (sh.m[st] + log2f(lh)) * LN2 : -INFINITY;
+          if (st < a.H) tc::st_f32_l2(part_lse + prow_i * a.H + st, lh > 0.f ? (sh.m[st] + log2f(lh)) * LN2 : -INFINITY, pol);
         }
         tc::named_bar(1, 256);
         float* po = part_o + prow_i * a.H * D;
@@ -1132,7 +1135,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const int h = hb + 4 * i4 + i;
-                if (h < a.H) po[(size_t)h * D + d] = __uint_as_float(o[4 * i4 + i]) * fv[i];
+                if (h < a.H) tc::st_f32_l2(po + (size_t)h * D + d, __uint_as_float(o[4 * i4 + i]) * fv[i], pol);
               }
             }
           }
