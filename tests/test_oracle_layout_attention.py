@@ -323,3 +323,36 @@ def test_v_layout_chunks_are_contiguous_runs():
     assert int(w[(2 * 8 + 1) * 128 + 44]) == 0x87654321
     assert int(w[(3 * 8 + 0) * 128 + 127]) == 0xFFFFFFFF
     assert np.count_nonzero(w) == 2
+
+
+def test_append_tokens_and_dequant_tokens():
+    """append_tokens writes the new token's own NVFP4 codes at slot pos % 64 of page
+    page_table[b][pos // 64] and nothing else; dequant_tokens returns the same rows as
+    the whole-sequence dequantization at the asked positions."""
+    wl = W.make_shared_prefix("app", 3, 4, 8, 128, [200, 260, 130, 199], 2, 128, append=True)
+    ts, _ = C.tensor_scales(wl)
+    Kp, Vp = C.fill_pages(wl, ts, ts)
+    before = [(C.dequant_seq(wl, Kp, ts, b, int(wl.fill_end[b])), C.dequant_seq(wl, Vp, ts, b, int(wl.fill_end[b])))
+              for b in range(wl.B)]
+    kd0, vd0 = Kp.data.copy(), Vp.data.copy()
+    knew, vnew = wl.new_rows(W.T_KNEW), wl.new_rows(W.T_VNEW)
+    pos = (wl.seq_len - 1).astype(np.int32)
+    C.append_tokens(wl, Kp, Vp, knew, vnew, np.arange(wl.B), pos, ts, ts)
+    touched = set()
+    for b in range(wl.B):
+        L = int(wl.seq_len[b])
+        K = C.dequant_seq(wl, Kp, ts, b, L)
+        V = C.dequant_seq(wl, Vp, ts, b, L)
+        assert (K[:L - 1] == before[b][0][:L - 1]).all() and (V[:L - 1] == before[b][1][:L - 1]).all()
+        c, s = F.nvfp4_quantize(knew[b:b + 1], ts)
+        assert (K[L - 1] == F.nvfp4_dequantize(c, s, ts)[0]).all()
+        c, s = F.nvfp4_quantize(vnew[b:b + 1], ts)
+        assert (V[L - 1] == F.nvfp4_dequantize(c, s, ts)[0]).all()
+        touched.add(int(wl.page_table[b, (L - 1) // W.PAGE]))
+        idx = np.random.default_rng(b).choice(L, size=min(L, 37), replace=False)
+        assert (C.dequant_tokens(wl, Kp, ts, b, idx) == K[idx]).all()
+        assert (C.dequant_tokens(wl, Vp, ts, b, idx) == V[idx]).all()
+    # pages no append landed on keep their bytes
+    for p in range(Kp.data.shape[0]):
+        if p not in touched:
+            assert (Kp.data[p] == kd0[p]).all() and (Vp.data[p] == vd0[p]).all()
