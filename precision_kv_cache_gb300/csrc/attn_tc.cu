@@ -19,21 +19,23 @@
 //     tensor-core contraction: A = the two K pages of a tile as stored (E2M1
 //     codes, K-major with the 128/64-byte swizzle; copied from shared memory
 //     into TMEM once per tile with tcgen05.cp), their E4M3 block scales in
-//     TMEM (written by warps 0-3, thread = tile row), B = the query written as a
+//     TMEM (written by warps 12-15, thread = tile row), B = the query written as a
 //     sum of NQT FP4 terms, q ~ sigma_h * sum_t c_t 8^-t (c_t E2M1 codes, one
 //     factor sigma_h per head applied to the logits; the term weights 8^-t are
 //     the constant B block scales).  No K dequantization.
 //   * the window tile's S^T runs on the FP8 contraction: A = the window K codes
 //     (E4M3, copied by TMA with the 128-byte swizzle), B = the query as two E4M3
 //     terms with a power-of-two factor per head (exact for a bf16 query).
-//   * warp 22 streams V pages into a shared-memory ring; warps 4-11 dequantize
-//     V^T to f16 into TMEM (thread = channel, 128 channels x 64 tokens at a
-//     time: the A operand of O^T = V^T P, M = 128 channels, N = 64 heads); warp
-//     23 issues the PV MMAs (P f16 in shared memory, B operand).
+//   * warp 22 streams V pages into a shared-memory ring; warps 0-11, three
+//     groups of four, dequantize V^T to f16 into TMEM (thread = channel, 128
+//     channels x 64 tokens at a time: the A operand of O^T = V^T P, M = 128
+//     channels, N = 64 heads); warp 23 issues the PV MMAs (P f16 in shared
+//     memory, B operand).
 //   * warps 12-19 run the online softmax on S (FP32, exp2, lazy max update with
-//     threshold 2^8), write P (f16), normalize O and write the partial result;
-//     at a row's start (and before its window tile) they also write the
-//     query's FP4 (or E4M3) terms into shared memory.
+//     threshold 2^8), write P (f16), normalize O and write the partial result.
+//     The query terms of each row are split ahead by qsplit_kernel; warp 21
+//     copies them into shared memory at the row's first tile (and its window
+//     tile) and issues the QK MMAs.
 //   * fused decode ("MegaAttention avec KV compressé NVFP4": query RoPE,
 //     attention, inverse RoPE on the output, FP8 output in one pass): the query
 //     is turned before it is split into terms, and the merge turns the final O
@@ -57,14 +59,14 @@ constexpr int NH = 64;                 // MMA N: query heads (zero-padded)
 constexpr int NQT = 5;                 // FP4 terms of the query
 constexpr int NTHREADS = 768;          // 24 warps
 // warp roles
-constexpr int W_SF = 0;                // 4 warps: K block scales -> TMEM
-constexpr int W_VDEQ = 4;              // 8 warps: V dequantizers
-constexpr int W_SMAX = 12;             // 8 warps: softmax + epilogue + query terms
+constexpr int W_VDEQ = 0;              // 12 warps: V dequantizers, NVG groups of four
+constexpr int W_SMAX = 12;             // 8 warps: softmax + epilogue; warps 12-15 also the K block scales
 constexpr int W_KPROD = 20;            // K tile producer
 constexpr int W_QK = 21;               // QK MMA issuer, TMEM owner
 constexpr int W_VPROD = 22;            // V page producer
 constexpr int W_PV = 23;               // PV MMA issuer
 constexpr uint32_t NGRP = 4;           // arrivals per V ring slot release / V chunk: one per warp of a group
+constexpr int NVG = 3;                 // V dequant groups (chunk i of the CTA to group i % NVG)
 constexpr float TAU = 8.f;             // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -81,7 +83,7 @@ static_assert(COL_SFA + 32 <= COL_SFB && COL_SFB + 32 <= COL_KA && COL_KA + 64 <
               "TMEM map");
 
 constexpr int NKS = 2;                 // K tile slots (two pages each, or window chunks)
-constexpr int NVR = 10;                // V ring: slots of one 128-channel chunk of one page
+constexpr int NVR = 9;                 // V ring: slots of one 128-channel chunk of one page
 constexpr int VGRP = 4;                // V ring slots filled by one warp instruction (one lane each)
 constexpr int VCODES = 8 * 128 * 4;    // V codes of a 128-channel chunk of a page (8 octets x 128 words)
 constexpr int VSCALES = 8 * PKV_PAGE;  // its block scales (8 blocks x 64 tokens)
@@ -122,8 +124,9 @@ struct Cfg {
 
 struct Shared {
   uint64_t kr_full[NKS], kr_empty[NKS], vr_full[NVR], vr_empty[NVR];
-  uint64_t sfa_full, sfa_empty;
-  uint64_t vfull[NVS], vempty[NVS];
+  uint64_t sfa_full;
+  uint64_t vfull[NVS];     // slot s holds chunk i (i % NVS == s): its four V warps stored it
+  uint64_t vempty[NVG];    // barrier i % NVG: the P.V of chunk i is complete
   uint64_t s_full, s_empty, p_full[2], p_empty[2], q_full, q_empty, o_empty, drain, drain2;
   uint32_t tmem_base;
   int abort_flag;
@@ -132,10 +135,11 @@ struct Shared {
   alignas(16) float zsg[NH];   // logit factor per head of the global tiles (log2 units)
   alignas(16) float zsw[NH];   // logit factor per head of the window tile (log2 units)
   float red[4][NH];            // cross-warp reductions
-  alignas(16) uint32_t vsc[8][64];   // per V warp: f16x2 block-scale pairs of its current chunk (2 blocks x 32)
+  alignas(16) uint32_t vsc[4 * NVG][64];   // per V warp: f16x2 block-scale pairs of its current chunk (2 blocks x 32)
+  alignas(16) uint32_t sfs[TILE][8];       // K block-scale words of the next tile, row m = token m (staged by cp.async)
 };
 static_assert(offsetof(Shared, m) % 16 == 0 && offsetof(Shared, alpha) % 16 == 0 && offsetof(Shared, zsg) % 16 == 0 &&
-                  offsetof(Shared, zsw) % 16 == 0 && offsetof(Shared, vsc) % 16 == 0,
+                  offsetof(Shared, zsw) % 16 == 0 && offsetof(Shared, vsc) % 16 == 0 && offsetof(Shared, sfs) % 16 == 0,
               "16-byte shared-memory vector accesses");
 
 // ---------------------------------------------------------------- schedule
@@ -244,6 +248,22 @@ __device__ __forceinline__ float warp_sum16(const float* v, int lane) {
   return d + __shfl_xor_sync(0xffffffffu, d, 1);
 }
 
+// The same reduce-scatter with max instead of sum.
+__device__ __forceinline__ float warp_max16(const float* v, int lane) {
+  float a[8], b[4], c[2];
+  const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4, u1 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    a[i] = fmaxf(u4 ? v[i + 8] : v[i], __shfl_xor_sync(0xffffffffu, u4 ? v[i] : v[i + 8], 16));
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    b[i] = fmaxf(u3 ? a[i + 4] : a[i], __shfl_xor_sync(0xffffffffu, u3 ? a[i] : a[i + 4], 8));
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    c[i] = fmaxf(u2 ? b[i + 2] : b[i], __shfl_xor_sync(0xffffffffu, u2 ? b[i] : b[i + 2], 4));
+  const float d = fmaxf(u1 ? c[1] : c[0], __shfl_xor_sync(0xffffffffu, u1 ? c[0] : c[1], 2));
+  return fmaxf(d, __shfl_xor_sync(0xffffffffu, d, 1));
+}
 
 // E4M3 code of 8 * 8^-t: the B-side block scale of query term t
 __host__ __device__ constexpr uint32_t term_scale_code(int t) {
@@ -401,6 +421,78 @@ __global__ void __launch_bounds__(256) qsplit_kernel(AttnArgs a, uint8_t* __rest
   }
 }
 
+// ---------------------------------------------------------------- K block scales
+// The block-scaled MMA of a global tile reads row m's E4M3 scales of K step k
+// from TMEM lane m, column COL_SFA + 4k + m/32.  Thread m of warps 12-15 stages
+// the scale words of its token (row m) of the CTA's next global tile in shared
+// memory (cp.async, issued a tile ahead) and stores them into TMEM once the MMAs
+// of the global tile before it are complete - which the softmax learns from that
+// tile's S.  The cursor walks the CTA's global tiles in order (a row's window
+// tile has no block scales).
+struct SfCursor {
+  int g, j, jend;        // query row, tile, end of the row's global tiles in range
+  int b, n_glob;         // the row's sequence and global length
+  bool live;
+};
+
+__device__ __forceinline__ void sf_settle(const AttnArgs& a, const int* tile_start, long long x1, SfCursor& c) {
+  while (c.live && c.j >= c.jend) {
+    ++c.g;
+    if (c.g >= a.n_groups || tile_start[c.g] >= x1) {
+      c.live = false;
+      break;
+    }
+    const int nt = tile_start[c.g + 1] - tile_start[c.g];
+    c.j = 0;
+    c.jend = (int)min((long long)(nt - 1), x1 - tile_start[c.g]);
+    int nw;
+    const uint8_t *wk, *wv;
+    unit_extent(a, c.g, &c.b, &c.n_glob, &nw, &wk, &wv);
+  }
+}
+
+__device__ __forceinline__ SfCursor sf_first(const AttnArgs& a, const int* tile_start, long long x0, long long x1, int g0) {
+  SfCursor c;
+  const int nt = tile_start[g0 + 1] - tile_start[g0];
+  c.g = g0;
+  c.j = (int)(x0 - tile_start[g0]);
+  c.jend = (int)min((long long)(nt - 1), x1 - tile_start[g0]);
+  c.live = x0 < x1;
+  int nw;
+  const uint8_t *wk, *wv;
+  unit_extent(a, g0, &c.b, &c.n_glob, &nw, &wk, &wv);
+  sf_settle(a, tile_start, x1, c);
+  return c;
+}
+
+// row m's scale words of the cursor's tile -> shared memory (zero past the end)
+template <int D>
+__device__ __forceinline__ void sf_stage(const AttnArgs& a, const SfCursor& c, int m, uint32_t dst) {
+  using C = Cfg<D>;
+  const int pos = TILE * c.j + m;
+  if (pos < c.n_glob) {
+    int pid = a.page_table[(size_t)c.b * a.max_pages + (pos >> 6)];
+    if (pid < 0 || pid >= a.cache.num_pages) pid = 0;      // the K producer reports it
+    const uint8_t* sp = a.cache.k_scale + (size_t)pid * C::PAGE_SCALE + (pos & 63) * 8;
+#pragma unroll
+    for (int q = 0; q < C::KS / 2; ++q) tc::cp_async8(dst + 8 * q, sp + q * (PKV_PAGE * 8));
+  } else {
+#pragma unroll
+    for (int k = 0; k < C::KS; ++k) tc::sts32(dst + 4 * k, 0u);
+  }
+  tc::cp_async_commit();
+}
+
+// the staged words -> TMEM: only the column the lane quarter's rows are read from
+template <int D>
+__device__ __forceinline__ void sf_store(uint32_t taddr, uint32_t src) {
+  using C = Cfg<D>;
+  tc::cp_async_wait_all();
+#pragma unroll
+  for (int k = 0; k < C::KS; ++k) tc::tmem_st1(taddr + 4 * k, tc::lds32(src + 4 * k));
+  tc::tc_wait_st();
+}
+
 // ---------------------------------------------------------------- the kernel
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap wmap,
@@ -429,11 +521,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       tc::mbar_init(&sh.vr_empty[i], NGRP);
     }
     tc::mbar_init(&sh.sfa_full, 4);
-    tc::mbar_init(&sh.sfa_empty, 1);
-    for (int i = 0; i < NVS; ++i) {
-      tc::mbar_init(&sh.vfull[i], NGRP);
-      tc::mbar_init(&sh.vempty[i], 1);
-    }
+    for (int i = 0; i < NVS; ++i) tc::mbar_init(&sh.vfull[i], NGRP);
+    for (int i = 0; i < NVG; ++i) tc::mbar_init(&sh.vempty[i], 1);
     tc::mbar_init(&sh.s_full, 1);
     tc::mbar_init(&sh.s_empty, 8);
     tc::mbar_init(&sh.p_full[0], 8);
@@ -675,7 +764,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
                                   tbase + COL_SFB + 4 * t, (t | k) != 0);
                 }
               }
-              tc::mma_commit(&sh.sfa_empty);
               tc::mma_commit(&sh.s_full);
               // the row's last global tile in range: its FP4 query terms are free
               if (j == min(j1, nt - 1) - 1) tc::mma_commit(&sh.q_empty);
@@ -749,7 +837,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           // chunk k of the tile: 128 channels (c = k / halves) x 64 tokens (page half h = k % halves)
           const int halves = (j == nt - 1 || TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
           for (int k = 0; k < C::NVCH * halves && ok; ++k) {
-            const int slot = ci % NVS, c = k / halves, h = k % halves;
+            const int slot = ci % NVS, c = k >> (halves - 1), h = k & (halves - 1);   // halves is 1 or 2
             ok = tc::mbar_wait(&sh.vfull[slot], (ci / NVS) & 1, abort_p, lim);
             tc::compiler_fence();
             if (!ok) break;
@@ -760,7 +848,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 tc::mma_ts(dO, aV + 8 * kk, bp + (uint64_t)(kk * (2048 >> 4)), idV, !(j == j0 && h == 0 && kk == 0));
-              tc::mma_commit(&sh.vempty[slot]);
+              tc::mma_commit(&sh.vempty[ci % NVG]);
               if (k == C::NVCH * halves - 1) tc::mma_commit(&sh.p_empty[np & 1]);
             }
             __syncwarp();
@@ -776,77 +864,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       __syncwarp();
       if (!tc::mbar_drain(&sh.drain2, 0, lim) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     }
-    // ======================================================== K block scales (thread = tile row)
-    // Thread m holds row m of the tile's S^T (page m/64, token m%64): it loads the
-    // 4 scale bytes of each 64-channel K step of its token and stores them where
-    // the block-scaled MMA reads row m's scales (lane m, column base + 4k + m/32;
-    // the other three columns of a K step are not read for these rows).
-    // One buffer: the scales of tile n+1 are loaded while tile n is contracted and
-    // stored as soon as its MMAs are complete.
-    else if (warp < W_SF + 4) {
-      const int m = 32 * (warp - W_SF) + lane;
-      const uint32_t lb = lane_base(warp);
-      {
-        // constant B-side block scales of the query terms, every lane quarter
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = i < 4 * NQT ? term_scale_code(i / 4) * 0x01010101u : 0u;
-        tc::tmem_st32(tbase + lb + COL_SFB, r);
-        tc::tc_wait_st();
-      }
-      int gt = 0;
-      bool ok = true;
-      long long x = x0;
-      int g = g0;
-      while (x < x1 && ok) {
-        const Unit u = unit_of(a, g);
-        const int nt = tile_start[g + 1] - tile_start[g];
-        const int j0 = (int)(x - tile_start[g]);
-        const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
-        for (int j = j0; j < j1 && j < nt - 1; ++j) {
-          const int pos = TILE * j + m;
-          uint32_t wrd[C::KS];
-#pragma unroll
-          for (int k = 0; k < C::KS; ++k) wrd[k] = 0u;
-          if (pos < u.n_glob) {
-            int pid = a.page_table[(size_t)u.b * a.max_pages + (pos >> 6)];
-            if (pid < 0 || pid >= a.cache.num_pages) pid = 0;      // the producer reports it
-            const uint8_t* sp = a.cache.k_scale + (size_t)pid * psb + (pos & 63) * 8;
-#pragma unroll
-            for (int q = 0; q < C::KS / 2; ++q) {
-              const uint2 v = __ldg(reinterpret_cast<const uint2*>(sp + q * (PKV_PAGE * 8)));
-              wrd[2 * q] = v.x;
-              wrd[2 * q + 1] = v.y;
-            }
-          }
-          const bool w_ok = tc::mbar_wait(&sh.sfa_empty, (gt & 1) ^ 1, abort_p, lim);
-          if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
-          tc::tc_fence_after();
-          // only the column this lane quarter's rows are read from, per K step
-#pragma unroll
-          for (int k = 0; k < C::KS; ++k) tc::tmem_st1(tbase + lb + COL_SFA + 4 * k + (warp - W_SF), wrd[k]);
-          tc::tc_wait_st();
-          tc::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sh.sfa_full);
-          ++gt;
-        }
-        x = tile_start[g] + j1;
-        ++g;
-      }
-    }
     // ======================================================== V dequantizer (thread = channel)
-    // Two groups of four warps (one warp per TMEM lane quarter) take the chunks of
+    // NVG groups of four warps (one warp per TMEM lane quarter) take the chunks of
     // the tiles in turn: chunk k of a tile is 128 channels (k / halves) x the 64
     // tokens of page half (k % halves), one V ring slot; group vg takes the chunk
-    // numbers i (counted over the CTA's tiles) of parity vg, into the 32-column
-    // TMEM slot i % NVS.  Each warp converts the E4M3 block scales it needs once per chunk
+    // numbers i (counted over the CTA's tiles) with i % NVG == vg, into the
+    // 32-column TMEM slot i % NVS once the P.V of chunk i - NVS is complete
+    // (barrier (i - NVS) % NVG: with one barrier per group, a group waits at most
+    // one phase ahead - its previous chunk's wait saw the phase before).  Each warp converts the E4M3 block scales it needs once per chunk
     // (two per lane) and shares them through shared memory; the ring slot is
     // released as soon as its codes are read.
     else if (warp < W_SMAX) {
-      const int vw = warp - W_VDEQ;                  // 0..7
+      const int vw = warp - W_VDEQ;                  // 0 .. 4 NVG - 1
       const int dl = 32 * (vw & 3) + lane;           // channel lane 0..127 within a chunk
-      const int vg = vw >> 2;                        // group: chunks of parity vg
+      const int vg = vw >> 2;                        // group: chunks i with i % NVG == vg
       const uint32_t lb = lane_base(warp);
       const uint32_t vsc_s = tc::smem_u32(sh.vsc[vw]);
       const uint32_t sv0 = tc::smem_u32(sV);
@@ -866,8 +897,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
 #pragma unroll 1
           for (int k = 0; k < C::NVCH * halves && ok; ++k, ++ci) {
-            if ((ci & 1) != vg) continue;
-            const int c = k / halves, h = k % halves;
+            if (ci % NVG != vg) continue;
+            const int c = k >> (halves - 1), h = k & (halves - 1);   // halves is 1 or 2
             const int d = 128 * c + dl;
             uint32_t r[32];
             if (!win) {
@@ -920,8 +951,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             }
             tc::reg_fence32(r);             // conversion done before the (blocking) slot wait
             // the PV of the chunk NVS before this one has read the TMEM slot
-            const int vs = ci % NVS;
-            const bool s_ok = tc::mbar_wait(&sh.vempty[vs], ((ci / NVS) & 1) ^ 1, abort_p, lim);
+            const int vs = ci % NVS, pc = ci - NVS;
+            const bool s_ok = pc < 0 || tc::mbar_wait(&sh.vempty[pc % NVG], (pc / NVG) & 1, abort_p, lim);
             if (!__all_sync(0xffffffffu, s_ok)) { fail(sh, a.err); ok = false; break; }
             tc::tc_fence_after();
             tc::tmem_st32(tbase + lb + COL_V + 32 * vs, r);
@@ -948,6 +979,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       // the partial results stay in L2 for the merge that follows (the K/V stream
       // would evict them otherwise)
       const uint64_t pol = tc::l2_evict_last();
+      // warps 12-15: the query terms' constant B-side block scales, then the K
+      // block scales of the CTA's first global tile (staged and stored at once)
+      // and, staged a tile ahead, those of each next one
+      const bool sfw = hh == 0;
+      const uint32_t sf_t = tbase + lb + COL_SFA + q4;     // this quarter's column of K step 0
+      const uint32_t sf_s = tc::smem_u32(sh.sfs[t]);
+      SfCursor sfc{};
+      if (sfw) {
+        sfc = sf_first(a, tile_start, x0, x1, g0);
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = i < 4 * NQT ? term_scale_code(i / 4) * 0x01010101u : 0u;
+        tc::tmem_st32(tbase + lb + COL_SFB, r);
+        tc::tc_wait_st();
+        if (sfc.live) {
+          sf_stage<D>(a, sfc, t, sf_s);
+          sf_store<D>(sf_t, sf_s);
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sh.sfa_full);
+          ++sfc.j;
+          sf_settle(a, tile_start, x1, sfc);
+          if (sfc.live) sf_stage<D>(a, sfc, t, sf_s);
+        }
+      }
       int ntile = 0;
       bool ok = true;
       long long x = x0;
@@ -992,6 +1048,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sh.s_empty);
+          // a global tile's S is complete, so are its MMAs: the next global
+          // tile's K block scales may replace its own
+          if (sfw && !win && sfc.live) {
+            sf_store<D>(sf_t, sf_s);
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sh.sfa_full);
+            ++sfc.j;
+            sf_settle(a, tile_start, x1, sfc);
+            if (sfc.live) sf_stage<D>(a, sfc, t, sf_s);
+          }
           // two passes of 16 heads (keeps 16 logits live instead of 32); the first
           // pass's f16 P values wait in registers until its P buffer is free
           const int pb = ntile & 1;
@@ -1020,13 +1087,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               }
             }
             if (tc::named_bar_or(2, 256, need)) {
-              // tile max per head: over the 32 tokens of the warp, then the 4 lane quarters
+              // tile max per head: over the 32 tokens of the warp (reduce-scatter:
+              // lanes 2i, 2i+1 end with head h0 + i), then the 4 lane quarters
+              {
+                float mv[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                float v = valid ? sv[i] : -INFINITY;
-#pragma unroll
-                for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                if (lane == 0) sh.red[q4][h0 + i] = v;
+                for (int i = 0; i < 16; ++i) mv[i] = valid ? sv[i] : -INFINITY;
+                const float v = warp_max16(mv, lane);
+                if ((lane & 1) == 0) sh.red[q4][h0 + hs] = v;
               }
               tc::named_bar(1, 256);
               if (q4 == 0 && lane < 16) {
@@ -1146,6 +1214,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         x = tile_start[g] + j1;
         ++g;
       }
+      if (sfw) tc::cp_async_wait_all();      // a staging copy of a role that gave up lands before exit
     }
   }
   tc::tc_fence_before();

@@ -127,6 +127,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 8-byte asynchronous copy global -> shared (both addresses 8-byte aligned),
+// completed by this thread's cp_async_wait_all
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // 2-D tiled tensor copy global -> shared through a tensor map (TMA), completion
 // as transaction bytes on `bar`.  x is the innermost coordinate (bytes for a
 // uint8 map; a multiple of 16), y the row.
