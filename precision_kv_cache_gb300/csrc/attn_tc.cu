@@ -882,7 +882,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       const uint32_t vsc_s = tc::smem_u32(sh.vsc[vw]);
       const uint32_t sv0 = tc::smem_u32(sV);
       int vbase = 0;            // ring slots of the tiles before this one
-      int ci = 0;               // chunks of both groups before this one
+      int ci0 = 0;              // chunks of all groups before this tile
       bool ok = true;
       long long x = x0;
       int g = g0;
@@ -895,9 +895,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           const bool win = (j == nt - 1);
           const int halves = (win || TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
           const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
+          const int nk = C::NVCH * halves;
+          // this group's chunks of the tile: numbers ci = ci0 + k with ci % NVG == vg
 #pragma unroll 1
-          for (int k = 0; k < C::NVCH * halves && ok; ++k, ++ci) {
-            if (ci % NVG != vg) continue;
+          for (int k = (vg + NVG - ci0 % NVG) % NVG; k < nk && ok; k += NVG) {
+            const int ci = ci0 + k;
             const int c = k >> (halves - 1), h = k & (halves - 1);   // halves is 1 or 2
             const int d = 128 * c + dl;
             uint32_t r[32];
@@ -961,7 +963,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
           }
-          if (!win) vbase += C::NVCH * halves;
+          ci0 += nk;
+          if (!win) vbase += nk;
         }
         x = tile_start[g] + j1;
         ++g;
