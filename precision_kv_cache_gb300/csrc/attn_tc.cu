@@ -1062,10 +1062,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             sf_settle(a, tile_start, x1, sfc);
             if (sfc.live) sf_stage<D>(a, sfc, t, sf_s);
           }
-          // two passes of 16 heads (keeps 16 logits live instead of 32); the first
-          // pass's f16 P values wait in registers until its P buffer is free
+          // two passes of 16 heads; the f16 P values of both wait in registers
+          // until the P buffer is free
           const int pb = ntile & 1;
           const uint32_t prow = tc::smem_u32(sP) + pb * C::P_BYTES + (t >> 3) * 1024 + (t & 7) * 128;
+          uint32_t pk2[2][8];
 #pragma unroll
           for (int hq = 0; hq < 2; ++hq) {
             const int h0 = 32 * hh + 16 * hq;            // first head of this pass
@@ -1133,7 +1134,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             }
             // ---- P = exp2(S * zs - m) (f16); l sums the FP32 values.  The
             // arguments are <= TAU, so the approximate exp2 stays in range.
-            uint32_t pk[8];
+            uint32_t* pk = pk2[hq];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               const uint4 ma = tc::lds128(m_s + 4 * (h0 + 8 * k));
@@ -1152,16 +1153,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               }
             }
             l[hq] += warp_sum16(sv, lane);
-            if (hq == 0) {
-              // P buffer ntile&1 is free once the P.V of tile ntile-2 is done
-              w_ok = tc::mbar_wait(&sh.p_empty[pb], ((ntile >> 1) & 1) ^ 1, abort_p, lim);
-              if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
-            }
-            // row t of P (MN-major, 128-byte swizzle): heads 8c .. 8c+7 = 16-byte chunk c
-            tc::sts128(prow + 16 * ((4 * hh + 2 * hq) ^ (t & 7)), make_uint4(pk[0], pk[1], pk[2], pk[3]));
-            tc::sts128(prow + 16 * ((4 * hh + 2 * hq + 1) ^ (t & 7)), make_uint4(pk[4], pk[5], pk[6], pk[7]));
           }
           if (!ok) break;
+          // P buffer ntile&1 is free once the P.V of tile ntile-2 is done; both
+          // passes' f16 P values wait in registers until then
+          w_ok = tc::mbar_wait(&sh.p_empty[pb], ((ntile >> 1) & 1) ^ 1, abort_p, lim);
+          if (tc::named_bar_or(3, 256, !w_ok)) { fail(sh, a.err); ok = false; break; }
+          // row t of P (MN-major, 128-byte swizzle): heads 8c .. 8c+7 = 16-byte chunk c
+#pragma unroll
+          for (int hq = 0; hq < 2; ++hq) {
+            tc::sts128(prow + 16 * ((4 * hh + 2 * hq) ^ (t & 7)), make_uint4(pk2[hq][0], pk2[hq][1], pk2[hq][2], pk2[hq][3]));
+            tc::sts128(prow + 16 * ((4 * hh + 2 * hq + 1) ^ (t & 7)), make_uint4(pk2[hq][4], pk2[hq][5], pk2[hq][6], pk2[hq][7]));
+          }
           tc::fence_proxy_async_smem();
           tc::tc_fence_before();
           __syncwarp();
