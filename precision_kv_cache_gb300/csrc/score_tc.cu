@@ -2,12 +2,13 @@
 // vLLM blog "Kernels"):  score_t = sum_h w_h * ReLU(q_h . k_t)  over the
 // 128-channel NVFP4 index keys, for every position of every sequence.
 //
-// One persistent CTA per SM, 512 threads, warp-specialized:
+// One persistent CTA per SM, 768 threads, warp-specialized:
 //   * warp 0 streams the 64-token key pages into a 24-page shared-memory ring
 //     (1-D bulk copies);
-//   * warps 4-11: two groups of four (one warp per TMEM lane quarter, thread =
-//     token) that take alternate 128-token tiles and dequantize them to f16
-//     into TMEM (exact: E2M1 x E4M3 has <= 6 significant bits);
+//   * warps 4-11 and 20-23: three groups of four (one warp per TMEM lane
+//     quarter, thread = token) that take every third 128-token tile and
+//     dequantize it to f16 into TMEM (exact: E2M1 x E4M3 has <= 6 significant
+//     bits);
 //   * warp 1 issues S^T = K Q^T on tcgen05 (M = 128 tokens, N = 64 index heads,
 //     K = 128; Q = the FP8 index queries, exact in f16, in shared memory), the
 //     whole warp running the schedule and one elected lane issuing;
@@ -25,8 +26,9 @@ namespace tcscore {
 constexpr int TILE = 128;
 constexpr int NH = 64;
 constexpr int D = 128;
-constexpr int NTHREADS = 640;                          // 20 warps
-constexpr int W_PROD = 0, W_MMA = 1, W_DEQ = 4, W_EPI = 12;
+constexpr int NTHREADS = 768;                          // 24 warps
+constexpr int W_PROD = 0, W_MMA = 1, W_DEQ = 4, W_EPI = 12, W_DEQ2 = 20;
+constexpr int NKG = 3;                                 // key dequant groups: warps 4-7, 8-11, 20-23
 constexpr int NR = 24;                                 // key ring: page slots
 constexpr int NS = 4;                                  // K / S^T tile slots in TMEM
 constexpr int PAGE_DATA = PKV_PAGE * D / 2;            // 4096
@@ -261,14 +263,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
       if (tc::elect_one()) tc::mma_commit(&sh.drain);
       __syncwarp();
       if (!tc::mbar_drain(&sh.drain, 0) && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
-    } else if (warp >= W_DEQ && warp < W_EPI) {
+    } else if ((warp >= W_DEQ && warp < W_EPI) || warp >= W_DEQ2) {
       // ======================================================== key dequantizer (thread = token)
-      // group kg takes the tiles n = kg, kg+2, ... of this CTA (n counted from x0)
+      // group kg takes the tiles n = kg, kg + NKG, ... of this CTA (n counted from x0)
       const int t = 32 * (warp & 3) + lane;
-      const int kg = (warp - W_DEQ) >> 2;
+      const int kg = warp >= W_DEQ2 ? 2 : (warp - W_DEQ) >> 2;
       const uint32_t lb = lane_base(warp);
       const uint32_t ring_s = tc::smem_u32(ring);
-      int pc = 0, n = 0;
+      int pc0 = 0, n0 = 0;      // ring pages and tiles of the CTA before this row's first tile in range
       bool ok = true;
       long long x = x0;
       int g = g0;
@@ -277,9 +279,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
         const int nt = tile_start[g + 1] - tile_start[g];
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
-        for (int j = j0; j < j1 && ok; ++j, ++n) {
+        // this group's tiles of the row (tile n = n0 + j - j0 with n % NKG == kg);
+        // every tile but a sequence's last has two pages
+        for (int j = j0 + (kg + NKG - n0 % NKG) % NKG; j < j1 && ok; j += NKG) {
+          const int n = n0 + (j - j0), pc = pc0 + 2 * (j - j0);
           const int npg = (TILE * j + PKV_PAGE < L) ? 2 : 1;
-          if ((n & 1) != kg) { pc += npg; continue; }
           const int s = n % NS;
           const uint32_t ph = (n / NS) & 1;
           bool w_ok = tc::mbar_wait(&sh.kempty[s], ph ^ 1, abort_p);
@@ -326,12 +330,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
             tc::mbar_arrive(&sh.kfull[s]);
             for (int q = 0; q < npg; ++q) tc::mbar_arrive(&sh.r_empty[(pc + q) % NR]);
           }
-          pc += npg;
         }
+        n0 += j1 - j0;
+        pc0 += 2 * (j1 - j0) - ((j1 == nt && j1 > j0 && TILE * (nt - 1) + PKV_PAGE >= L) ? 1 : 0);
         x = tile_start[g] + j1;
         ++g;
       }
-    } else if (warp >= W_EPI) {
+    } else if (warp >= W_EPI && warp < W_DEQ2) {
       // ======================================================== epilogue (thread = token)
       // group eg takes the tiles n = eg, eg+2, ... of this CTA
       const int t = 32 * (warp & 3) + lane;
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
       const uint32_t lb = lane_base(warp);
       const float sc = a.tq * a.ic.ts;
       const uint32_t w_s = tc::smem_u32(sh.w);
-      int n = 0;
+      int n0 = 0;               // tiles of the CTA before this row's first tile in range
       bool ok = true;
       long long x = x0;
       int g = g0;
@@ -358,32 +363,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
           }
           tc::named_bar(1, 256);                    // sh.w of this sequence visible to both groups
         }
-        for (int j = j0; j < j1; ++j, ++n) {
-          if ((n & 1) != eg) continue;
+        // this group's tiles of the row: tile n0 + j - j0 with n % 2 == eg
+        for (int j = j0 + ((eg - n0) & 1); j < j1; j += 2) {
+          const int n = n0 + (j - j0);
           const int s = n % NS;
           const uint32_t ph = (n / NS) & 1;
           const bool w_ok = tc::mbar_wait(&sh.s_full[s], ph, abort_p);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
           tc::tc_fence_after();
-          uint32_t r[64];
-          tc::tmem_ld32(tbase + lb + COL_S + 64 * s, r);
-          tc::tmem_ld32(tbase + lb + COL_S + 64 * s + 32, r + 32);
-          tc::tc_wait_ld();
-          tc::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sh.s_empty[s]);
           float acc = 0.f;
 #pragma unroll
-          for (int i4 = 0; i4 < 16; ++i4) {
-            const uint4 wv = tc::lds128(w_s + 16 * i4);
-            acc = fmaf(__uint_as_float(wv.x), fmaxf(__uint_as_float(r[4 * i4]), 0.f), acc);
-            acc = fmaf(__uint_as_float(wv.y), fmaxf(__uint_as_float(r[4 * i4 + 1]), 0.f), acc);
-            acc = fmaf(__uint_as_float(wv.z), fmaxf(__uint_as_float(r[4 * i4 + 2]), 0.f), acc);
-            acc = fmaf(__uint_as_float(wv.w), fmaxf(__uint_as_float(r[4 * i4 + 3]), 0.f), acc);
+          for (int hf = 0; hf < 2; ++hf) {           // heads 32 hf .. 32 hf + 31
+            uint32_t r[32];
+            tc::tmem_ld32(tbase + lb + COL_S + 64 * s + 32 * hf, r);
+            tc::tc_wait_ld();
+            if (hf == 1) {
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sh.s_empty[s]);
+            }
+#pragma unroll
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const uint4 wv = tc::lds128(w_s + 16 * (8 * hf + i4));
+              acc = fmaf(__uint_as_float(wv.x), fmaxf(__uint_as_float(r[4 * i4]), 0.f), acc);
+              acc = fmaf(__uint_as_float(wv.y), fmaxf(__uint_as_float(r[4 * i4 + 1]), 0.f), acc);
+              acc = fmaf(__uint_as_float(wv.z), fmaxf(__uint_as_float(r[4 * i4 + 2]), 0.f), acc);
+              acc = fmaf(__uint_as_float(wv.w), fmaxf(__uint_as_float(r[4 * i4 + 3]), 0.f), acc);
+            }
           }
           const int tok = TILE * j + t;
           if (tok < L) a.scores[(size_t)g * a.Lmax + tok] = acc * sc;
         }
+        n0 += j1 - j0;
         x = tile_start[g] + j1;
         ++g;
       }
