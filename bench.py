@@ -501,8 +501,8 @@ def run_gpu(args, rank, world, pool):
         tf = flops / (kern_ms * 1e-3) / 1e12
         roofline = {"kernel": "attention (replay)", "bound": "tensor", "achieved": round(tf, 1), "peak": tpeak,
                     "unit": "TFLOP/s", "frac": round(tf / tpeak, 4), "peak_kind": tkind,
-                    "flops_per_launch": flops, "launch_ms": round(kern_ms, 5), "traffic": None,
-                    "hbm_gbs": round(achieved, 2)}
+                    "flops_per_launch": flops, "launch_ms": round(kern_ms, 5),
+                    "traffic": committed_traffic("attention", name), "hbm_gbs": round(achieved, 2)}
     launches_per_step = (n1 - n0) / args.steps
 
     # ---- end to end through the public API with host buffers: every step copies its
