@@ -89,6 +89,9 @@ constexpr int VCODES = 8 * 128 * 4;    // V codes of a 128-channel chunk of a pa
 constexpr int VSCALES = 8 * PKV_PAGE;  // its block scales (8 blocks x 64 tokens)
 constexpr int VSLOT = VCODES + VSCALES;
 constexpr int WCHUNK = 128 * 128;      // window K chunk: 128 entries x 128 channels of E4M3
+constexpr int WVROWS = 32;             // window V chunk: 32 entries x 128 channels of E4M3, one V ring slot
+constexpr int WVQ = PKV_WINDOW / WVROWS;   // window V chunks per 128-channel chunk
+static_assert(WVROWS * 128 <= VCODES, "a window V chunk fits a ring slot");
 
 template <int D>
 struct Cfg {
@@ -496,6 +499,7 @@ __device__ __forceinline__ void sf_store(uint32_t taddr, uint32_t src) {
 // ---------------------------------------------------------------- the kernel
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap wmap,
+                                                              const __grid_constant__ CUtensorMap vmap,
                                                               const int* __restrict__ tile_start,
                                                               float* __restrict__ part_o,
                                                               float* __restrict__ part_lse) {
@@ -566,20 +570,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       bool ok = true;
       long long x = x0;
       int g = g0;
-      const uint8_t* last_win = nullptr;
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
         const int nt = tile_start[g + 1] - tile_start[g];
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         const int npr = (u.n_glob + PKV_PAGE - 1) / PKV_PAGE;       // pages of the row
-        if (lane == 0) {
-          // the window V (read from global memory by the V dequantizers): warm L2
-          if (j1 == nt && u.wv != last_win && ((uintptr_t)u.wv & 15u) == 0) {
-            tc::bulk_prefetch_l2(u.wv, (uint32_t)(PKV_WINDOW * D));
-            last_win = u.wv;
-          }
-        }
         int pbase = -1, pl = -1;            // lane i holds page id pbase + i of the row
         for (int j = j0; j < j1 && ok; ++j) {
           const bool win = (j == nt - 1);
@@ -688,6 +684,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               uint8_t* dst = sV + slot * VSLOT;
               tc::bulk_g2s(dst, a.cache.v_data + (size_t)pid * pdb + c * VCODES, VCODES, &sh.vr_full[slot]);
               tc::bulk_g2s(dst + VCODES, a.cache.v_scale + (size_t)pid * psb + c * VSCALES, VSCALES, &sh.vr_full[slot]);
+            }
+            vi += ni;
+          }
+        }
+        // the window tile: NVCH x WVQ chunks of WVROWS entries x 128 channels (E4M3),
+        // one ring slot each, by TMA in the same groups of VGRP
+        if (ok && j1 == nt) {
+          const int n = C::NVCH * WVQ;
+          for (int k = 0; k < n && ok; k += VGRP) {
+            const int ni = min(VGRP, n - k);
+            const int cq = k + lane, c = cq / WVQ, q = cq % WVQ;
+            const int slot = (vi + lane) % NVR, use = (vi + lane) / NVR;
+            bool w_ok = true;
+            if (lane < ni) w_ok = tc::mbar_wait(&sh.vr_empty[slot], (use & 1) ^ 1, abort_p, lim);
+            if (!__all_sync(0xffffffffu, w_ok)) {
+              if (lane == 0) fail(sh, a.err);
+              ok = false;
+              break;
+            }
+            if (lane < ni) {
+              tc::mbar_arrive_expect_tx(&sh.vr_full[slot], WVROWS * 128);
+              tc::tma_load_2d(sV + slot * VSLOT, &vmap, 128 * c, u.b * PKV_WINDOW + WVROWS * q, &sh.vr_full[slot]);
             }
             vi += ni;
           }
@@ -834,22 +852,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         for (int j = j0; j < j1 && ok; ++j) {
           ok = tc::mbar_wait(&sh.p_full[np & 1], (np >> 1) & 1, abort_p, lim);
           const uint64_t bpn = dp0 + (uint64_t)(((np & 1) * C::P_BYTES) >> 4);
-          // chunk k of the tile: 128 channels (c = k / halves) x 64 tokens (page half h = k % halves)
-          const int halves = (j == nt - 1 || TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
-          for (int k = 0; k < C::NVCH * halves && ok; ++k) {
-            const int slot = ci % NVS, c = k >> (halves - 1), h = k & (halves - 1);   // halves is 1 or 2
+          // global tile: chunk k = 128 channels (k / halves) x the 64 tokens of page
+          // half k % halves, 4 MMAs; window tile: 128 channels (k / WVQ) x WVROWS
+          // entries, WVROWS / 16 MMAs
+          const bool win = (j == nt - 1);
+          const int halves = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
+          const int nk = win ? C::NVCH * WVQ : C::NVCH * halves;
+          const int nmma = win ? WVROWS / 16 : 4;
+          for (int k = 0; k < nk && ok; ++k) {
+            const int slot = ci % NVS;
+            const int c = win ? k / WVQ : k >> (halves - 1);                     // halves is 1 or 2
+            const int t0 = win ? WVROWS * (k % WVQ) : 64 * (k & (halves - 1));   // the chunk's first token
             ok = tc::mbar_wait(&sh.vfull[slot], (ci / NVS) & 1, abort_p, lim);
             tc::compiler_fence();
             if (!ok) break;
             tc::tc_fence_after();
             const uint32_t dO = tbase + COL_O + 64 * c, aV = tbase + COL_V + 32 * slot;
-            const uint64_t bp = bpn + (uint64_t)((h * 8192) >> 4);
+            const uint64_t bp = bpn + (uint64_t)(((t0 / 8) * 1024) >> 4);       // P rows: 8 tokens per 1 KB
             if (tc::elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                tc::mma_ts(dO, aV + 8 * kk, bp + (uint64_t)(kk * (2048 >> 4)), idV, !(j == j0 && h == 0 && kk == 0));
+                if (kk < nmma)
+                  tc::mma_ts(dO, aV + 8 * kk, bp + (uint64_t)(kk * (2048 >> 4)), idV, !(j == j0 && t0 == 0 && kk == 0));
               tc::mma_commit(&sh.vempty[ci % NVG]);
-              if (k == C::NVCH * halves - 1) tc::mma_commit(&sh.p_empty[np & 1]);
+              if (k == nk - 1) tc::mma_commit(&sh.p_empty[np & 1]);
             }
             __syncwarp();
             ++ci;
@@ -893,18 +919,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         for (int j = j0; j < j1 && ok; ++j) {
           const bool win = (j == nt - 1);
-          const int halves = (win || TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
+          const int halves = (TILE * j + PKV_PAGE < u.n_glob) ? 2 : 1;
           const int nvalid = win ? u.n_win : min(TILE, u.n_glob - TILE * j);
-          const int nk = C::NVCH * halves;
+          // global tile: NVCH x halves chunks of 64 tokens; window tile: NVCH x WVQ
+          // chunks of WVROWS entries; one ring slot each
+          const int nk = win ? C::NVCH * WVQ : C::NVCH * halves;
           // this group's chunks of the tile: numbers ci = ci0 + k with ci % NVG == vg
 #pragma unroll 1
           for (int k = (vg + NVG - ci0 % NVG) % NVG; k < nk && ok; k += NVG) {
             const int ci = ci0 + k;
-            const int c = k >> (halves - 1), h = k & (halves - 1);   // halves is 1 or 2
-            const int d = 128 * c + dl;
+            const int ri = vbase + k, rs = ri % NVR;
+            const int vs = ci % NVS, pc = ci - NVS;
+            if (win) {
+              // WVROWS entries x this lane's channel of the ring slot (row-major
+              // [entry][128 channels] E4M3), pairs of entries -> f16x2
+              const bool w_ok = tc::mbar_wait(&sh.vr_full[rs], (ri / NVR) & 1, abort_p, lim);
+              if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
+              const uint32_t wb = sv0 + rs * VSLOT + dl;
+              uint32_t r[WVROWS / 2];
+#pragma unroll
+              for (int i = 0; i < WVROWS / 2; ++i)
+                r[i] = tc::e4m3x2_to_f16x2(tc::lds8(wb + 256 * i) | (tc::lds8(wb + 256 * i + 128) << 8));
+              tc::reg_fence16(r);
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sh.vr_empty[rs]);
+              // entries beyond the window's count are zero
+              const int t0 = WVROWS * (k % WVQ);
+              if (t0 + WVROWS > nvalid) {
+#pragma unroll
+                for (int i = 0; i < WVROWS / 2; ++i) {
+                  const int tt = t0 + 2 * i;
+                  if (tt >= nvalid) r[i] = 0u;
+                  else if (tt + 1 >= nvalid) r[i] &= 0xFFFFu;
+                }
+              }
+              tc::reg_fence16(r);
+              const bool s_ok = pc < 0 || tc::mbar_wait(&sh.vempty[pc % NVG], (pc / NVG) & 1, abort_p, lim);
+              if (!__all_sync(0xffffffffu, s_ok)) { fail(sh, a.err); ok = false; break; }
+              tc::tc_fence_after();
+              tc::tmem_st16(tbase + lb + COL_V + 32 * vs, r);
+              tc::tc_wait_st();
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
+              continue;
+            }
+            const int h = k & (halves - 1);           // page half (halves is 1 or 2)
             uint32_t r[32];
-            if (!win) {
-              const int ri = vbase + k, rs = ri % NVR;
+            {
               const bool w_ok = tc::mbar_wait(&sh.vr_full[rs], (ri / NVR) & 1, abort_p, lim);
               if (!__all_sync(0xffffffffu, w_ok)) { fail(sh, a.err); ok = false; break; }
               const uint32_t base = sv0 + rs * VSLOT;
@@ -932,14 +994,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
               tc::reg_fence32(r);                      // the slot's codes are in registers: release it
               __syncwarp();
               if (lane == 0) tc::mbar_arrive(&sh.vr_empty[rs]);
-            } else {
-              const uint8_t* col = u.wv + d;
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int e = 64 * h + 2 * i;
-                const uint32_t b0 = __ldg(col + (size_t)e * D), b1 = __ldg(col + (size_t)(e + 1) * D);
-                r[i] = tc::e4m3x2_to_f16x2(b0 | (b1 << 8));
-              }
             }
             // zero the tokens beyond the valid count
             const int t0 = 64 * h;
@@ -953,7 +1007,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             }
             tc::reg_fence32(r);             // conversion done before the (blocking) slot wait
             // the PV of the chunk NVS before this one has read the TMEM slot
-            const int vs = ci % NVS, pc = ci - NVS;
             const bool s_ok = pc < 0 || tc::mbar_wait(&sh.vempty[pc % NVG], (pc / NVG) & 1, abort_p, lim);
             if (!__all_sync(0xffffffffu, s_ok)) { fail(sh, a.err); ok = false; break; }
             tc::tc_fence_after();
@@ -964,7 +1017,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             if (lane == 0) tc::mbar_arrive(&sh.vfull[vs]);
           }
           ci0 += nk;
-          if (!win) vbase += nk;
+          vbase += nk;
         }
         x = tile_start[g] + j1;
         ++g;
@@ -1350,14 +1403,16 @@ cudaError_t set_attrs() {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // tensor map of a window K buffer [rows][d] (uint8): boxes of 128 rows x 128 bytes, 128-byte swizzle
-cudaError_t window_map(const uint8_t* wk, int d, int rows, CUtensorMap* map) {
+// window K (128 x 128 boxes, 128-byte swizzle: the MMA's A operand) or window V
+// (128 channels x WVROWS entries, no swizzle: read byte by byte by the V warps)
+cudaError_t window_map(const uint8_t* w, int d, int rows, int box_rows, bool swz, CUtensorMap* map) {
   if (!g_encode) return cudaErrorInitializationError;
   const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)d};
-  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(wk), dims, strides, box, es,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -1421,9 +1476,10 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   p += rows * a.H * 4;
   p = (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
   a.qs = p;
-  CUtensorMap wmap;
+  CUtensorMap wmap, vmap;
   const int nseq = a.replay ? a.n_groups / PKV_WINDOW : a.n_groups;
-  cudaError_t e = window_map(a.wk, a.D, nseq * PKV_WINDOW, &wmap);
+  cudaError_t e = window_map(a.wk, a.D, nseq * PKV_WINDOW, 128, true, &wmap);
+  if (e == cudaSuccess) e = window_map(a.wv, a.D, nseq * PKV_WINDOW, WVROWS, false, &vmap);
   if (e != cudaSuccess) return e;
   plan_kernel<<<1, 1024, 0, st>>>(a, tile_start, G);
   e = cudaGetLastError();
@@ -1438,9 +1494,9 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   if (e != cudaSuccess) return e;
   if (e0 && e1) cudaEventRecord(e0, st);
   switch (a.D) {
-    case 128: attn_tc_kernel<128><<<G, NTHREADS, Cfg<128>::DYN, st>>>(a, wmap, tile_start, part_o, part_lse); break;
-    case 256: attn_tc_kernel<256><<<G, NTHREADS, Cfg<256>::DYN, st>>>(a, wmap, tile_start, part_o, part_lse); break;
-    case 512: attn_tc_kernel<512><<<G, NTHREADS, Cfg<512>::DYN, st>>>(a, wmap, tile_start, part_o, part_lse); break;
+    case 128: attn_tc_kernel<128><<<G, NTHREADS, Cfg<128>::DYN, st>>>(a, wmap, vmap, tile_start, part_o, part_lse); break;
+    case 256: attn_tc_kernel<256><<<G, NTHREADS, Cfg<256>::DYN, st>>>(a, wmap, vmap, tile_start, part_o, part_lse); break;
+    case 512: attn_tc_kernel<512><<<G, NTHREADS, Cfg<512>::DYN, st>>>(a, wmap, vmap, tile_start, part_o, part_lse); break;
     default: return cudaErrorInvalidValue;
   }
   e = cudaGetLastError();

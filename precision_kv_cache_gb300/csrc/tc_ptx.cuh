@@ -25,6 +25,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(saddr));
   return v;
 }
+__device__ __forceinline__ uint32_t lds8(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(saddr));
+  return v;
+}
 __device__ __forceinline__ uint32_t lds16(uint32_t saddr) {
   uint16_t v;
   asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(saddr));
@@ -395,6 +400,11 @@ __device__ __forceinline__ void reg_fence32(uint32_t* r) {
   asm volatile("" : "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]),
                "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
                "+r"(r[31]));
+}
+// The same on 16 values.
+__device__ __forceinline__ void reg_fence16(uint32_t* r) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+               "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 
 // ---------------------------------------------------------------- conversions
