@@ -67,6 +67,11 @@ constexpr int W_VPROD = 22;            // V page producer
 constexpr int W_PV = 23;               // PV MMA issuer
 constexpr uint32_t NGRP = 4;           // arrivals per V ring slot release / V chunk: one per warp of a group
 constexpr int NVG = 3;                 // V dequant groups (chunk i of the CTA to group i % NVG)
+// Planning units per query row beyond its tiles: the CTA ranges are cut over
+// tiles + ROW_END units per row, so a range that holds a row's end (window tile,
+// partial write, the next row's start: measured at about four to five tiles of
+// time) gets that many fewer tiles.  The extra units hold no work.
+constexpr int ROW_END = 5;
 constexpr float TAU = 8.f;             // lazy rescale threshold (log2 units)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, int* tile_start,
       int b, ng, nw;
       const uint8_t *wk, *wv;
       unit_extent(a, g, &b, &ng, &nw, &wk, &wv);
-      n = (ng + TILE - 1) / TILE + 1;
+      n = (ng + TILE - 1) / TILE + 1 + ROW_END;
     }
     int incl = n;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -445,7 +450,7 @@ __device__ __forceinline__ void sf_settle(const AttnArgs& a, const int* tile_sta
       c.live = false;
       break;
     }
-    const int nt = tile_start[c.g + 1] - tile_start[c.g];
+    const int nt = tile_start[c.g + 1] - tile_start[c.g] - ROW_END;
     c.j = 0;
     c.jend = (int)min((long long)(nt - 1), x1 - tile_start[c.g]);
     int nw;
@@ -456,7 +461,7 @@ __device__ __forceinline__ void sf_settle(const AttnArgs& a, const int* tile_sta
 
 __device__ __forceinline__ SfCursor sf_first(const AttnArgs& a, const int* tile_start, long long x0, long long x1, int g0) {
   SfCursor c;
-  const int nt = tile_start[g0 + 1] - tile_start[g0];
+  const int nt = tile_start[g0 + 1] - tile_start[g0] - ROW_END;
   c.g = g0;
   c.j = (int)(x0 - tile_start[g0]);
   c.jend = (int)min((long long)(nt - 1), x1 - tile_start[g0]);
@@ -572,7 +577,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       int g = g0;
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
-        const int nt = tile_start[g + 1] - tile_start[g];
+        const int nt = tile_start[g + 1] - tile_start[g] - ROW_END;   // tiles of the row
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         const int npr = (u.n_glob + PKV_PAGE - 1) / PKV_PAGE;       // pages of the row
@@ -629,7 +634,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             }
           }
         }
-        x = tile_start[g] + j1;
+        x = min((long long)tile_start[g + 1], x1);
         ++g;
       }
       // drain: every copy issued must have landed before this CTA may exit
@@ -649,7 +654,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       int g = g0;
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
-        const int nt = tile_start[g + 1] - tile_start[g];
+        const int nt = tile_start[g + 1] - tile_start[g] - ROW_END;   // tiles of the row
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         const int npr = (u.n_glob + PKV_PAGE - 1) / PKV_PAGE;
@@ -690,7 +695,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         }
         // the window tile: NVCH x WVQ chunks of WVROWS entries x 128 channels (E4M3),
         // one ring slot each, by TMA in the same groups of VGRP
-        if (ok && j1 == nt) {
+        if (ok && j0 < j1 && j1 == nt) {
           const int n = C::NVCH * WVQ;
           for (int k = 0; k < n && ok; k += VGRP) {
             const int ni = min(VGRP, n - k);
@@ -710,7 +715,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
             vi += ni;
           }
         }
-        x = tile_start[g] + j1;
+        x = min((long long)tile_start[g + 1], x1);
         ++g;
       }
       if (lane == 0)
@@ -732,7 +737,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       long long x = x0;
       int g = g0;
       while (x < x1 && ok) {
-        const int nt = tile_start[g + 1] - tile_start[g];
+        const int nt = tile_start[g + 1] - tile_start[g] - ROW_END;   // tiles of the row
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         for (int j = j0; j < j1 && ok; ++j) {
@@ -819,7 +824,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           }
           ++nq;
         }
-        x = tile_start[g] + j1;
+        x = min((long long)tile_start[g + 1], x1);
         ++g;
       }
       if (!ok && lane == 0) fail(sh, a.err);
@@ -843,12 +848,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       int g = g0;
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
-        const int nt = tile_start[g + 1] - tile_start[g];
+        const int nt = tile_start[g + 1] - tile_start[g] - ROW_END;   // tiles of the row
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
-        // O of the previous item read out by the epilogue
-        ok = tc::mbar_wait(&sh.o_empty, (ip & 1) ^ 1, abort_p, lim);
-        ++ip;
+        // O of the previous item read out by the epilogue (a row whose part of the
+        // range is planning units only is no item)
+        if (j0 < j1) {
+          ok = tc::mbar_wait(&sh.o_empty, (ip & 1) ^ 1, abort_p, lim);
+          ++ip;
+        }
         for (int j = j0; j < j1 && ok; ++j) {
           ok = tc::mbar_wait(&sh.p_full[np & 1], (np >> 1) & 1, abort_p, lim);
           const uint64_t bpn = dp0 + (uint64_t)(((np & 1) * C::P_BYTES) >> 4);
@@ -882,7 +890,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           }
           ++np;
         }
-        x = tile_start[g] + j1;
+        x = min((long long)tile_start[g + 1], x1);
         ++g;
       }
       if (!ok && lane == 0) fail(sh, a.err);
@@ -900,7 +908,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
     // one phase ahead - its previous chunk's wait saw the phase before).  Each warp converts the E4M3 block scales it needs once per chunk
     // (two per lane) and shares them through shared memory; the ring slot is
     // released as soon as its codes are read.
-    else if (warp < W_SMAX) {
+    else if (warp >= W_VDEQ && warp < W_VDEQ + 4 * NVG) {
       const int vw = warp - W_VDEQ;                  // 0 .. 4 NVG - 1
       const int dl = 32 * (vw & 3) + lane;           // channel lane 0..127 within a chunk
       const int vg = vw >> 2;                        // group: chunks i with i % NVG == vg
@@ -914,7 +922,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       int g = g0;
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
-        const int nt = tile_start[g + 1] - tile_start[g];
+        const int nt = tile_start[g + 1] - tile_start[g] - ROW_END;   // tiles of the row
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
         for (int j = j0; j < j1 && ok; ++j) {
@@ -1019,12 +1027,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
           ci0 += nk;
           vbase += nk;
         }
-        x = tile_start[g] + j1;
+        x = min((long long)tile_start[g + 1], x1);
         ++g;
       }
     }
     // ======================================================== softmax + epilogue
-    else if (warp < W_KPROD) {
+    else if (warp >= W_SMAX && warp < W_SMAX + 8) {
       const int st = tid - 32 * W_SMAX;         // 0..255
       const int hh = (warp - W_SMAX) >> 2;      // head half: heads 32*hh .. 32*hh+31
       const int q4 = warp & 3;                  // TMEM lane quarter
@@ -1066,9 +1074,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
       int g = g0;
       while (x < x1 && ok) {
         const Unit u = unit_of(a, g);
-        const int nt = tile_start[g + 1] - tile_start[g];
+        const int nt = tile_start[g + 1] - tile_start[g] - ROW_END;   // tiles of the row
         const int j0 = (int)(x - tile_start[g]);
         const int j1 = (int)min((long long)nt, x1 - tile_start[g]);
+        if (j0 >= j1) {                     // planning units only: no item
+          x = min((long long)tile_start[g + 1], x1);
+          ++g;
+          continue;
+        }
         // the running max and the logit factors of the row's two query forms
         // (split ahead, in global memory); every thread passed the previous
         // row's closing barrier, so nobody reads the old ones any more
@@ -1270,7 +1283,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
         tc::tc_fence_before();
         tc::named_bar(1, 256);                 // sh.red / sh.m / zs reads done before the next item resets them
         if (lane == 0) tc::mbar_arrive(&sh.o_empty);
-        x = tile_start[g] + j1;
+        x = min((long long)tile_start[g + 1], x1);
         ++g;
       }
       if (sfw) tc::cp_async_wait_all();      // a staging copy of a role that gave up lands before exit
@@ -1306,7 +1319,7 @@ __global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups
   const int g = blockIdx.x / H, h = blockIdx.x % H;
   const long long T = tile_start[n_groups];
   if (threadIdx.x < 32) {
-    const long long first = tile_start[g], last = tile_start[g + 1] - 1;
+    const long long first = tile_start[g], last = tile_start[g + 1] - 1 - ROW_END;   // the window tile
     const int c_lo = (int)(((first + 1) * G - 1) / T), c_hi = (int)(((last + 1) * G - 1) / T);
     const int n = min(c_hi - c_lo + 1, 1024);
     float m = -INFINITY;
