@@ -13,8 +13,9 @@
 //
 // Design (one persistent CTA per SM, 768 threads, warp-specialized):
 //   * work = 128-token tiles; each query row has ceil(L/128) NVFP4 tiles plus
-//     one window tile; the concatenated tile list is cut into one contiguous
-//     range per CTA (balanced to one tile).
+//     one window tile; the concatenated tile list, with ROW_END empty planning
+//     units after every row (the cost of a row's end), is cut into one
+//     contiguous range per CTA.
 //   * S^T = K Q^T (M = 128 tokens, N = 64 heads) runs on the block-scaled FP4
 //     tensor-core contraction: A = the two K pages of a tile as stored (E2M1
 //     codes, K-major with the 128/64-byte swizzle; copied from shared memory
@@ -26,7 +27,8 @@
 //   * the window tile's S^T runs on the FP8 contraction: A = the window K codes
 //     (E4M3, copied by TMA with the 128-byte swizzle), B = the query as two E4M3
 //     terms with a power-of-two factor per head (exact for a bf16 query).
-//   * warp 22 streams V pages into a shared-memory ring; warps 0-11, three
+//   * warp 22 streams V pages (and the window V, 32 entries per ring slot, by
+//     TMA) into a shared-memory ring; warps 0-11, three
 //     groups of four, dequantize V^T to f16 into TMEM (thread = channel, 128
 //     channels x 64 tokens at a time: the A operand of O^T = V^T P, M = 128
 //     channels, N = 64 heads); warp 23 issues the PV MMAs (P f16 in shared
