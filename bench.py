@@ -159,7 +159,8 @@ class ClockSampler:
                 if v.strip().lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "sampled_s": round(self.t1 - self.t0 + 0.25, 3)}
 
 
 def measured_peak():
