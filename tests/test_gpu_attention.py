@@ -63,6 +63,21 @@ def test_decode_ragged(d, H):
     _decode_case(wl, win_len=[128, 5, 0, 1])
 
 
+@pytest.mark.parametrize("d,H", [(512, 64), (256, 16)])
+def test_decode_many_short_rows(d, H):
+    """Many short ragged rows: most CTA ranges hold several row ends (window tiles
+    read through the V ring), some hold planning units only, windows of every
+    length from empty to full."""
+    rs = np.random.default_rng(11)
+    B = 40
+    lens = rs.integers(0, 400, size=B)
+    lens[:4] = [0, 1, 64, 129]
+    wins = rs.integers(0, 129, size=B)
+    wins[:4] = [0, 128, 1, 31]
+    wl = W.make_dense("short_rows", 12, B, H, d, lens)
+    _decode_case(wl, win_len=list(int(w) for w in wins))
+
+
 def test_decode_empty_everything():
     import torch
     wl = W.make_dense("empty", 6, 2, 64, 512, [0, 64])
