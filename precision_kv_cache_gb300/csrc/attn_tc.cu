@@ -180,15 +180,17 @@ __device__ __forceinline__ Unit unit_of(const AttnArgs& a, int g) {
   return u;
 }
 
-// ---------------------------------------------------------------- plan kernel
-// tile_start[g] = sum over g' < g of (ceil(n_glob(g')/128) + 1); tile_start[n] = total;
-// then tile_start[n + 1 + c] = the query row where CTA c (of G) starts.
-__global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, int* tile_start, int G) {
+// ---------------------------------------------------------------- plan
+// tile_start[g] = sum over g' < g of (ceil(n_glob(g')/128) + 1 + ROW_END); tile_start[n] =
+// total; then tile_start[n + 1 + c] = the query row where CTA c (of G) starts
+// (run by one block of the query-split launch, whose other blocks do not read it)
+__device__ __noinline__ void plan_tiles(const AttnArgs& a, int* tile_start, int G) {
   __shared__ int wsum[32];
   __shared__ int carry;
+  const int NT = blockDim.x;
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
-  for (int base = 0; base < a.n_groups; base += 1024) {
+  for (int base = 0; base < a.n_groups; base += NT) {
     const int g = base + threadIdx.x;
     int n = 0;
     if (g < a.n_groups) {
@@ -210,13 +212,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a, int* tile_start,
     for (int i = 0; i < w; ++i) pre += wsum[i];
     if (g < a.n_groups) tile_start[g] = pre + incl - n;
     __syncthreads();
-    if (threadIdx.x == 1023) carry = pre + incl;
+    if (threadIdx.x == NT - 1) carry = pre + incl;
     __syncthreads();
   }
   if (threadIdx.x == 0) tile_start[a.n_groups] = carry;
   __syncthreads();
   const long long T = carry;
-  for (int c = threadIdx.x; c < G; c += 1024) tile_start[a.n_groups + 1 + c] = group_of(tile_start, a.n_groups, cta_start(T, G, c));
+  for (int c = threadIdx.x; c < G; c += NT) tile_start[a.n_groups + 1 + c] = group_of(tile_start, a.n_groups, cta_start(T, G, c));
 }
 
 // ---------------------------------------------------------------- helpers
@@ -328,7 +330,8 @@ __device__ __forceinline__ void cvt_q8(const AttnArgs& a, uint4 v, int c, int po
 // group of 256 / (D/32) heads); thread st takes head st / (D/32) of the group
 // and its 32 channels 32 * (st % (D/32)) ..; heads >= H are written as zero.
 template <int D>
-__global__ void __launch_bounds__(256) qsplit_kernel(AttnArgs a, uint8_t* __restrict__ qs) {
+__global__ void __launch_bounds__(256) qsplit_kernel(AttnArgs a, uint8_t* __restrict__ qs, int* tile_start, int G) {
+  if (blockIdx.x == 0 && blockIdx.y == 0) plan_tiles(a, tile_start, G);   // the attention launch's tile plan
   using C = Cfg<D>;
   using KL = KLayout<D>;
   constexpr int PARTS = D / 32;              // threads per head
@@ -1496,13 +1499,10 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   cudaError_t e = window_map(a.wk, a.D, nseq * PKV_WINDOW, 128, true, &wmap);
   if (e == cudaSuccess) e = window_map(a.wv, a.D, nseq * PKV_WINDOW, WVROWS, false, &vmap);
   if (e != cudaSuccess) return e;
-  plan_kernel<<<1, 1024, 0, st>>>(a, tile_start, G);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   switch (a.D) {
-    case 128: qsplit_kernel<128><<<dim3(a.n_groups, 1), 256, 0, st>>>(a, p); break;
-    case 256: qsplit_kernel<256><<<dim3(a.n_groups, 2), 256, 0, st>>>(a, p); break;
-    case 512: qsplit_kernel<512><<<dim3(a.n_groups, 4), 256, 0, st>>>(a, p); break;
+    case 128: qsplit_kernel<128><<<dim3(a.n_groups, 1), 256, 0, st>>>(a, p, tile_start, G); break;
+    case 256: qsplit_kernel<256><<<dim3(a.n_groups, 2), 256, 0, st>>>(a, p, tile_start, G); break;
+    case 512: qsplit_kernel<512><<<dim3(a.n_groups, 4), 256, 0, st>>>(a, p, tile_start, G); break;
     default: return cudaErrorInvalidValue;
   }
   e = cudaGetLastError();
@@ -1529,6 +1529,6 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   ep.err = a.err;
   merge_tc_kernel<<<a.n_groups * a.H, a.D / 4, 0, st>>>(tile_start, a.n_groups, G, a.H, a.D, part_o, part_lse,
                                                         out, out_lse, ep);
-  *n_launches = 4;
+  *n_launches = 3;
   return cudaGetLastError();
 }
