@@ -2,13 +2,13 @@
 // vLLM blog "Kernels"):  score_t = sum_h w_h * ReLU(q_h . k_t)  over the
 // 128-channel NVFP4 index keys, for every position of every sequence.
 //
-// One persistent CTA per SM, 768 threads, warp-specialized:
+// One persistent CTA per SM, 896 threads, warp-specialized:
 //   * warp 0 streams the 64-token key pages into a 24-page shared-memory ring
 //     (1-D bulk copies);
-//   * warps 4-11 and 20-23: three groups of four (one warp per TMEM lane
-//     quarter, thread = token) that take every third 128-token tile and
+//   * warps 4-11 and 20-27: four groups of four (one warp per TMEM lane
+//     quarter, thread = token) that take every fourth 128-token tile and
 //     dequantize it to f16 into TMEM (exact: E2M1 x E4M3 has <= 6 significant
-//     bits);
+//     bits), 32 channels at a time;
 //   * warp 1 issues S^T = K Q^T on tcgen05 (M = 128 tokens, N = 64 index heads,
 //     K = 128; Q = the FP8 index queries, exact in f16, in shared memory), the
 //     whole warp running the schedule and one elected lane issuing;
@@ -26,11 +26,14 @@ namespace tcscore {
 constexpr int TILE = 128;
 constexpr int NH = 64;
 constexpr int D = 128;
-constexpr int NTHREADS = 768;                          // 24 warps
+constexpr int NTHREADS = 896;                          // 28 warps
 constexpr int W_PROD = 0, W_MMA = 1, W_DEQ = 4, W_EPI = 12, W_DEQ2 = 20;
-constexpr int NKG = 3;                                 // key dequant groups: warps 4-7, 8-11, 20-23
+constexpr int NKG = 4;                                 // key dequant groups: warps 4-7, 8-11, 20-23, 24-27
 constexpr int NR = 24;                                 // key ring: page slots
 constexpr int NS = 4;                                  // K / S^T tile slots in TMEM
+// A ring slot's consecutive uses (pages k and k + NR: tiles NR / 2 apart) must fall to
+// the same dequant group, so that a group never waits on a slot one phase too early.
+static_assert((NR / 2) % NKG == 0, "ring depth in tiles must be a multiple of the dequant groups");
 constexpr int PAGE_DATA = PKV_PAGE * D / 2;            // 4096
 constexpr int PAGE_SCALE = PKV_PAGE * D / 16;          // 512
 constexpr int PSLOT = PAGE_DATA + PAGE_SCALE;          // 4608
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
       // ======================================================== key dequantizer (thread = token)
       // group kg takes the tiles n = kg, kg + NKG, ... of this CTA (n counted from x0)
       const int t = 32 * (warp & 3) + lane;
-      const int kg = warp >= W_DEQ2 ? 2 : (warp - W_DEQ) >> 2;
+      const int kg = warp >= W_DEQ2 ? 2 + ((warp - W_DEQ2) >> 2) : (warp - W_DEQ) >> 2;
       const uint32_t lb = lane_base(warp);
       const uint32_t ring_s = tc::smem_u32(ring);
       int pc0 = 0, n0 = 0;      // ring pages and tiles of the CTA before this row's first tile in range
@@ -301,27 +304,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
             sc[1] = (slot & 1) ? sv.w : sv.y;
           }
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {             // channels 64*hf .. 64*hf+63
-            uint32_t r[32];
+          for (int qt = 0; qt < 4; ++qt) {             // channels 32*qt .. 32*qt+31
+            uint32_t r[16];
             if (valid) {
-              const uint4 lo = tc::lds128(row + 16 * ((2 * hf) ^ (slot & 3)));
-              const uint4 hi = tc::lds128(row + 16 * ((2 * hf + 1) ^ (slot & 3)));
-              const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+              const uint4 v = tc::lds128(row + 16 * (qt ^ (slot & 3)));
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
               uint32_t s4[2];
-              tc::e4m3x4_to_f16x2x2(sc[hf], s4);
+              tc::e4m3x4_to_f16x2x2(sc[qt >> 1], s4);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
+              for (int q = 0; q < 4; ++q) {
                 uint32_t e[4];
                 tc::e2m1x8_to_f16x2x4(w[q], e);
+                const int qq = 4 * (qt & 1) + q;
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                  r[4 * q + i] = (q & 2) ? tc::hmul2_hi(e[i], s4[q >> 2]) : tc::hmul2_lo(e[i], s4[q >> 2]);
+                  r[4 * q + i] = (qq & 2) ? tc::hmul2_hi(e[i], s4[qq >> 2]) : tc::hmul2_lo(e[i], s4[qq >> 2]);
               }
             } else {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = 0u;
+              for (int i = 0; i < 16; ++i) r[i] = 0u;
             }
-            tc::tmem_st32(tbase + lb + COL_K + 64 * s + 32 * hf, r);
+            tc::tmem_st16(tbase + lb + COL_K + 64 * s + 16 * qt, r);
           }
           tc::tc_wait_st();
           tc::tc_fence_before();

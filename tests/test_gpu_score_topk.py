@@ -17,7 +17,7 @@ from oracle import formats as F
 pytestmark = pytest.mark.gpu
 
 
-def _index_case(wl, k, keys_override=None, w_override=None):
+def _index_case(wl, k, keys_override=None, w_override=None, qc_override=None):
     import torch
     import precision_kv_cache_gb300 as P
     dev = torch_dev()
@@ -27,9 +27,12 @@ def _index_case(wl, k, keys_override=None, w_override=None):
         rows = wl.index_rows(p) if keys_override is None else keys_override(p)
         c, s = F.nvfp4_quantize(rows, ts)
         pool.store(p, np.arange(64), c, s)
-    qf = wl.index_q()
-    tq = F.tensor_scale_fp8(qf)
-    qc = F.fp8_quantize(qf, tq)
+    if qc_override is None:
+        qf = wl.index_q()
+        tq = F.tensor_scale_fp8(qf)
+        qc = F.fp8_quantize(qf, tq)
+    else:
+        qc, tq = qc_override
     w = wl.index_w() if w_override is None else w_override
     ic = P.IdxCache(torch.from_numpy(pool.data).to(dev), torch.from_numpy(pool.scale).to(dev), float(ts))
     ctx = P.Context(512, 64)
@@ -98,3 +101,22 @@ def test_planted_tokens_selected():
     gi = _index_case(wl, 16, keys_override=keys)
     for (pp, s) in planted:
         assert 64 * pp + s in set(gi[0].tolist())
+
+
+def test_score_queries_of_every_magnitude():
+    """FP8 query codes over the whole E4M3 range (448 down to the 2^-9 subnormal, both
+    signs) in every 16-channel block, blocks mixing the largest and smallest
+    magnitudes, a head of zeros and an all-zero query: the largest number of FP4
+    query terms the kernel builds, each score within the FP32 bound (exactly 0 for
+    the zero query)."""
+    wl = W.make_dense("qmag", 23, 3, 64, 512, [3000, 1500, 700])
+    rng = np.random.default_rng(23)
+    valid = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    qc = rng.choice(valid, size=(3, 64, 128)).astype(np.uint8)
+    qc[0, 0, :] = 0x7E                     # 448 everywhere
+    qc[0, 1, :] = 0x01                     # 2^-9 everywhere
+    qc[0, 2, 0::2], qc[0, 2, 1::2] = 0x7E, 0x81     # 448 and -2^-9 side by side
+    qc[0, 3, :] = 0x00
+    qc[1, :, :16] = 0xFE                   # -448 in block 0 of every head
+    qc[2] = 0                              # zero query: every score is exactly 0
+    _index_case(wl, 200, qc_override=(qc, np.float32(0.0125)))
