@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
     const float* __restrict__ k_new, const float* __restrict__ v_new,
     const int32_t* __restrict__ seq_idx, const int32_t* __restrict__ pos, int n,
     pkv_kv_cache cache, const int32_t* __restrict__ page_table, int max_pages, int* err) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   const int i = warp >> 1;
@@ -101,6 +103,8 @@ __global__ void __launch_bounds__(256) append_index_kernel(
     const float* __restrict__ x, const int32_t* __restrict__ seq_idx,
     const int32_t* __restrict__ pos, int n, pkv_idx_cache ic,
     const int32_t* __restrict__ page_table, int max_pages, int* err) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   constexpr int D = 128;
   const int i = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -113,6 +117,8 @@ __global__ void __launch_bounds__(256) append_index_kernel(
 
 __global__ void __launch_bounds__(256) quantize_fp8_kernel(const float* __restrict__ x, size_t n,
                                                            float tw, uint8_t* __restrict__ out) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   size_t i = (size_t)(blockIdx.x * blockDim.x + threadIdx.x) * 4;
   const size_t stride = (size_t)gridDim.x * blockDim.x * 4;
   for (; i < n; i += stride) {
@@ -137,12 +143,11 @@ cudaError_t pkv_launch_append_kv(int d, const float* k_new, const float* v_new, 
   const long long warps = 2LL * n;
   const int blocks = (int)((warps * 32 + 255) / 256);
   switch (d) {
-    case 128: pkv::append_kv_kernel<128><<<blocks, 256, 0, st>>>(k_new, v_new, seq_idx, pos, n, cache, page_table, max_pages, err); break;
-    case 256: pkv::append_kv_kernel<256><<<blocks, 256, 0, st>>>(k_new, v_new, seq_idx, pos, n, cache, page_table, max_pages, err); break;
-    case 512: pkv::append_kv_kernel<512><<<blocks, 256, 0, st>>>(k_new, v_new, seq_idx, pos, n, cache, page_table, max_pages, err); break;
+    case 128: return pkv::launch_pdl(pkv::append_kv_kernel<128>, blocks, 256, 0, st, k_new, v_new, seq_idx, pos, n, cache, page_table, max_pages, err);
+    case 256: return pkv::launch_pdl(pkv::append_kv_kernel<256>, blocks, 256, 0, st, k_new, v_new, seq_idx, pos, n, cache, page_table, max_pages, err);
+    case 512: return pkv::launch_pdl(pkv::append_kv_kernel<512>, blocks, 256, 0, st, k_new, v_new, seq_idx, pos, n, cache, page_table, max_pages, err);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t pkv_launch_append_index(const float* x, const int32_t* seq_idx, const int32_t* pos, int n,
@@ -150,8 +155,7 @@ cudaError_t pkv_launch_append_index(const float* x, const int32_t* seq_idx, cons
                                     int* err, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   const int blocks = (int)(((long long)n * 32 + 255) / 256);
-  pkv::append_index_kernel<<<blocks, 256, 0, st>>>(x, seq_idx, pos, n, ic, page_table, max_pages, err);
-  return cudaGetLastError();
+  return pkv::launch_pdl(pkv::append_index_kernel, blocks, 256, 0, st, x, seq_idx, pos, n, ic, page_table, max_pages, err);
 }
 
 cudaError_t pkv_launch_quantize_fp8(const float* x, size_t n, float tw, uint8_t* out, cudaStream_t st) {
@@ -159,6 +163,5 @@ cudaError_t pkv_launch_quantize_fp8(const float* x, size_t n, float tw, uint8_t*
   size_t threads = (n + 3) / 4;
   int blocks = (int)((threads + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
-  pkv::quantize_fp8_kernel<<<blocks, 256, 0, st>>>(x, n, tw, out);
-  return cudaGetLastError();
+  return pkv::launch_pdl(pkv::quantize_fp8_kernel, blocks, 256, 0, st, x, n, tw, out);
 }

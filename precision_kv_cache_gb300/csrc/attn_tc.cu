@@ -331,6 +331,8 @@ __device__ __forceinline__ void cvt_q8(const AttnArgs& a, uint4 v, int c, int po
 // and its 32 channels 32 * (st % (D/32)) ..; heads >= H are written as zero.
 template <int D>
 __global__ void __launch_bounds__(256) qsplit_kernel(AttnArgs a, uint8_t* __restrict__ qs, int* tile_start, int G) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   if (blockIdx.x == 0 && blockIdx.y == 0) plan_tiles(a, tile_start, G);   // the attention launch's tile plan
   using C = Cfg<D>;
   using KL = KLayout<D>;
@@ -520,9 +522,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int G = gridDim.x, cta = blockIdx.x;
-  const long long T = tile_start[a.n_groups];
-  const long long x0 = cta_start(T, G, cta), x1 = cta_start(T, G, cta + 1);
-  const int g0 = tile_start[a.n_groups + 1 + cta];     // query row of tile x0 (from the plan)
   const long long lim = a.wait_limit;
 
   if (tid == 0) {
@@ -559,6 +558,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(AttnArgs a, const 
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tbase = sh.tmem_base;
+  // the set-up above may overlap the end of the query split; from here on the
+  // plan, the query terms and the cache it saw are read
+  pkv::dep_wait();
+  pkv::dep_trigger();
+  const long long T = tile_start[a.n_groups];
+  const long long x0 = cta_start(T, G, cta), x1 = cta_start(T, G, cta + 1);
+  const int g0 = tile_start[a.n_groups + 1 + cta];     // query row of tile x0 (from the plan)
 
   volatile int* abort_p = &sh.abort_flag;
 
@@ -1318,6 +1324,8 @@ struct Epilogue {
 __global__ void merge_tc_kernel(const int* __restrict__ tile_start, int n_groups, int G, int H, int D,
                                 const float* __restrict__ part_o, const float* __restrict__ part_lse,
                                 float* __restrict__ out, float* __restrict__ out_lse, Epilogue ep) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   __shared__ float wts[1024];
   __shared__ int nseg_s, cl_s, pos_s;
   __shared__ float lse_s;
@@ -1500,21 +1508,19 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   if (e == cudaSuccess) e = window_map(a.wv, a.D, nseq * PKV_WINDOW, WVROWS, false, &vmap);
   if (e != cudaSuccess) return e;
   switch (a.D) {
-    case 128: qsplit_kernel<128><<<dim3(a.n_groups, 1), 256, 0, st>>>(a, p, tile_start, G); break;
-    case 256: qsplit_kernel<256><<<dim3(a.n_groups, 2), 256, 0, st>>>(a, p, tile_start, G); break;
-    case 512: qsplit_kernel<512><<<dim3(a.n_groups, 4), 256, 0, st>>>(a, p, tile_start, G); break;
+    case 128: e = pkv::launch_pdl(qsplit_kernel<128>, dim3(a.n_groups, 1), 256, 0, st, a, p, tile_start, G); break;
+    case 256: e = pkv::launch_pdl(qsplit_kernel<256>, dim3(a.n_groups, 2), 256, 0, st, a, p, tile_start, G); break;
+    case 512: e = pkv::launch_pdl(qsplit_kernel<512>, dim3(a.n_groups, 4), 256, 0, st, a, p, tile_start, G); break;
     default: return cudaErrorInvalidValue;
   }
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (e0 && e1) cudaEventRecord(e0, st);
   switch (a.D) {
-    case 128: attn_tc_kernel<128><<<G, NTHREADS, Cfg<128>::DYN, st>>>(a, wmap, vmap, tile_start, part_o, part_lse); break;
-    case 256: attn_tc_kernel<256><<<G, NTHREADS, Cfg<256>::DYN, st>>>(a, wmap, vmap, tile_start, part_o, part_lse); break;
-    case 512: attn_tc_kernel<512><<<G, NTHREADS, Cfg<512>::DYN, st>>>(a, wmap, vmap, tile_start, part_o, part_lse); break;
+    case 128: e = pkv::launch_pdl(attn_tc_kernel<128>, G, NTHREADS, Cfg<128>::DYN, st, a, wmap, vmap, tile_start, part_o, part_lse); break;
+    case 256: e = pkv::launch_pdl(attn_tc_kernel<256>, G, NTHREADS, Cfg<256>::DYN, st, a, wmap, vmap, tile_start, part_o, part_lse); break;
+    case 512: e = pkv::launch_pdl(attn_tc_kernel<512>, G, NTHREADS, Cfg<512>::DYN, st, a, wmap, vmap, tile_start, part_o, part_lse); break;
     default: return cudaErrorInvalidValue;
   }
-  e = cudaGetLastError();
   if (e0 && e1) cudaEventRecord(e1, st);
   if (e != cudaSuccess) return e;
   Epilogue ep{};
@@ -1527,8 +1533,7 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   ep.out_scale = a.out_scale;
   ep.out_fp8 = a.out_fp8;
   ep.err = a.err;
-  merge_tc_kernel<<<a.n_groups * a.H, a.D / 4, 0, st>>>(tile_start, a.n_groups, G, a.H, a.D, part_o, part_lse,
-                                                        out, out_lse, ep);
   *n_launches = 3;
-  return cudaGetLastError();
+  return pkv::launch_pdl(merge_tc_kernel, a.n_groups * a.H, a.D / 4, 0, st, (const int*)tile_start, a.n_groups, G,
+                         a.H, a.D, (const float*)part_o, (const float*)part_lse, out, out_lse, ep);
 }

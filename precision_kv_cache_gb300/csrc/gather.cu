@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) gather_kernel(pkv_kv_cache src, const int
                                                      int max_pages, const int32_t* __restrict__ sel, int k,
                                                      int npb, pkv_kv_cache dst, int32_t* __restrict__ dst_len,
                                                      int* err) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   constexpr int PD = PKV_PAGE * D / 2, PS = PKV_PAGE * D / 16;
   __shared__ int spage[8], sslot[8];
   const int page = blockIdx.x >> 3, o = blockIdx.x & 7;
@@ -95,6 +97,8 @@ __global__ void __launch_bounds__(256) gather_kernel(pkv_kv_cache src, const int
 }
 
 __global__ void identity_table_kernel(int32_t* pt, int B, int npb) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < B * npb) pt[i] = i;
 }
@@ -127,15 +131,15 @@ cudaError_t pkv_launch_gather(int d, const pkv_kv_cache& src, const int32_t* pag
   *dst_pt = (int32_t*)take(pages * 4);
   *dst_len = (int32_t*)take((size_t)B * 4);
   *npb_out = npb;
-  pkv::identity_table_kernel<<<(int)((pages + 255) / 256), 256, 0, st>>>(*dst_pt, B, npb);
+  cudaError_t e = pkv::launch_pdl(pkv::identity_table_kernel, (int)((pages + 255) / 256), 256, 0, st, *dst_pt, B, npb);
+  if (e != cudaSuccess) return e;
   const int grid = (int)pages * 8;
   switch (d) {
-    case 128: pkv::gather_kernel<128><<<grid, 256, 0, st>>>(src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err); break;
-    case 256: pkv::gather_kernel<256><<<grid, 256, 0, st>>>(src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err); break;
-    case 512: pkv::gather_kernel<512><<<grid, 256, 0, st>>>(src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err); break;
+    case 128: return pkv::launch_pdl(pkv::gather_kernel<128>, grid, 256, 0, st, src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err);
+    case 256: return pkv::launch_pdl(pkv::gather_kernel<256>, grid, 256, 0, st, src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err);
+    case 512: return pkv::launch_pdl(pkv::gather_kernel<512>, grid, 256, 0, st, src, page_table, max_pages, sel, k, npb, *dst, *dst_len, err);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- candidate index keys
@@ -151,6 +155,8 @@ __global__ void __launch_bounds__(256) gather_index_kernel(pkv_idx_cache src, co
                                                            int max_pages, const int32_t* __restrict__ cand, int n,
                                                            int npb, pkv_idx_cache dst, int32_t* __restrict__ cnt,
                                                            int* err) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   constexpr int PD = PKV_PAGE * 64, PS = PKV_PAGE * 8;    // 128-channel index keys
   __shared__ int spage[64], sslot[64];
   const int page = blockIdx.x, b = page / npb, jp = page % npb;
@@ -199,6 +205,8 @@ __global__ void __launch_bounds__(256) gather_index_kernel(pkv_idx_cache src, co
 
 // out[b][i] (a candidate index, or -1) -> the candidate's position
 __global__ void map_cand_kernel(int32_t* __restrict__ out, const int32_t* __restrict__ cand, int B, int n, int k) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= B * k) return;
   const int b = i / k, c = out[i];
@@ -227,13 +235,13 @@ cudaError_t pkv_launch_gather_index(const pkv_idx_cache& src, const int32_t* pag
   *dst_pt = (int32_t*)take(pages * 4);
   *dst_cnt = (int32_t*)take((size_t)B * 4);
   *npb_out = npb;
-  pkv::identity_table_kernel<<<(int)((pages + 255) / 256), 256, 0, st>>>(*dst_pt, B, npb);
-  pkv::gather_index_kernel<<<(int)pages, 256, 0, st>>>(src, page_table, max_pages, cand, n, npb, *dst, *dst_cnt, err);
-  return cudaGetLastError();
+  const cudaError_t e = pkv::launch_pdl(pkv::identity_table_kernel, (int)((pages + 255) / 256), 256, 0, st, *dst_pt, B, npb);
+  if (e != cudaSuccess) return e;
+  return pkv::launch_pdl(pkv::gather_index_kernel, (int)pages, 256, 0, st, src, page_table, max_pages, cand, n, npb,
+                         *dst, *dst_cnt, err);
 }
 
 cudaError_t pkv_launch_map_cand(int32_t* out, const int32_t* cand, int B, int n, int k, cudaStream_t st) {
   const int tot = B * k;
-  pkv::map_cand_kernel<<<(tot + 255) / 256, 256, 0, st>>>(out, cand, B, n, k);
-  return cudaGetLastError();
+  return pkv::launch_pdl(pkv::map_cand_kernel, (tot + 255) / 256, 256, 0, st, out, cand, B, n, k);
 }

@@ -10,6 +10,8 @@ namespace pkv {
 // one block of 128 threads per row; o / lse may alias the a inputs
 __global__ void merge2_kernel(const float* o_a, const float* lse_a, const float* o_b,
                               const float* lse_b, float* o, float* lse, int rows, int dv) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   const int r = blockIdx.x;
   if (r >= rows) return;
   const float la = lse_a[r], lb = lse_b[r];
@@ -30,6 +32,5 @@ __global__ void merge2_kernel(const float* o_a, const float* lse_a, const float*
 cudaError_t pkv_launch_merge2(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
                               float* o, float* lse, int rows, int dv, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  pkv::merge2_kernel<<<rows, 128, 0, st>>>(o_a, lse_a, o_b, lse_b, o, lse, rows, dv);
-  return cudaGetLastError();
+  return pkv::launch_pdl(pkv::merge2_kernel, rows, 128, 0, st, o_a, lse_a, o_b, lse_b, o, lse, rows, dv);
 }

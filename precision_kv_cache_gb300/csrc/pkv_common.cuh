@@ -23,6 +23,35 @@ __device__ __forceinline__ void report(int* err, int bit) {
   if (err) atomicOr(err, bit);
 }
 
+// ---------------------------------------------------------------- dependent launch
+// A kernel started by launch_pdl may begin while the kernel before it in the
+// stream is still running (programmatic dependent launch).  Before it reads or
+// writes anything in global memory it calls dep_wait(), which returns once that
+// kernel has finished and its writes are visible; dep_trigger() then lets the
+// next kernel of the stream start.  Called after dep_wait(), it keeps at most
+// two kernels of a stream on the GPU at once.  Both are no-ops in a kernel
+// launched the plain way.
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with programmatic stream serialization (the kernel must call dep_wait()
+// before touching global memory).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---------------------------------------------------------------- encoders
 // E4M3 code of a finite a >= 0: nearest finite value, ties to the even code,
 // saturating at 448 (0x7E).  Subnormals (a < 2^-6) are multiples of 2^-9.

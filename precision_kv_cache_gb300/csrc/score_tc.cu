@@ -85,6 +85,8 @@ __device__ __forceinline__ int group_of(const int* ts, int n, long long x) {
 // tile_start[b] = sum over b' < b of ceil(L(b')/128); tile_start[B] = total;
 // then tile_start[B + 1 + c] = the sequence where CTA c (of G) starts.
 __global__ void __launch_bounds__(1024) plan_kernel(Args a, int* tile_start, int G) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   __shared__ int wsum[32];
   __shared__ int carry;
   if (threadIdx.x == 0) carry = 0;
@@ -152,9 +154,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
   __shared__ Shared sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
-  const long long T = tile_start[a.B];
-  const long long x0 = cta_start(T, G, cta), x1 = cta_start(T, G, cta + 1);
-  const int g0 = tile_start[a.B + 1 + cta];
   if (tid == 0) {
     for (int i = 0; i < NR; ++i) {
       tc::mbar_init(&sh.r_full[i], 1);
@@ -179,6 +178,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) score_tc_kernel(Args a, const int
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tbase = sh.tmem_base;
+  // the set-up above may overlap the end of the plan kernel
+  pkv::dep_wait();
+  pkv::dep_trigger();
+  const long long T = tile_start[a.B];
+  const long long x0 = cta_start(T, G, cta), x1 = cta_start(T, G, cta + 1);
+  const int g0 = tile_start[a.B + 1 + cta];
   volatile int* abort_p = &sh.abort_flag;
   uint8_t* sQ = dyn + OFF_Q;
   uint8_t* ring = dyn + OFF_R;
@@ -431,10 +436,10 @@ cudaError_t pkv_launch_score_tc(const uint8_t* q_idx, float tq, const float* w, 
   int* tile_start = (int*)ws;
   const long long tmax = (long long)B * ((Lmax + TILE - 1) / TILE);
   const int G = (int)(tmax < num_sms ? (tmax > 0 ? tmax : 1) : num_sms);
-  plan_kernel<<<1, 1024, 0, st>>>(a, tile_start, G);
+  cudaError_t e = pkv::launch_pdl(plan_kernel, 1, 1024, 0, st, a, tile_start, G);
+  if (e != cudaSuccess) return e;
   if (prof_start && prof_stop) cudaEventRecord(prof_start, st);
-  score_tc_kernel<<<G, NTHREADS, DYN, st>>>(a, tile_start);
-  const cudaError_t e = cudaGetLastError();
+  e = pkv::launch_pdl(score_tc_kernel, G, NTHREADS, DYN, st, a, (const int*)tile_start);
   if (prof_start && prof_stop) cudaEventRecord(prof_stop, st);
   return e;
 }

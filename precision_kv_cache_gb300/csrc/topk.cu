@@ -33,6 +33,8 @@ __device__ __forceinline__ int seq_length(const int32_t* seq_len, int b, int Lma
 __global__ void __launch_bounds__(TK_THREADS) tk_pass1(const float* __restrict__ scores, int Lmax,
                                                        const int32_t* __restrict__ seq_len,
                                                        uint32_t* __restrict__ hist) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   __shared__ uint32_t h[TK_BINS];
   const int b = blockIdx.y;
   for (int i = threadIdx.x; i < TK_BINS; i += TK_THREADS) h[i] = 0u;
@@ -61,6 +63,8 @@ __global__ void __launch_bounds__(TK_THREADS) tk_pass1(const float* __restrict__
 // at or above it first reaches `need` (scanning from the top bin down).
 __global__ void __launch_bounds__(1024) tk_find(const uint32_t* __restrict__ hist, int* __restrict__ state,
                                                 const int32_t* __restrict__ seq_len, int Lmax, int k, int level) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   __shared__ uint32_t warp_tot[32];
   const int b = blockIdx.x;
   int* st = state + b * ST_WORDS;
@@ -115,6 +119,8 @@ __device__ __forceinline__ void emit(uint32_t* bm_b, int* st, int t) {
 __global__ void __launch_bounds__(TK_THREADS) tk_pass2(const float* __restrict__ scores, int Lmax,
                                                        int* __restrict__ state, uint32_t* __restrict__ hist2,
                                                        uint32_t* __restrict__ bm, int W) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   __shared__ uint32_t h[TK_BINS];
   const int b = blockIdx.y;
   int* st = state + b * ST_WORDS;
@@ -151,6 +157,8 @@ __global__ void __launch_bounds__(TK_THREADS) tk_pass2(const float* __restrict__
 __global__ void __launch_bounds__(TK_THREADS) tk_pass3(const float* __restrict__ scores, int Lmax,
                                                        int* __restrict__ state, unsigned long long* __restrict__ cand,
                                                        int cap, uint32_t* __restrict__ bm, int W) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   const int b = blockIdx.y;
   int* st = state + b * ST_WORDS;
   const int bin1 = st[ST_BIN1];
@@ -204,6 +212,8 @@ __global__ void __launch_bounds__(1024) tk_finish(const float* __restrict__ scor
                                                   int* __restrict__ state,
                                                   const unsigned long long* __restrict__ cand, int cap,
                                                   uint32_t* __restrict__ bm, int W) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   extern __shared__ unsigned long long sv[];
   const int b = blockIdx.x;
   int* st = state + b * ST_WORDS;
@@ -280,6 +290,8 @@ __global__ void __launch_bounds__(1024) tk_finish(const float* __restrict__ scor
 // words, a block scan gives its output offset); the rest of the row is -1.
 __global__ void __launch_bounds__(1024) tk_extract(const uint32_t* __restrict__ bm, int W, int32_t* __restrict__ out,
                                                    int k) {
+  pkv::dep_wait();
+  pkv::dep_trigger();
   __shared__ int wsum[32];
   const int b = blockIdx.x;
   const uint32_t* bmb = bm + (size_t)b * W;
@@ -354,11 +366,15 @@ cudaError_t pkv_launch_topk(const float* scores, int Lmax, const int32_t* seq_le
   const int chunks = (Lmax + TK_THREADS * TK_ITEMS - 1) / (TK_THREADS * TK_ITEMS);
   dim3 grid(chunks > 0 ? chunks : 1, B);
   tk_pass1<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, seq_len, hist1);
-  tk_find<<<B, 1024, 0, st>>>(hist1, state, seq_len, Lmax, k, 1);
-  tk_pass2<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, state, hist2, bm, W);
-  tk_find<<<B, 1024, 0, st>>>(hist2, state, seq_len, Lmax, k, 2);
-  tk_pass3<<<grid, TK_THREADS, 0, st>>>(scores, Lmax, state, cand, PKV_TOPK_CAND, bm, W);
-  tk_finish<<<B, 1024, PKV_TOPK_CAND * 8, st>>>(scores, Lmax, state, cand, PKV_TOPK_CAND, bm, W);
-  tk_extract<<<B, 1024, 0, st>>>(bm, W, out, k);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_pdl(tk_find, B, 1024, 0, st, hist1, state, seq_len, Lmax, k, 1);
+  if (e == cudaSuccess) e = launch_pdl(tk_pass2, grid, TK_THREADS, 0, st, scores, Lmax, state, hist2, bm, W);
+  if (e == cudaSuccess) e = launch_pdl(tk_find, B, 1024, 0, st, hist2, state, seq_len, Lmax, k, 2);
+  if (e == cudaSuccess)
+    e = launch_pdl(tk_pass3, grid, TK_THREADS, 0, st, scores, Lmax, state, cand, (int)PKV_TOPK_CAND, bm, W);
+  if (e == cudaSuccess)
+    e = launch_pdl(tk_finish, B, 1024, (size_t)PKV_TOPK_CAND * 8, st, scores, Lmax, state, cand,
+                   (int)PKV_TOPK_CAND, bm, W);
+  if (e == cudaSuccess) e = launch_pdl(tk_extract, B, 1024, 0, st, bm, W, out, k);
+  return e;
 }
