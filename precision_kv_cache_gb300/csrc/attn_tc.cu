@@ -329,11 +329,16 @@ __device__ __forceinline__ void cvt_q8(const AttnArgs& a, uint4 v, int c, int po
 // plus the per-head logit factors (log2 units) of each form.  Grid: (row,
 // group of 256 / (D/32) heads); thread st takes head st / (D/32) of the group
 // and its 32 channels 32 * (st % (D/32)) ..; heads >= H are written as zero.
+// One more block (x = n_groups, y = 0) computes the attention launch's tile
+// plan, beside the splits rather than before one of them.
 template <int D>
 __global__ void __launch_bounds__(256) qsplit_kernel(AttnArgs a, uint8_t* __restrict__ qs, int* tile_start, int G) {
   pkv::dep_wait();
   pkv::dep_trigger();
-  if (blockIdx.x == 0 && blockIdx.y == 0) plan_tiles(a, tile_start, G);   // the attention launch's tile plan
+  if ((int)blockIdx.x == a.n_groups) {
+    if (blockIdx.y == 0) plan_tiles(a, tile_start, G);   // the attention launch's tile plan
+    return;
+  }
   using C = Cfg<D>;
   using KL = KLayout<D>;
   constexpr int PARTS = D / 32;              // threads per head
@@ -1508,9 +1513,9 @@ cudaError_t pkv_launch_attn_tc(pkv::AttnArgs& a, int num_sms, int max_entries, f
   if (e == cudaSuccess) e = window_map(a.wv, a.D, nseq * PKV_WINDOW, WVROWS, false, &vmap);
   if (e != cudaSuccess) return e;
   switch (a.D) {
-    case 128: e = pkv::launch_pdl(qsplit_kernel<128>, dim3(a.n_groups, 1), 256, 0, st, a, p, tile_start, G); break;
-    case 256: e = pkv::launch_pdl(qsplit_kernel<256>, dim3(a.n_groups, 2), 256, 0, st, a, p, tile_start, G); break;
-    case 512: e = pkv::launch_pdl(qsplit_kernel<512>, dim3(a.n_groups, 4), 256, 0, st, a, p, tile_start, G); break;
+    case 128: e = pkv::launch_pdl(qsplit_kernel<128>, dim3(a.n_groups + 1, 1), 256, 0, st, a, p, tile_start, G); break;
+    case 256: e = pkv::launch_pdl(qsplit_kernel<256>, dim3(a.n_groups + 1, 2), 256, 0, st, a, p, tile_start, G); break;
+    case 512: e = pkv::launch_pdl(qsplit_kernel<512>, dim3(a.n_groups + 1, 4), 256, 0, st, a, p, tile_start, G); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
