@@ -7,7 +7,8 @@
 //   finish  sort candidates by (key desc, position asc), emit what is still needed
 //           (if the candidate buffer overflowed: an ordered scan of the sequence)
 //   extract "emit" sets the position's bit in a per-sequence bitmap; the k
-//           positions are read out of it in ascending order (no sort)
+//           positions are read out of it in ascending order (no sort), one
+//           block per 1024-word chunk of the bitmap
 #include "pkv_common.cuh"
 #include "launch.h"
 
@@ -285,61 +286,61 @@ __global__ void __launch_bounds__(1024) tk_finish(const float* __restrict__ scor
   }
 }
 
-// The selected positions of sequence b, ascending, from its bitmap (one block of
-// 1024 threads per sequence: each thread counts the bits of a contiguous run of
-// words, a block scan gives its output offset); the rest of the row is -1.
+// The selected positions of sequence b, ascending, from its bitmap.  Grid
+// (chunks of 1024 words, sequences), 1024 threads: block j first counts the bits
+// of the words before its chunk (its output offset), then thread i takes word
+// 1024 j + i, a block scan gives the thread's offset inside the chunk, and the
+// set bits are written in order.  The last chunk's block pads the row with -1.
 __global__ void __launch_bounds__(1024) tk_extract(const uint32_t* __restrict__ bm, int W, int32_t* __restrict__ out,
                                                    int k) {
   pkv::dep_wait();
   pkv::dep_trigger();
   __shared__ int wsum[32];
-  const int b = blockIdx.x;
+  __shared__ int base_s;
+  const int b = blockIdx.y, j = blockIdx.x;
   const uint32_t* bmb = bm + (size_t)b * W;
   int32_t* ob = out + (size_t)b * k;
-  // thread i owns words [i*per, i*per + per); up to 16 of them are held in registers
-  const int per = (W + 1023) / 1024;
-  const int w0 = threadIdx.x * per, w1 = min(W, w0 + per);
-  constexpr int R = 16;
-  uint32_t x[R];
-#pragma unroll
-  for (int i = 0; i < R; ++i) x[i] = (i < per && w0 + i < w1) ? bmb[w0 + i] : 0u;
-  int cnt = 0;
-#pragma unroll
-  for (int i = 0; i < R; ++i) cnt += __popc(x[i]);
-  for (int w = w0 + R; w < w1; ++w) cnt += __popc(bmb[w]);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  // bits before this chunk
+  int before = 0;
+  for (int w = threadIdx.x; w < 1024 * j; w += 1024) before += __popc(bmb[w]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+  if (lane == 0) wsum[wid] = before;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int i = 0; i < 32; ++i) t += wsum[i];
+    base_s = t;
+  }
+  __syncthreads();
+  const int base = base_s;
+  // this chunk: one word per thread, offsets by a block scan
+  const int w = 1024 * j + threadIdx.x;
+  uint32_t y = w < W ? bmb[w] : 0u;
+  const int cnt = __popc(y);
   int incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
+  __syncthreads();                       // every thread has read base_s / the first wsum use is over
   if (lane == 31) wsum[wid] = incl;
   __syncthreads();
-  int pos = incl - cnt;
+  int pos = base + incl - cnt;
   for (int i = 0; i < wid; ++i) pos += wsum[i];
-  int total = 0;
-  for (int i = 0; i < 32; ++i) total += wsum[i];
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    uint32_t y = x[i];
-    while (y) {
-      const int bit = __ffs(y) - 1;
-      if (pos < k) ob[pos] = 32 * (w0 + i) + bit;
-      ++pos;
-      y &= y - 1;
-    }
+  while (y) {
+    const int bit = __ffs(y) - 1;
+    if (pos < k) ob[pos] = 32 * w + bit;
+    ++pos;
+    y &= y - 1;
   }
-  for (int w = w0 + R; w < w1; ++w) {
-    uint32_t y = bmb[w];
-    while (y) {
-      const int bit = __ffs(y) - 1;
-      if (pos < k) ob[pos] = 32 * w + bit;
-      ++pos;
-      y &= y - 1;
-    }
+  if (j == (int)gridDim.x - 1) {
+    int total = base;
+    for (int i = 0; i < 32; ++i) total += wsum[i];
+    for (int i = min(total, k) + threadIdx.x; i < k; i += 1024) ob[i] = -1;
   }
-  for (int i = min(total, k) + threadIdx.x; i < k; i += 1024) ob[i] = -1;
 }
 
 }  // namespace pkv
@@ -375,6 +376,6 @@ cudaError_t pkv_launch_topk(const float* scores, int Lmax, const int32_t* seq_le
   if (e == cudaSuccess)
     e = launch_pdl(tk_finish, B, 1024, (size_t)PKV_TOPK_CAND * 8, st, scores, Lmax, state, cand,
                    (int)PKV_TOPK_CAND, bm, W);
-  if (e == cudaSuccess) e = launch_pdl(tk_extract, B, 1024, 0, st, bm, W, out, k);
+  if (e == cudaSuccess) e = launch_pdl(tk_extract, dim3((W + 1023) / 1024, B), 1024, 0, st, bm, W, out, k);
   return e;
 }
