@@ -27,7 +27,11 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Every call is asynchronous on that stream; host-side validation happens
  *     before any launch and returns PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED
- *     without launching anything.
+ *     without launching anything.  The library's kernels are launched with
+ *     programmatic dependent launch: one may start while the kernel before it
+ *     on the stream is finishing, but waits for it to complete before touching
+ *     global memory, so stream order holds as for plain launches (a call sees
+ *     what earlier work on the stream wrote; later work sees its results).
  *   - Faults found on the device (a page id outside [0, num_pages), a sequence
  *     longer than its page table) never trap: the kernel skips the access,
  *     records a code in the context's device error word and finishes.
