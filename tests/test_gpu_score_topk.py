@@ -17,7 +17,7 @@ from oracle import formats as F
 pytestmark = pytest.mark.gpu
 
 
-def _index_case(wl, k, keys_override=None, w_override=None, qc_override=None):
+def _index_case(wl, k, keys_override=None, w_override=None, qc_override=None, quantize_on_device=False):
     import torch
     import precision_kv_cache_gb300 as P
     dev = torch_dev()
@@ -39,10 +39,21 @@ def _index_case(wl, k, keys_override=None, w_override=None, qc_override=None):
     Lmax = wl.page_table.shape[1] * 64
     out_idx = torch.empty(wl.B, k, dtype=torch.int32, device=dev)
     out_score = torch.empty(wl.B, Lmax, device=dev)
-    ctx.pkv_score_topk(torch.from_numpy(qc).to(dev), float(tq), torch.from_numpy(w).to(dev), ic,
-                       i32(wl.page_table), i32(wl.seq_len), k, out_idx, out_score)
+    wd, pt, sl = torch.from_numpy(w).to(dev), i32(wl.page_table), i32(wl.seq_len)
+    if quantize_on_device:
+        # the library's FP8 encode feeds the scoring launch directly: same stream,
+        # no synchronization in between (dependent launch keeps the order)
+        qf_dev = torch.from_numpy(np.ascontiguousarray(qf, np.float32)).to(dev)
+        torch.cuda.synchronize()
+        q_dev = torch.empty(qc.shape, dtype=torch.uint8, device=dev)
+        P.pkv_quantize_fp8(qf_dev, float(tq), q_dev)
+    else:
+        q_dev = torch.from_numpy(qc).to(dev)
+    ctx.pkv_score_topk(q_dev, float(tq), wd, ic, pt, sl, k, out_idx, out_score)
     torch.cuda.synchronize()
     assert ctx.pkv_get_error() == P.OK
+    if quantize_on_device:
+        assert np.array_equal(q_dev.cpu().numpy(), qc), "device FP8 encode differs from the oracle's"
     gi, gs = out_idx.cpu().numpy(), out_score.cpu().numpy()
     for b in range(wl.B):
         L = int(wl.seq_len[b])
@@ -120,3 +131,11 @@ def test_score_queries_of_every_magnitude():
     qc[1, :, :16] = 0xFE                   # -448 in block 0 of every head
     qc[2] = 0                              # zero query: every score is exactly 0
     _index_case(wl, 200, qc_override=(qc, np.float32(0.0125)))
+
+
+def test_score_reads_queries_encoded_just_before_on_the_stream():
+    """FP8 index queries encoded by the library on the device and scored by the
+    next call on the same stream without a synchronization: the codes equal the
+    oracle's bit for bit and the scores and top-k match the oracle."""
+    wl = W.make_dense("qdev", 24, 3, 64, 512, [5000, 2100, 900])
+    _index_case(wl, 300, quantize_on_device=True)
