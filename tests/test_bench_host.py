@@ -1,5 +1,5 @@
 """Host-side pieces of the benchmark and of the GPU tests' checkers (no GPU):
-the needed-bytes accounting against a hand count, the comment-insensitive
+the needed-bytes accounting against a hand count, the L2 flush, the comment-insensitive
 code hash that keys committed DRAM captures, the FP8 interval check used by the
 fused-decode parity tests, and the JSON line of the reference arm."""
 import json
@@ -85,3 +85,17 @@ def test_every_bench_workload_builds_and_is_described():
         assert total > 0 and tokens >= 0, name
         bench._WL.pop(name, None)
     assert set(bench.FUSED) <= set(bench.WORKLOADS)
+
+
+def test_l2_flush_writes_then_reads_twice_the_l2():
+    """The flush before a timed step writes one buffer and then reads another, each
+    at least twice the 129 MB L2, so no line of the step stays resident and the
+    lines left behind are clean; the config string says so."""
+    import torch
+    f = bench.L2Flush(torch.device("cpu"))
+    assert f.w.numel() * f.w.element_size() >= 2 * bench.L2_BYTES
+    assert f.r.numel() * f.r.element_size() >= 2 * bench.L2_BYTES
+    assert f.w.data_ptr() != f.r.data_ptr()
+    f()
+    assert int(f.w[0]) == 1 and int(f.w[-1]) == 1
+    assert "written" in bench.L2Flush.DESC and "read" in bench.L2Flush.DESC
